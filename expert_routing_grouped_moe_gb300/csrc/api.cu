@@ -1,0 +1,497 @@
+// C ABI of the MoE-LoRA expert layer: argument checks, tensor-map encoding and
+// kernel launches.  No call here allocates device memory or synchronises,
+// except moe_status().  See include/moe_gb300.h for the contract of each call.
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+#include <string>
+
+#include "../../include/moe_gb300.h"
+#include "internal.h"
+
+namespace moe {
+
+// Per-device status word: kernels record data errors (bad expert ids) and
+// pipeline timeouts here; moe_status() reads and clears it.
+static __device__ int g_status_word;
+
+namespace {
+
+thread_local std::string t_err;
+
+int fail(int code, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof(buf), fmt, ap);
+  va_end(ap);
+  t_err = buf;
+  return code;
+}
+int ok() {
+  t_err.clear();
+  return MOE_OK;
+}
+int cuda_fail(cudaError_t e, const char* where) {
+  return fail(MOE_ERR_CUDA, "%s: %s", where, cudaGetErrorString(e));
+}
+
+struct DevState {
+  bool init = false;
+  int* status = nullptr;
+  int num_sms = 0;
+};
+constexpr int kMaxDevices = 64;
+DevState g_dev[kMaxDevices];
+std::mutex g_mu;
+
+// Status-word address and SM count of the current device (looked up once).
+int device_state(DevState** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  if (dev < 0 || dev >= kMaxDevices) return fail(MOE_ERR_UNSUPPORTED, "device index %d", dev);
+  std::lock_guard<std::mutex> lk(g_mu);
+  DevState& st = g_dev[dev];
+  if (!st.init) {
+    void* ptr = nullptr;
+    e = cudaGetSymbolAddress(&ptr, g_status_word);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(status)");
+    int sms = 0;
+    e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceGetAttribute");
+    st.status = static_cast<int*>(ptr);
+    st.num_sms = sms;
+    st.init = true;
+  }
+  *out = &st;
+  return MOE_OK;
+}
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+EncodeTiledFn g_encode = nullptr;
+std::once_flag g_encode_once;
+
+EncodeTiledFn encode_fn() {
+  std::call_once(g_encode_once, [] {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      g_encode = reinterpret_cast<EncodeTiledFn>(fn);
+  });
+  return g_encode;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int64_t padded_rows_max(int64_t T, int64_t K, int64_t G) {
+  const int64_t n = T * K + G * (kTileM - 1);
+  return (n + kTileM - 1) / kTileM * kTileM;
+}
+
+int check_dims(const moe_dims* dm) {
+  if (dm == nullptr) return fail(MOE_ERR_INVALID_ARG, "dims is NULL");
+  if (dm->T <= 0 || dm->d <= 0 || dm->f <= 0 || dm->E <= 0 || dm->k <= 0 || dm->r <= 0)
+    return fail(MOE_ERR_INVALID_ARG, "T, d, f, E, k, r must be positive");
+  if (dm->shared_expert != 0 && dm->shared_expert != 1)
+    return fail(MOE_ERR_INVALID_ARG, "shared_expert must be 0 or 1");
+  if (dm->k > dm->E) return fail(MOE_ERR_INVALID_ARG, "k=%d > E=%d", dm->k, dm->E);
+  if (dm->E > kMaxExperts) return fail(MOE_ERR_UNSUPPORTED, "E=%d > %d", dm->E, kMaxExperts);
+  if (dm->k > 32) return fail(MOE_ERR_UNSUPPORTED, "k=%d > 32", dm->k);
+  if (dm->d % 8 || dm->f % 8 || dm->r % 8)
+    return fail(MOE_ERR_INVALID_ARG, "d, f and r must be multiples of 8");
+  if (dm->r > 64) return fail(MOE_ERR_UNSUPPORTED, "LoRA rank r=%d > 64", dm->r);
+  const int64_t K = dm->k + dm->shared_expert, G = dm->E + dm->shared_expert;
+  if (padded_rows_max(dm->T, K, G) >= (int64_t(1) << 31))
+    return fail(MOE_ERR_UNSUPPORTED, "too many routed rows");
+  return MOE_OK;
+}
+
+#define MOE_CHECK_PTR(p)                                                          \
+  do {                                                                            \
+    if ((p) == nullptr) return fail(MOE_ERR_INVALID_ARG, "%s is NULL", #p);       \
+    if (!aligned16(p)) return fail(MOE_ERR_INVALID_ARG, "%s not 16-byte aligned", #p); \
+  } while (0)
+
+}  // namespace
+
+bool make_map_2d(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols,
+                 uint32_t box_rows, uint32_t box_cols) {
+  EncodeTiledFn fn = encode_fn();
+  if (fn == nullptr) return false;
+  const cuuint64_t dims[2] = {cols, rows};
+  const cuuint64_t strides[1] = {cols * 2};
+  const cuuint32_t box[2] = {box_cols, box_rows};
+  const cuuint32_t es[2] = {1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box,
+            es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool make_map_3d(CUtensorMap* m, const void* base, uint64_t G, uint64_t rows, uint64_t cols,
+                 uint32_t box_rows, uint32_t box_cols) {
+  EncodeTiledFn fn = encode_fn();
+  if (fn == nullptr) return false;
+  const cuuint64_t dims[3] = {cols, rows, G};
+  const cuuint64_t strides[2] = {cols * 2, rows * cols * 2};
+  const cuuint32_t box[3] = {box_cols, box_rows, 1};
+  const cuuint32_t es[3] = {1, 1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box,
+            es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+namespace {
+
+struct BwdWs {
+  uint16_t *us, *uw, *xw, *vs, *dh;  // hi/lo pair buffers
+  float* dwp;
+  size_t bytes;
+};
+
+size_t align_up(size_t x) { return (x + 1023) & ~size_t(1023); }
+
+BwdWs bwd_layout(const moe_dims* dm, void* base) {
+  const int64_t K = dm->k + dm->shared_expert, G = dm->E + dm->shared_expert;
+  const size_t P = static_cast<size_t>(padded_rows_max(dm->T, K, G));
+  const size_t nr = align_up(2 * P * dm->r * 2);
+  const size_t ndh = align_up(2 * P * 2 * static_cast<size_t>(dm->f) * 2);
+  const size_t nparts = (dm->f + 255) / 256;
+  const size_t ndw = align_up(nparts * P * 4);
+  BwdWs w{};
+  uint8_t* b = static_cast<uint8_t*>(base);
+  size_t o = 0;
+  w.us = reinterpret_cast<uint16_t*>(b + o); o += nr;
+  w.uw = reinterpret_cast<uint16_t*>(b + o); o += nr;
+  w.xw = reinterpret_cast<uint16_t*>(b + o); o += nr;
+  w.vs = reinterpret_cast<uint16_t*>(b + o); o += nr;
+  w.dh = reinterpret_cast<uint16_t*>(b + o); o += ndh;
+  w.dwp = reinterpret_cast<float*>(b + o); o += ndw;
+  w.bytes = o;
+  return w;
+}
+
+GemmParams base_params(const moe_dims* dm, const int32_t* offsets, const int32_t* tile_off,
+                       const int32_t* sorted_src, const float* topk_w, int* status) {
+  GemmParams p;
+  std::memset(&p, 0, sizeof(p));
+  p.G = dm->E + dm->shared_expert;
+  p.k = dm->k;
+  p.K = dm->k + dm->shared_expert;
+  p.scale = dm->lora_scale;
+  p.tile_off = tile_off;
+  p.offsets = offsets;
+  p.sorted_src = sorted_src;
+  p.topk_w = topk_w;
+  p.status = status;
+  return p;
+}
+
+int run_gemm(const GemmShape& sh, GemmParams& p, int64_t P, int num_sms, cudaStream_t s,
+             const char* what) {
+  if (!sh.wgrad) p.max_tiles = static_cast<int>(P / kTileM) * p.n_ntiles;
+  cudaError_t e = launch_gemm(sh, p, num_sms, s);
+  if (e != cudaSuccess) return cuda_fail(e, what);
+  return MOE_OK;
+}
+
+#define MAP2(dst, ptr, rows, cols, br, bc)                                         \
+  do {                                                                             \
+    if (!make_map_2d(&(dst), (ptr), (rows), (cols), (br), (bc)))                   \
+      return fail(MOE_ERR_CUDA, "tensor map encode failed (%s)", #ptr);            \
+  } while (0)
+#define MAP3(dst, ptr, g, rows, cols, br, bc)                                      \
+  do {                                                                             \
+    if (!make_map_3d(&(dst), (ptr), (g), (rows), (cols), (br), (bc)))              \
+      return fail(MOE_ERR_CUDA, "tensor map encode failed (%s)", #ptr);            \
+  } while (0)
+
+#define SLICE(p, i, amap_ptr, amap_rows, amap_cols, bexpr, kext)                  \
+  do {                                                                           \
+    MAP2((p).sl[i].a, (amap_ptr), (amap_rows), (amap_cols), 128, 64);            \
+    bexpr;                                                                       \
+    (p).sl[i].K = (kext);                                                        \
+  } while (0)
+
+}  // namespace
+}  // namespace moe
+
+using namespace moe;
+
+extern "C" {
+
+int moe_abi_version(void) { return 1; }
+
+const char* moe_last_error(void) { return t_err.c_str(); }
+
+int64_t moe_padded_rows_max(int32_t T, int32_t K, int32_t G) {
+  if (T <= 0 || K <= 0 || G <= 0) return -1;
+  return padded_rows_max(T, K, G);
+}
+
+size_t moe_route_workspace_size(int32_t T, int32_t K, int32_t G) {
+  if (T <= 0 || K <= 0 || G <= 0) return 0;
+  return route_ws_bytes(static_cast<int64_t>(T) * K, G);
+}
+
+int moe_status(moe_stream_t stream) {
+  DevState* st = nullptr;
+  int rc = device_state(&st);
+  if (rc) return rc;
+  int v = 0;
+  cudaError_t e = cudaMemcpyAsync(&v, st->status, sizeof(int), cudaMemcpyDeviceToHost, stream);
+  if (e == cudaSuccess) e = cudaMemsetAsync(st->status, 0, sizeof(int), stream);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(stream);
+  if (e != cudaSuccess) return cuda_fail(e, "moe_status");
+  if (v != 0) return fail(v, "device status %d", v);
+  return ok();
+}
+
+int moe_router_topk(const float* logits, int32_t T, int32_t E, int32_t k, int32_t* ids,
+                    float* weights, moe_stream_t stream) {
+  if (logits == nullptr || ids == nullptr || weights == nullptr)
+    return fail(MOE_ERR_INVALID_ARG, "NULL pointer");
+  if (T <= 0 || E <= 0 || k <= 0 || k > E) return fail(MOE_ERR_INVALID_ARG, "bad T/E/k");
+  if (E > kMaxExperts || k > 32) return fail(MOE_ERR_UNSUPPORTED, "E > 1024 or k > 32");
+  cudaError_t e = launch_router_topk(logits, T, E, k, ids, weights, stream);
+  if (e != cudaSuccess) return cuda_fail(e, "router_topk launch");
+  return ok();
+}
+
+int moe_route(const int32_t* ids, int32_t T, int32_t k, int32_t E, int32_t shared_expert,
+              int32_t* counts, int32_t* offsets, int32_t* tile_off, int32_t* sorted_src,
+              int32_t* dest_pos, void* ws, size_t ws_bytes, moe_stream_t stream) {
+  if (!ids || !counts || !offsets || !tile_off || !sorted_src || !dest_pos || !ws)
+    return fail(MOE_ERR_INVALID_ARG, "NULL pointer");
+  if (T <= 0 || k <= 0 || E <= 0 || (shared_expert != 0 && shared_expert != 1))
+    return fail(MOE_ERR_INVALID_ARG, "bad T/k/E/shared_expert");
+  if (k > E) return fail(MOE_ERR_INVALID_ARG, "k=%d > E=%d", k, E);
+  if (E > kMaxExperts || k > 32) return fail(MOE_ERR_UNSUPPORTED, "E > 1024 or k > 32");
+  const int64_t K = k + shared_expert, G = E + shared_expert;
+  if (padded_rows_max(T, K, G) >= (int64_t(1) << 31))
+    return fail(MOE_ERR_UNSUPPORTED, "too many routed rows");
+  if (!aligned16(ws)) return fail(MOE_ERR_INVALID_ARG, "ws not 16-byte aligned");
+  if (ws_bytes < moe_route_workspace_size(T, static_cast<int32_t>(K), static_cast<int32_t>(G)))
+    return fail(MOE_ERR_WORKSPACE, "route workspace too small");
+  DevState* st = nullptr;
+  int rc = device_state(&st);
+  if (rc) return rc;
+  cudaError_t e = launch_route(ids, T, k, E, shared_expert, counts, offsets, tile_off,
+                               sorted_src, dest_pos, static_cast<int32_t*>(ws), st->status,
+                               stream);
+  if (e != cudaSuccess) return cuda_fail(e, "route launch");
+  return ok();
+}
+
+int moe_permute(const moe_bf16* src, int32_t T, int32_t d, int32_t K, int32_t G,
+                const int32_t* offsets, const int32_t* tile_off, const int32_t* sorted_src,
+                moe_bf16* dst, moe_stream_t stream) {
+  MOE_CHECK_PTR(src);
+  MOE_CHECK_PTR(dst);
+  if (!offsets || !tile_off || !sorted_src) return fail(MOE_ERR_INVALID_ARG, "NULL pointer");
+  if (T <= 0 || d <= 0 || K <= 0 || G <= 0) return fail(MOE_ERR_INVALID_ARG, "bad sizes");
+  if (d % 8) return fail(MOE_ERR_INVALID_ARG, "d must be a multiple of 8");
+  if (G > kMaxExperts + 1) return fail(MOE_ERR_UNSUPPORTED, "too many groups");
+  const int64_t P = padded_rows_max(T, K, G);
+  if (P >= (int64_t(1) << 31)) return fail(MOE_ERR_UNSUPPORTED, "too many routed rows");
+  cudaError_t e =
+      launch_permute(src, T, d, K, G, offsets, tile_off, sorted_src, dst, P, stream);
+  if (e != cudaSuccess) return cuda_fail(e, "permute launch");
+  return ok();
+}
+
+int moe_unpermute_combine(const moe_bf16* rows, const int32_t* ids, const int32_t* dest_pos,
+                          const int32_t* offsets, const int32_t* tile_off, int32_t T, int32_t d,
+                          int32_t k, int32_t E, int32_t shared_expert, const float* weights,
+                          const float* row_scalars, float* slot_out, moe_bf16* out,
+                          moe_stream_t stream) {
+  MOE_CHECK_PTR(rows);
+  MOE_CHECK_PTR(out);
+  if (!ids || !dest_pos || !offsets || !tile_off) return fail(MOE_ERR_INVALID_ARG, "NULL pointer");
+  if (T <= 0 || d <= 0 || k <= 0 || E <= 0 || (shared_expert != 0 && shared_expert != 1))
+    return fail(MOE_ERR_INVALID_ARG, "bad sizes");
+  if (d % 8) return fail(MOE_ERR_INVALID_ARG, "d must be a multiple of 8");
+  if (k > 32 || E > kMaxExperts) return fail(MOE_ERR_UNSUPPORTED, "k > 32 or E > 1024");
+  if ((row_scalars == nullptr) != (slot_out == nullptr))
+    return fail(MOE_ERR_INVALID_ARG, "row_scalars and slot_out go together");
+  cudaError_t e = launch_combine(rows, ids, dest_pos, offsets, tile_off, T, d, k, E,
+                                 shared_expert, weights, row_scalars, slot_out, out, stream);
+  if (e != cudaSuccess) return cuda_fail(e, "combine launch");
+  return ok();
+}
+
+int moe_lora_grouped_mlp_fwd(const moe_dims* dims, const moe_bf16* Xp, const int32_t* counts,
+                             const int32_t* offsets, const int32_t* tile_off,
+                             const int32_t* sorted_src, const float* topk_w,
+                             const moe_bf16* W_gu, const moe_bf16* A_gu, const moe_bf16* B_gu,
+                             const moe_bf16* W_dn, const moe_bf16* A_dn, const moe_bf16* B_dn,
+                             moe_bf16* Yp, float* h, moe_bf16* act, moe_bf16* xa_gu,
+                             moe_bf16* xa_dn, moe_stream_t stream) {
+  (void)counts;
+  int rc = check_dims(dims);
+  if (rc) return rc;
+  MOE_CHECK_PTR(Xp);
+  MOE_CHECK_PTR(W_gu); MOE_CHECK_PTR(A_gu); MOE_CHECK_PTR(B_gu);
+  MOE_CHECK_PTR(W_dn); MOE_CHECK_PTR(A_dn); MOE_CHECK_PTR(B_dn);
+  MOE_CHECK_PTR(Yp); MOE_CHECK_PTR(h); MOE_CHECK_PTR(act); MOE_CHECK_PTR(xa_gu);
+  MOE_CHECK_PTR(xa_dn);
+  if (!offsets || !tile_off || !sorted_src || !topk_w)
+    return fail(MOE_ERR_INVALID_ARG, "NULL routing pointer");
+  DevState* st = nullptr;
+  rc = device_state(&st);
+  if (rc) return rc;
+  const int d = dims->d, f = dims->f, r = dims->r;
+  const int G = dims->E + dims->shared_expert;
+  const int64_t P = padded_rows_max(dims->T, dims->k + dims->shared_expert, G);
+  const GemmParams base = base_params(dims, offsets, tile_off, sorted_src, topk_w, st->status);
+  cudaStream_t s = stream;
+
+  const int64_t Pf = P * f, Pr = P * r;
+  {  // xa_gu pair = s * Xp A_gu^T
+    GemmParams p = base;
+    SLICE(p, 0, Xp, P, d, MAP3(p.sl[0].b, A_gu, G, r, d, 64, 64), d);
+    p.nslices = 1; p.N = r; p.n_ntiles = (r + 63) / 64; p.out0 = xa_gu; p.ld0 = r; p.pair = Pr;
+    if ((rc = run_gemm({64, false, false, Epi::kLoRA}, p, P, st->num_sms, s, "xa_gu"))) return rc;
+  }
+  {  // h = Xp W_gu^T + (s xa) B_gu^T (fp32) ; act pair = silu(gate) * up
+    GemmParams p = base;
+    SLICE(p, 0, Xp, P, d, MAP3(p.sl[0].b, W_gu, G, 2 * f, d, 128, 64), d);
+    SLICE(p, 1, xa_gu, P, r, MAP3(p.sl[1].b, B_gu, G, 2 * f, r, 128, 64), r);
+    SLICE(p, 2, xa_gu + Pr, P, r, MAP3(p.sl[2].b, B_gu, G, 2 * f, r, 128, 64), r);
+    p.nslices = 3; p.N = f; p.n_ntiles = (f + 127) / 128; p.b_split = f;
+    p.fout = h; p.ld0 = 2 * f; p.out0 = act; p.pair = Pf;
+    if ((rc = run_gemm({256, false, false, Epi::kSwiGLU}, p, P, st->num_sms, s, "gate_up")))
+      return rc;
+  }
+  {  // xa_dn pair = s * act A_dn^T   (act = hi + lo)
+    GemmParams p = base;
+    SLICE(p, 0, act, P, f, MAP3(p.sl[0].b, A_dn, G, r, f, 64, 64), f);
+    SLICE(p, 1, act + Pf, P, f, MAP3(p.sl[1].b, A_dn, G, r, f, 64, 64), f);
+    p.nslices = 2; p.N = r; p.n_ntiles = (r + 63) / 64; p.out0 = xa_dn; p.ld0 = r; p.pair = Pr;
+    if ((rc = run_gemm({64, false, false, Epi::kLoRA}, p, P, st->num_sms, s, "xa_dn"))) return rc;
+  }
+  {  // Yp = w * (act W_dn^T + (s xa_dn) B_dn^T)
+    GemmParams p = base;
+    SLICE(p, 0, act, P, f, MAP3(p.sl[0].b, W_dn, G, d, f, 256, 64), f);
+    SLICE(p, 1, xa_dn, P, r, MAP3(p.sl[1].b, B_dn, G, d, r, 256, 64), r);
+    p.nslices = 2; p.N = d; p.n_ntiles = (d + 255) / 256; p.out0 = Yp; p.ld0 = d;
+    if ((rc = run_gemm({256, false, false, Epi::kScaleW}, p, P, st->num_sms, s, "down")))
+      return rc;
+  }
+  return ok();
+}
+
+size_t moe_mlp_bwd_workspace_size(const moe_dims* dims) {
+  if (check_dims(dims)) return 0;
+  return bwd_layout(dims, nullptr).bytes;
+}
+
+int moe_lora_grouped_mlp_bwd(const moe_dims* dims, const moe_bf16* dYp, const moe_bf16* Xp,
+                             const int32_t* counts, const int32_t* offsets,
+                             const int32_t* tile_off, const int32_t* sorted_src,
+                             const float* topk_w, const moe_bf16* W_gu, const moe_bf16* A_gu,
+                             const moe_bf16* B_gu, const moe_bf16* W_dn, const moe_bf16* A_dn,
+                             const moe_bf16* B_dn, const float* h, const moe_bf16* act,
+                             const moe_bf16* xa_gu, const moe_bf16* xa_dn, moe_bf16* dXp,
+                             float* dw_rows, float* dA_gu, float* dB_gu, float* dA_dn,
+                             float* dB_dn, void* ws, size_t ws_bytes, moe_stream_t stream) {
+  (void)counts;
+  int rc = check_dims(dims);
+  if (rc) return rc;
+  MOE_CHECK_PTR(dYp); MOE_CHECK_PTR(Xp);
+  MOE_CHECK_PTR(W_gu); MOE_CHECK_PTR(A_gu); MOE_CHECK_PTR(B_gu);
+  MOE_CHECK_PTR(W_dn); MOE_CHECK_PTR(A_dn); MOE_CHECK_PTR(B_dn);
+  MOE_CHECK_PTR(h); MOE_CHECK_PTR(act); MOE_CHECK_PTR(xa_gu); MOE_CHECK_PTR(xa_dn);
+  MOE_CHECK_PTR(dXp); MOE_CHECK_PTR(dw_rows);
+  MOE_CHECK_PTR(dA_gu); MOE_CHECK_PTR(dB_gu); MOE_CHECK_PTR(dA_dn); MOE_CHECK_PTR(dB_dn);
+  MOE_CHECK_PTR(ws);
+  if (!offsets || !tile_off || !sorted_src || !topk_w)
+    return fail(MOE_ERR_INVALID_ARG, "NULL routing pointer");
+  const BwdWs w = bwd_layout(dims, ws);
+  if (ws_bytes < w.bytes) return fail(MOE_ERR_WORKSPACE, "bwd workspace too small");
+  DevState* st = nullptr;
+  rc = device_state(&st);
+  if (rc) return rc;
+  const int d = dims->d, f = dims->f, r = dims->r;
+  const int G = dims->E + dims->shared_expert;
+  const int64_t P = padded_rows_max(dims->T, dims->k + dims->shared_expert, G);
+  const GemmParams base = base_params(dims, offsets, tile_off, sorted_src, topk_w, st->status);
+  cudaStream_t s = stream;
+  const int nparts = (f + 255) / 256;
+
+  const int64_t Pr = P * r, P2f = P * 2 * f;
+  {  // u = dYp B_dn -> pairs us = s*u, uw = s*w*u, xw = w * (s xa_dn)
+    GemmParams p = base;
+    SLICE(p, 0, dYp, P, d, MAP3(p.sl[0].b, B_dn, G, d, r, 64, 64), d);
+    p.nslices = 1; p.N = r; p.n_ntiles = (r + 63) / 64; p.ld0 = r; p.pair = Pr;
+    p.out0 = w.us; p.out1 = w.uw; p.out2 = w.xw; p.aux0 = xa_dn;
+    if ((rc = run_gemm({64, true, false, Epi::kLoRA}, p, P, st->num_sms, s, "u"))) return rc;
+  }
+  {  // g = dYp W_dn + us A_dn ; SwiGLU backward from fp32 h -> dh pair ; dw partials
+    GemmParams p = base;
+    SLICE(p, 0, dYp, P, d, MAP3(p.sl[0].b, W_dn, G, d, f, 64, 64), d);
+    SLICE(p, 1, w.us, P, r, MAP3(p.sl[1].b, A_dn, G, r, f, 64, 64), r);
+    SLICE(p, 2, w.us + Pr, P, r, MAP3(p.sl[2].b, A_dn, G, r, f, 64, 64), r);
+    p.nslices = 3; p.N = f; p.n_ntiles = nparts;
+    p.fin = h; p.out0 = w.dh; p.ld0 = 2 * f; p.pair = P2f; p.fout = w.dwp; p.fstride = P;
+    if ((rc = run_gemm({256, true, false, Epi::kDgradDn}, p, P, st->num_sms, s, "dgrad_dn")))
+      return rc;
+  }
+  {  // v = dh B_gu (dh = hi + lo) -> vs pair = s*v
+    GemmParams p = base;
+    SLICE(p, 0, w.dh, P, 2 * f, MAP3(p.sl[0].b, B_gu, G, 2 * f, r, 64, 64), 2 * f);
+    SLICE(p, 1, w.dh + P2f, P, 2 * f, MAP3(p.sl[1].b, B_gu, G, 2 * f, r, 64, 64), 2 * f);
+    p.nslices = 2; p.N = r; p.n_ntiles = (r + 63) / 64; p.ld0 = r; p.pair = Pr; p.out0 = w.vs;
+    if ((rc = run_gemm({64, true, false, Epi::kLoRA}, p, P, st->num_sms, s, "v"))) return rc;
+  }
+  {  // dXp = dh W_gu + vs A_gu   (high halves: dX is an output, not a row reduction)
+    GemmParams p = base;
+    SLICE(p, 0, w.dh, P, 2 * f, MAP3(p.sl[0].b, W_gu, G, 2 * f, d, 64, 64), 2 * f);
+    SLICE(p, 1, w.vs, P, r, MAP3(p.sl[1].b, A_gu, G, r, d, 64, 64), r);
+    p.nslices = 2; p.N = d; p.n_ntiles = (d + 255) / 256; p.out0 = dXp; p.ld0 = d;
+    if ((rc = run_gemm({256, true, false, Epi::kStore}, p, P, st->num_sms, s, "dgrad_gu")))
+      return rc;
+  }
+  // per-group LoRA gradients: sum over the group's rows of A^T [B_hi | B_lo],
+  // A from one exact bf16 source or a hi/lo pair
+  struct WgradJob {
+    const moe_bf16* a;
+    int a_pair;  // 1: a is a hi/lo pair buffer
+    int M;
+    const uint16_t* b;  // hi/lo pair buffer [2, P, r]
+    float* out;
+    int transpose;
+    const char* name;
+  };
+  const WgradJob jobs[4] = {
+      {dYp, 0, d, w.xw, dB_dn, 0, "dB_dn"},
+      {act, 1, f, w.uw, dA_dn, 1, "dA_dn"},
+      {w.dh, 1, 2 * f, xa_gu, dB_gu, 0, "dB_gu"},
+      {Xp, 0, d, w.vs, dA_gu, 1, "dA_gu"},
+  };
+  for (const WgradJob& j : jobs) {
+    GemmParams p = base;
+    MAP2(p.sl[0].a, j.a, P, j.M, 64, 64);
+    p.nslices = 1;
+    if (j.a_pair) {
+      MAP2(p.sl[1].a, j.a + P * static_cast<int64_t>(j.M), P, j.M, 64, 64);
+      p.nslices = 2;
+    }
+    MAP2(p.wb_hi, j.b, P, r, 64, 64);
+    MAP2(p.wb_lo, j.b + Pr, P, r, 64, 64);
+    p.M = j.M; p.N = r; p.n_ntiles = (j.M + 127) / 128;
+    p.fout = j.out; p.fstride = static_cast<int64_t>(j.M) * r; p.transpose_out = j.transpose;
+    if ((rc = run_gemm({128, true, true, Epi::kWgrad}, p, P, st->num_sms, s, j.name))) return rc;
+  }
+  cudaError_t e = launch_sum_parts(w.dwp, nparts, P, P, dw_rows, s);
+  if (e != cudaSuccess) return cuda_fail(e, "dw reduce");
+  return ok();
+}
+
+}  // extern "C"

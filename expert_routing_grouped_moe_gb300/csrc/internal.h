@@ -1,0 +1,120 @@
+// Internal interfaces between the C-ABI layer (api.cu) and the kernel
+// translation units.  Host-side only; nothing here is exported.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+namespace moe {
+
+constexpr int kTileM = 128;            // rows per M tile (= permuted layout granularity)
+constexpr int kMaxExperts = 1024;      // routed experts supported
+constexpr uint64_t kWaitTimeoutNs = 4000000000ull;  // pipeline waits give up after 4 s
+
+// Error codes recorded in the device status word (same values as moe_status_t).
+constexpr int kErrBadIds = -5;
+constexpr int kErrTimeout = -6;
+
+// ---- routing (route.cu) ----------------------------------------------------
+constexpr int kRouteThreads = 256;                  // 8 warps per CTA
+constexpr int kRouteWarps = kRouteThreads / 32;
+constexpr int kRoutePerLane = 8;                    // assignments per lane
+constexpr int kRouteChunk = kRouteThreads * kRoutePerLane;  // assignments per CTA
+
+inline int route_ctas(int64_t n) { return static_cast<int>((n + kRouteChunk - 1) / kRouteChunk); }
+inline size_t route_ws_bytes(int64_t n, int G) {
+  // per-(group, CTA) histogram, int32
+  return static_cast<size_t>(G) * static_cast<size_t>(route_ctas(n > 0 ? n : 1)) * 4u;
+}
+
+cudaError_t launch_router_topk(const float* logits, int T, int E, int k, int32_t* ids,
+                               float* w, cudaStream_t s);
+cudaError_t launch_route(const int32_t* ids, int T, int k, int E, int shared, int32_t* counts,
+                         int32_t* offsets, int32_t* tile_off, int32_t* sorted_src,
+                         int32_t* dest_pos, int32_t* hist, int* status, cudaStream_t s);
+
+// ---- row gather / combine (rows.cu) ------------------------------------------
+cudaError_t launch_permute(const uint16_t* src, int T, int d, int K, int G,
+                           const int32_t* offsets, const int32_t* tile_off,
+                           const int32_t* sorted_src, uint16_t* dst, int64_t max_rows,
+                           cudaStream_t s);
+cudaError_t launch_combine(const uint16_t* rows, const int32_t* ids, const int32_t* dest_pos,
+                           const int32_t* offsets, const int32_t* tile_off, int T, int d, int k,
+                           int E, int shared, const float* weights, const float* row_scalars,
+                           float* slot_out, uint16_t* out, cudaStream_t s);
+cudaError_t launch_sum_parts(const float* parts, int nparts, int64_t stride, int64_t n,
+                             float* out, cudaStream_t s);
+
+// ---- grouped GEMMs (gemm.cu) -------------------------------------------------
+// Derived intermediates that feed a reduction over rows (the LoRA weight
+// gradients, the routing-weight gradient) are carried as a pair of bf16
+// values hi + lo (hi = bf16(v), lo = bf16(v - hi)), ~16 significant bits; a
+// pair buffer holds hi at [0, P*cols) and lo at [P*cols, 2*P*cols).
+enum class Epi : int {
+  kSwiGLU = 0,   // h = acc (fp32, gate|up halves), act = silu(gate)*up as a hi/lo pair
+  kScaleW = 1,   // out0 = bf16(w_row * acc)
+  kStore = 2,    // out0 = bf16(acc)
+  kLoRA = 3,     // pairs: out0 = s*acc; out1 = s*w*acc; out2 = w*(aux0 hi + lo)
+  kDgradDn = 4,  // SwiGLU backward from fp32 h (fin): dh pair (out0), dw partial (fout)
+  kWgrad = 5,    // fp32 per-group weight gradient: acc[:, n] + acc[:, 64 + n]
+};
+
+constexpr int kMaxSlices = 4;
+
+// One K-slice of a contraction: D += A_slice * B_slice^T over K columns.
+struct GemmSlice {
+  CUtensorMap a;
+  CUtensorMap b;
+  int K;
+};
+
+struct GemmParams {
+  GemmSlice sl[kMaxSlices];  // rows mode: A/B per slice; wgrad: A sources (hi, lo)
+  CUtensorMap wb_hi, wb_lo;  // wgrad: B operand hi / lo (columns [0,64) / [64,128))
+  int nslices;
+  int N;              // valid output columns (rows mode) / LoRA rank r (wgrad)
+  int M;              // wgrad: rows of the weight gradient (d, f or 2f)
+  int n_ntiles;       // N tiles per M tile (rows mode) / M tiles per group (wgrad)
+  int b_split;        // rows offset of the second B half (gate/up pairing), 0 = none
+  int G, k, K;        // groups, top-k, slots per token
+  float scale;        // LoRA scale s
+  const int32_t* tile_off;
+  const int32_t* offsets;
+  const int32_t* sorted_src;
+  const float* topk_w;
+  uint16_t* out0;
+  uint16_t* out1;
+  uint16_t* out2;
+  const uint16_t* aux0;
+  float* fout;        // fp32 output: h (SwiGLU), dw partials (dgrad), weight grad (wgrad)
+  const float* fin;   // fp32 input: h (dgrad)
+  int64_t ld0;        // leading dimension (elements) of out*/aux0 rows
+  int64_t pair;       // element offset from the hi to the lo half of a pair buffer
+  int64_t fstride;    // stride between dw partial slices, or group stride of fout
+  int transpose_out;  // wgrad: write fout[g][n][m] instead of fout[g][m][n]
+  int max_tiles;      // upper bound of tiles (host-known), rows mode
+  int* status;
+};
+
+// Kernel shapes: BN in {64, 128, 256}; B operand K-major or MN-major; two modes.
+struct GemmShape {
+  int BN;
+  bool b_mn;
+  bool wgrad;  // wgrad: A and B both MN-major, K = group rows
+  Epi epi;
+};
+
+cudaError_t launch_gemm(const GemmShape& shape, const GemmParams& p, int num_sms,
+                        cudaStream_t s);
+
+// ---- tensor maps (api.cu) ----------------------------------------------------
+// 2D bf16 map over [rows, cols] row-major; box (box_cols, box_rows); 128B swizzle.
+bool make_map_2d(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols,
+                 uint32_t box_rows, uint32_t box_cols);
+// 3D bf16 map over [G, rows, cols]; box (box_cols, box_rows, 1); 128B swizzle.
+bool make_map_3d(CUtensorMap* m, const void* base, uint64_t G, uint64_t rows, uint64_t cols,
+                 uint32_t box_rows, uint32_t box_cols);
+
+}  // namespace moe

@@ -1,0 +1,123 @@
+"""MoE-LoRA expert layer object: owns the device buffers, calls the C ABI.
+
+``MoELoRALayer`` is a convenience wrapper over the library's calls for one
+layer shape: it allocates every buffer once (torch device memory), then
+``forward`` runs route -> permute -> grouped split-LoRA SwiGLU MLP ->
+combine and ``backward`` runs the dY permute -> grouped backward -> combine
+of dX and of the routing-weight gradient.  All arithmetic happens in the CUDA
+library; this module only sequences calls and owns memory.
+"""
+from __future__ import annotations
+
+import torch
+
+from . import _lib as L
+
+# Kernel launches issued by one forward / one backward (every call below
+# launches a fixed number of kernels: route 3, permute 1, forward GEMMs 4,
+# combine 1; backward: permute 1, GEMMs 4 + weight-gradient GEMMs 4,
+# partial-sum 1, combine 1).
+LAUNCHES_FWD = 9
+LAUNCHES_BWD = 11
+
+
+class MoELoRALayer:
+    def __init__(self, T, d, f, E, k, r, alpha, weights: dict, shared_expert=False,
+                 device="cuda"):
+        self.dims = L.make_dims(T, d, f, E, k, r, alpha / r, shared_expert)
+        self.T, self.d, self.f, self.E, self.k, self.r = T, d, f, E, k, r
+        self.shared = bool(shared_expert)
+        self.G = E + (1 if shared_expert else 0)
+        self.K = k + (1 if shared_expert else 0)
+        self.N = T * self.K
+        self.P = L.moe_padded_rows_max(T, self.K, self.G)
+        dev = torch.device(device)
+        self.w = {n: weights[n].contiguous() for n in ("W_gu", "A_gu", "B_gu", "W_dn", "A_dn",
+                                                          "B_dn")}
+        i32 = dict(dtype=torch.int32, device=dev)
+        bf = dict(dtype=torch.bfloat16, device=dev)
+        f32 = dict(dtype=torch.float32, device=dev)
+        P, G = self.P, self.G
+        self.counts = torch.zeros(G, **i32)
+        self.offsets = torch.zeros(G + 1, **i32)
+        self.tile_off = torch.zeros(G + 1, **i32)
+        self.sorted_src = torch.zeros(self.N, **i32)
+        self.dest_pos = torch.zeros(self.N, **i32)
+        self.route_ws = torch.empty(max(16, L.moe_route_workspace_size(T, self.K, G)),
+                                    dtype=torch.uint8, device=dev)
+        self.Xp = torch.empty(P, d, **bf)
+        self.Yp = torch.empty(P, d, **bf)
+        # saved intermediates: h in fp32; act / xa_gu / xa_dn as hi+lo bf16 pairs
+        self.h = torch.empty(P, 2 * f, **f32)
+        self.act = torch.empty(2, P, f, **bf)
+        self.xa_gu = torch.empty(2, P, r, **bf)
+        self.xa_dn = torch.empty(2, P, r, **bf)
+        self.Y = torch.empty(T, d, **bf)
+        self.dYp = torch.empty(P, d, **bf)
+        self.dXp = torch.empty(P, d, **bf)
+        self.dw_rows = torch.empty(P, **f32)
+        self.dX = torch.empty(T, d, **bf)
+        self.dw = torch.empty(T, k, **f32)
+        self.grads = {
+            "dA_gu": torch.empty(G, r, d, **f32), "dB_gu": torch.empty(G, 2 * f, r, **f32),
+            "dA_dn": torch.empty(G, r, f, **f32), "dB_dn": torch.empty(G, d, r, **f32),
+        }
+        self.bwd_ws = torch.empty(L.moe_mlp_bwd_workspace_size(self.dims), dtype=torch.uint8,
+                                  device=dev)
+        self._ids = None
+        self._topk_w = None
+
+    # ------------------------------------------------------------------ steps
+    def route(self, ids, stream=None):
+        L.moe_route(ids, self.E, self.shared, self.counts, self.offsets, self.tile_off,
+                    self.sorted_src, self.dest_pos, self.route_ws, stream)
+
+    def forward(self, X, ids, topk_w, stream=None):
+        """Y [T,d] bf16 for token rows X [T,d], top-k ids [T,k], weights [T,k]."""
+        self._ids, self._topk_w = ids, topk_w
+        self.route(ids, stream)
+        L.moe_permute(X, self.K, self.G, self.offsets, self.tile_off, self.sorted_src, self.Xp,
+                      stream)
+        w = self.w
+        L.moe_lora_grouped_mlp_fwd(self.dims, self.Xp, self.counts, self.offsets, self.tile_off,
+                                   self.sorted_src, topk_w, w["W_gu"], w["A_gu"], w["B_gu"],
+                                   w["W_dn"], w["A_dn"], w["B_dn"], self.Yp, self.h, self.act,
+                                   self.xa_gu, self.xa_dn, stream)
+        L.moe_unpermute_combine(self.Yp, ids, self.dest_pos, self.offsets, self.tile_off, self.E,
+                                self.shared, self.Y, stream=stream)
+        return self.Y
+
+    def backward(self, dY, stream=None):
+        """dX [T,d] bf16, dw [T,k] fp32 and the four fp32 LoRA gradients."""
+        if self._ids is None:
+            raise RuntimeError("backward before forward")
+        L.moe_permute(dY, self.K, self.G, self.offsets, self.tile_off, self.sorted_src, self.dYp,
+                      stream)
+        w, g = self.w, self.grads
+        L.moe_lora_grouped_mlp_bwd(self.dims, self.dYp, self.Xp, self.counts, self.offsets,
+                                   self.tile_off, self.sorted_src, self._topk_w, w["W_gu"],
+                                   w["A_gu"], w["B_gu"], w["W_dn"], w["A_dn"], w["B_dn"], self.h,
+                                   self.act, self.xa_gu, self.xa_dn, self.dXp, self.dw_rows,
+                                   g["dA_gu"], g["dB_gu"], g["dA_dn"], g["dB_dn"], self.bwd_ws,
+                                   stream)
+        L.moe_unpermute_combine(self.dXp, self._ids, self.dest_pos, self.offsets, self.tile_off,
+                                self.E, self.shared, self.dX, row_scalars=self.dw_rows,
+                                slot_out=self.dw, stream=stream)
+        return {"dX": self.dX, "dw": self.dw, **g}
+
+    def step(self, X, ids, topk_w, dY, stream=None):
+        """One forward + backward pass of the layer (the hot path)."""
+        self.forward(X, ids, topk_w, stream)
+        return self.backward(dY, stream)
+
+    # -------------------------------------------------------------- helpers
+    def padded_row_of(self):
+        """Permuted row of each flat assignment [N] (host-side index helper for
+        tests): tile_off[g]*128 + dest_pos - offsets[g]."""
+        ids = self._ids.reshape(self.T, self.k).to(torch.int64)
+        if self.shared:
+            ids = torch.cat([ids, torch.full((self.T, 1), self.E, dtype=torch.int64,
+                                             device=ids.device)], 1)
+        g = ids.reshape(-1)
+        return (self.tile_off.to(torch.int64)[g] * L.TILE_M + self.dest_pos.to(torch.int64)
+                - self.offsets.to(torch.int64)[g])

@@ -1,0 +1,252 @@
+/*
+ * moe_gb300.h -- C ABI of the GB300 (sm_103a) MoE-LoRA expert layer.
+ *
+ * The layer is the MoE expert block that the Unsloth "Faster MoE" docs and the
+ * Unsloth x NVIDIA training article optimise for LoRA fine-tuning:
+ *
+ *   routing   flatten the [T,k] top-k expert ids, stable-sort them by expert id,
+ *             count them with one bincount, turn the counts into offsets and
+ *             permute the token rows once (article, section "Optimisation 3:
+ *             MoE routing done in one grouped pass", steps 1-5);
+ *   experts   per expert a SwiGLU MLP, gate_up then down, with "split LoRA":
+ *             X W^T + s (X A^T) B^T, never forming B A (docs, sections "What is
+ *             torch._grouped_mm" and "Faster LoRA MoE training"; the
+ *             split-LoRA equations of "Implementation details");
+ *   combine   Y[t] = sum_j w[t,j] * expert_{ids[t,j]}(X[t]) (the plain top-k
+ *             mixture; the pages do not print this step);
+ *   backward  dX, the routing-weight gradient and dA, dB of both adapters for
+ *             frozen base weights (docs: the router and base weights are frozen,
+ *             "loss, gradients and outputs are unchanged").
+ *
+ * Conventions for every call
+ *   - Every pointer is caller-owned DEVICE memory unless stated otherwise.  The
+ *     library never allocates or frees device memory and never synchronises,
+ *     except moe_status(), which synchronises the given stream.
+ *   - All work is enqueued on `stream` (a cudaStream_t; NULL = legacy default
+ *     stream).  Calls are stream-ordered; results are valid once the stream
+ *     reaches them.
+ *   - Tensors are dense row-major.  bf16 values are passed as 16-bit patterns
+ *     (moe_bf16).  Every bf16 matrix row must start on a 16-byte boundary: the
+ *     base pointers 16-byte aligned and d, f, r multiples of 8.
+ *   - Argument errors are detected on the host before anything is launched and
+ *     returned synchronously (MOE_ERR_INVALID_ARG / MOE_ERR_WORKSPACE /
+ *     MOE_ERR_UNSUPPORTED); moe_last_error() then describes the problem.
+ *     Launch failures return MOE_ERR_CUDA.  Errors found by kernels (an expert
+ *     id outside [0,E), a pipeline wait that timed out) are recorded in a
+ *     per-device status word read by moe_status().
+ *   - Determinism: no floating-point atomics; equal inputs give bit-identical
+ *     outputs.
+ *
+ * Notation
+ *   T tokens, d hidden size, f expert intermediate size, E routed experts,
+ *   k experts per token, r LoRA rank, s = lora_scale = alpha / r.
+ *   shared_expert = 1 adds one always-active expert with weight 1 (group E).
+ *   G = E + shared_expert expert groups, K = k + shared_expert slots per token,
+ *   N = T * K routed rows (flat index i = t*K + j; slot j = k is the shared one).
+ *
+ * Permuted ("padded") row layout used between calls
+ *   Expert g's rows are the rows routed to it in stable order (ascending flat
+ *   index).  In permuted buffers each group starts on a multiple of
+ *   MOE_TILE_M rows: group g occupies rows [MOE_TILE_M * tile_off[g],
+ *   MOE_TILE_M * tile_off[g+1]); its first counts[g] rows are real, the rest are
+ *   zero padding.  The number of permuted rows is MOE_TILE_M * tile_off[G], at
+ *   most moe_padded_rows_max(); allocate that many rows.
+ */
+#ifndef MOE_GB300_H
+#define MOE_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define MOE_API __attribute__((visibility("default")))
+#else
+#define MOE_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef uint16_t moe_bf16;                 /* bf16 bit pattern */
+typedef struct CUstream_st* moe_stream_t;  /* same type as cudaStream_t */
+
+typedef enum {
+  MOE_OK = 0,
+  MOE_ERR_INVALID_ARG = -1, /* null pointer, bad size, misaligned pointer */
+  MOE_ERR_UNSUPPORTED = -2, /* valid but outside what this build supports */
+  MOE_ERR_WORKSPACE = -3,   /* workspace too small */
+  MOE_ERR_CUDA = -4,        /* a CUDA runtime / driver call failed */
+  MOE_ERR_BAD_IDS = -5,     /* (device) an expert id outside [0,E) was seen */
+  MOE_ERR_TIMEOUT = -6      /* (device) a pipeline wait gave up */
+} moe_status_t;
+
+#define MOE_TILE_M 128      /* row granularity of the permuted layout */
+#define MOE_MAX_EXPERTS 1024
+
+typedef struct moe_dims {
+  int32_t T, d, f, E, k, r;
+  float lora_scale;        /* s = alpha / r */
+  int32_t shared_expert;   /* 0 or 1 */
+} moe_dims;
+
+/* Upper bound on permuted rows: T*K + G*(MOE_TILE_M-1) rounded to whole tiles.
+ * Returns -1 on bad arguments. */
+MOE_API int64_t moe_padded_rows_max(int32_t T, int32_t K, int32_t G);
+
+/* ------------------------------------------------------------------------ */
+/* Router (upstream of the layer; the docs keep the router frozen).          */
+/* ------------------------------------------------------------------------ */
+
+/* Softmax over the E logits of each token, top-k by descending logit (equal
+ * logits: lower expert id first), weights renormalised to sum to one -- the
+ * router rule of the layer workloads.  The renormalised weights equal a
+ * softmax over the k selected logits, which is what is computed (fp32).
+ *   logits  [T,E] fp32 (read)        ids [T,k] int32 (written)
+ *   weights [T,k] fp32 (written)     1 <= k <= min(E, 32), E <= MOE_MAX_EXPERTS */
+MOE_API int moe_router_topk(const float* logits, int32_t T, int32_t E, int32_t k,
+                    int32_t* ids, float* weights, moe_stream_t stream);
+
+/* ------------------------------------------------------------------------ */
+/* Routing: article section "Optimisation 3", steps 1-5.                     */
+/* ------------------------------------------------------------------------ */
+
+/* Bytes of scratch moe_route needs for T tokens, K slots, G groups. */
+MOE_API size_t moe_route_workspace_size(int32_t T, int32_t K, int32_t G);
+
+/* Flatten ids [T,k] row-major (the shared slot j = k carries id E when
+ * shared_expert = 1), stable-sort by expert id, bincount, offsets:
+ *   counts    [G]    counts[g] = #{i : id(i) = g}
+ *   offsets   [G+1]  exclusive prefix sum of counts
+ *   tile_off  [G+1]  exclusive prefix sum of ceil(counts / MOE_TILE_M)
+ *   sorted_src[N]    flat index i at each sorted position (stable: equal ids
+ *                    keep ascending i)
+ *   dest_pos  [N]    inverse permutation: sorted_src[dest_pos[i]] = i
+ * No data-dependent value reaches the host.  An id outside [0,E) sets
+ * MOE_ERR_BAD_IDS in the status word; that assignment is left out of counts
+ * and its dest_pos is -1 (sorted positions past the valid total are -1).
+ * ws: device scratch of at least moe_route_workspace_size() bytes, 16-byte
+ * aligned; its contents need no initialisation. */
+MOE_API int moe_route(const int32_t* ids, int32_t T, int32_t k, int32_t E, int32_t shared_expert,
+              int32_t* counts, int32_t* offsets, int32_t* tile_off,
+              int32_t* sorted_src, int32_t* dest_pos,
+              void* ws, size_t ws_bytes, moe_stream_t stream);
+
+/* Row permute (article step 5, "slice the token list by offsets"): for every
+ * permuted row p of group g with rank q = p - MOE_TILE_M*tile_off[g]:
+ *   dst[p,:] = src[sorted_src[offsets[g] + q] / K, :]   if q < counts[g]
+ *   dst[p,:] = 0                                         otherwise (padding)
+ *   src [T,d] bf16;  dst [moe_padded_rows_max(T,K,G), d] bf16; rows past
+ *   MOE_TILE_M*tile_off[G] are not touched.  Used for X (forward) and for the
+ *   upstream gradient dY (backward). */
+MOE_API int moe_permute(const moe_bf16* src, int32_t T, int32_t d, int32_t K, int32_t G,
+                const int32_t* offsets, const int32_t* tile_off,
+                const int32_t* sorted_src, moe_bf16* dst, moe_stream_t stream);
+
+/* Combine (unpermute + reduce): for every token t, with p(t,j) the permuted
+ * row of slot j (group g = id of slot j, p = MOE_TILE_M*tile_off[g] +
+ * dest_pos[t*K+j] - offsets[g]):
+ *   out[t,:] = bf16( sum_{j<K} c_j * rows[p(t,j),:] ),  fp32 sum in j order,
+ *   c_j = weights[t,j] for j < k and 1 for the shared slot, or c_j = 1 when
+ *   weights is NULL (rows already scaled, or a gradient sum);
+ *   slot_out[t,j] = row_scalars[p(t,j)] for j < k when both are non-NULL.
+ *   rows [.,d] bf16 permuted; ids [T,k]; out [T,d] bf16;
+ *   row_scalars [moe_padded_rows_max] fp32 or NULL; slot_out [T,k] fp32 or NULL.
+ * Assignments with dest_pos = -1 (bad ids) contribute nothing. */
+MOE_API int moe_unpermute_combine(const moe_bf16* rows, const int32_t* ids, const int32_t* dest_pos,
+                          const int32_t* offsets, const int32_t* tile_off,
+                          int32_t T, int32_t d, int32_t k, int32_t E, int32_t shared_expert,
+                          const float* weights, const float* row_scalars, float* slot_out,
+                          moe_bf16* out, moe_stream_t stream);
+
+/* ------------------------------------------------------------------------ */
+/* Grouped split-LoRA SwiGLU expert MLP (docs: "Faster LoRA MoE training",    */
+/* "Implementation details").                                                */
+/* ------------------------------------------------------------------------ */
+/* Weights, all bf16, row-major, G groups (shared expert last):
+ *   W_gu [G,2f,d]  rows [0,f) gate, rows [f,2f) up   A_gu [G,r,d]  B_gu [G,2f,r]
+ *   W_dn [G,d,f]                                      A_dn [G,r,f]  B_dn [G,d,r]
+ * Per permuted row p of group g with routing weight w_p (w of its slot; 1 for
+ * the shared slot; 0 for padding):
+ *   xa   = Xp A_gu^T             h = Xp W_gu^T + s xa B_gu^T      [.,2f]
+ *   act  = silu(h[:, :f]) * h[:, f:]                               [.,f]
+ *   xa_dn = act A_dn^T           o = act W_dn^T + s xa_dn B_dn^T  [.,d]
+ *   Yp   = w_p * o
+ * B A is never formed.  Accumulation is fp32 on tensor cores. */
+
+/* Precision of saved intermediates.  Every value that later feeds a sum over
+ * the rows of an expert (the LoRA weight gradients and the routing-weight
+ * gradient) keeps ~16 significant bits: h is stored in fp32, and the other
+ * such intermediates as "pair" buffers [2, P, cols] of bf16 with
+ * value = pair[0] + pair[1] (pair[0] = bf16(v), pair[1] = bf16(v - pair[0])).
+ * The tensor cores consume a pair as two bf16 operands (extra K steps).
+ * Here P = moe_padded_rows_max(T, K, G). */
+
+/* Forward.  Inputs: Xp (moe_permute of X), the routing outputs (counts is
+ * not read; offsets, tile_off and sorted_src locate each row's routing
+ * weight), topk weights [T,k] fp32, the six weight tensors.  Outputs:
+ *   Yp    [P,d]    bf16  w-scaled expert outputs (feed moe_unpermute_combine
+ *                        with weights = NULL)
+ *   h     [P,2f]   fp32  saved gate|up pre-activations
+ *   act   [2,P,f]  bf16 pair  saved silu(gate) * up
+ *   xa_gu [2,P,r]  bf16 pair  saved s * Xp A_gu^T
+ *   xa_dn [2,P,r]  bf16 pair  saved s * act A_dn^T
+ * The down projection consumes act's high half (Yp is a bf16 output). */
+MOE_API int moe_lora_grouped_mlp_fwd(const moe_dims* dims, const moe_bf16* Xp,
+                             const int32_t* counts, const int32_t* offsets,
+                             const int32_t* tile_off, const int32_t* sorted_src,
+                             const float* topk_w,
+                             const moe_bf16* W_gu, const moe_bf16* A_gu, const moe_bf16* B_gu,
+                             const moe_bf16* W_dn, const moe_bf16* A_dn, const moe_bf16* B_dn,
+                             moe_bf16* Yp, float* h, moe_bf16* act,
+                             moe_bf16* xa_gu, moe_bf16* xa_dn, moe_stream_t stream);
+
+/* Bytes of scratch moe_lora_grouped_mlp_bwd needs. */
+MOE_API size_t moe_mlp_bwd_workspace_size(const moe_dims* dims);
+
+/* Backward for frozen W (and frozen router).  dYp = moe_permute of the
+ * upstream gradient dY (unscaled); Xp, h, act, xa_gu, xa_dn as saved by the
+ * forward.  With dO = w_p dYp:
+ *   dw_rows[p] = <dYp_p, o_p> = <act_p, g_p>  [P] fp32, the gradient of the
+ *                routing weight of row p (moe_unpermute_combine gathers it
+ *                to [T,k] through row_scalars / slot_out)
+ *   g = dYp W_dn + s u A_dn with u = dYp B_dn;  dact = w_p g
+ *   dh = [dact*up*silu'(gate) | dact*silu(gate)];  v = dh B_gu
+ *   dXp = dh W_gu + s v A_gu              [P,d] bf16 (combine -> dX)
+ *   dB_dn[g] = s sum_p dO^T xa_dn          [G,d,r] fp32
+ *   dA_dn[g] = s sum_p (dO B_dn)^T act     [G,r,f] fp32
+ *   dB_gu[g] = s sum_p dh^T xa             [G,2f,r] fp32
+ *   dA_gu[g] = s sum_p v^T Xp              [G,r,d] fp32
+ * Gradients are overwritten (not accumulated); groups with no rows get zeros.
+ * ws: >= moe_mlp_bwd_workspace_size bytes of device scratch, 16-byte aligned. */
+MOE_API int moe_lora_grouped_mlp_bwd(const moe_dims* dims, const moe_bf16* dYp, const moe_bf16* Xp,
+                             const int32_t* counts, const int32_t* offsets,
+                             const int32_t* tile_off, const int32_t* sorted_src,
+                             const float* topk_w,
+                             const moe_bf16* W_gu, const moe_bf16* A_gu, const moe_bf16* B_gu,
+                             const moe_bf16* W_dn, const moe_bf16* A_dn, const moe_bf16* B_dn,
+                             const float* h, const moe_bf16* act,
+                             const moe_bf16* xa_gu, const moe_bf16* xa_dn,
+                             moe_bf16* dXp, float* dw_rows,
+                             float* dA_gu, float* dB_gu, float* dA_dn, float* dB_dn,
+                             void* ws, size_t ws_bytes, moe_stream_t stream);
+
+/* ------------------------------------------------------------------------ */
+/* Status                                                                    */
+/* ------------------------------------------------------------------------ */
+
+/* Synchronises `stream`, then returns and clears the current device's status
+ * word: MOE_OK, MOE_ERR_BAD_IDS or MOE_ERR_TIMEOUT (first error recorded), or
+ * MOE_ERR_CUDA if the synchronisation itself failed. */
+MOE_API int moe_status(moe_stream_t stream);
+
+/* Message for the last error returned on this thread ("" if none). */
+MOE_API const char* moe_last_error(void);
+
+/* Library ABI version (bumped on any signature change). */
+MOE_API int moe_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MOE_GB300_H */

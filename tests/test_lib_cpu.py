@@ -1,0 +1,116 @@
+"""The C-ABI library builds, loads and exports every declared symbol; host-side
+argument checks return their error codes before anything is launched.  No
+compute call runs here (no GPU needed)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "moe_gb300.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from expert_routing_grouped_moe_gb300 import build, _lib
+    build.build()
+    return _lib.load()
+
+
+def declared_symbols():
+    txt = open(HEADER).read()
+    return sorted(set(re.findall(r"^MOE_API [^(]*?\b(moe_\w+)\(", txt, flags=re.M)))
+
+
+def test_header_declares_the_five_layer_calls():
+    syms = declared_symbols()
+    for s in ("moe_route", "moe_permute", "moe_lora_grouped_mlp_fwd",
+              "moe_lora_grouped_mlp_bwd", "moe_unpermute_combine"):
+        assert s in syms
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for s in declared_symbols():
+        assert hasattr(lib, s), s
+    from expert_routing_grouped_moe_gb300 import _lib
+    assert set(_lib.EXPORTED) == set(declared_symbols())
+
+
+def test_sizes(lib):
+    assert lib.moe_abi_version() == 1
+    assert lib.moe_padded_rows_max(256, 2, 8) == ((256 * 2 + 8 * 127 + 127) // 128) * 128
+    assert lib.moe_padded_rows_max(0, 2, 8) == -1
+    assert lib.moe_route_workspace_size(4096, 8, 128) >= 128 * 4
+    assert lib.moe_route_workspace_size(0, 8, 128) == 0
+
+
+def _dims(**kw):
+    from expert_routing_grouped_moe_gb300 import _lib
+    base = dict(T=256, d=128, f=64, E=8, k=2, r=8, lora_scale=2.0, shared_expert=0)
+    base.update(kw)
+    return _lib.MoeDims(**base)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(k=9), -1), (dict(d=100), -1), (dict(r=12), -1), (dict(T=0), -1),
+    (dict(shared_expert=2), -1), (dict(E=2000, k=2), -2), (dict(r=128), -2),
+])
+def test_bwd_workspace_rejects_bad_dims(lib, kw, code):
+    from expert_routing_grouped_moe_gb300 import _lib
+    d = _dims(**kw)
+    assert lib.moe_mlp_bwd_workspace_size(ctypes.byref(d)) == 0
+
+
+def test_fwd_argument_errors_before_launch(lib):
+    from expert_routing_grouped_moe_gb300 import _lib
+    P = ctypes.c_void_p
+    fake = P(1 << 20)  # never dereferenced: checks fail first
+    d = _dims(k=9)
+    rc = lib.moe_lora_grouped_mlp_fwd(ctypes.byref(d), *([fake] * 17), None)
+    assert rc == _lib.MOE_ERR_INVALID_ARG
+    assert b"k=9" in lib.moe_last_error()
+    d = _dims()
+    args = [fake] * 17
+    args[0] = None  # Xp
+    rc = lib.moe_lora_grouped_mlp_fwd(ctypes.byref(d), *args, None)
+    assert rc == _lib.MOE_ERR_INVALID_ARG
+    assert b"Xp" in lib.moe_last_error()
+    args = [fake] * 17
+    args[12] = P((1 << 20) + 4)  # Yp misaligned
+    rc = lib.moe_lora_grouped_mlp_fwd(ctypes.byref(d), *args, None)
+    assert rc == _lib.MOE_ERR_INVALID_ARG
+    assert b"aligned" in lib.moe_last_error()
+
+
+def test_route_argument_errors_before_launch(lib):
+    from expert_routing_grouped_moe_gb300 import _lib
+    P = ctypes.c_void_p
+    fake = P(1 << 20)
+    assert lib.moe_route(None, 4, 2, 8, 0, *([fake] * 6), 1 << 20, None) == _lib.MOE_ERR_INVALID_ARG
+    assert lib.moe_route(fake, 4, 9, 8, 0, *([fake] * 6), 1 << 20, None) == _lib.MOE_ERR_INVALID_ARG
+    assert lib.moe_route(fake, 4, 2, 2048, 0, *([fake] * 6), 1 << 20, None) == _lib.MOE_ERR_UNSUPPORTED
+    assert lib.moe_route(fake, 4, 2, 8, 0, *([fake] * 6), 4, None) == _lib.MOE_ERR_WORKSPACE
+    assert lib.moe_route(fake, 4, 2, 8, 3, *([fake] * 6), 1 << 20, None) == _lib.MOE_ERR_INVALID_ARG
+
+
+def test_rows_and_router_argument_errors(lib):
+    from expert_routing_grouped_moe_gb300 import _lib
+    P = ctypes.c_void_p
+    fake = P(1 << 20)
+    assert lib.moe_permute(fake, 4, 12, 2, 8, fake, fake, fake, fake, None) == _lib.MOE_ERR_INVALID_ARG
+    assert lib.moe_permute(fake, 4, 16, 2, 8, None, fake, fake, fake, None) == _lib.MOE_ERR_INVALID_ARG
+    # row_scalars without slot_out
+    assert lib.moe_unpermute_combine(fake, fake, fake, fake, fake, 4, 16, 2, 8, 0, None, fake,
+                                     None, fake, None) == _lib.MOE_ERR_INVALID_ARG
+    assert lib.moe_router_topk(fake, 4, 8, 9, fake, fake, None) == _lib.MOE_ERR_INVALID_ARG
+    assert lib.moe_router_topk(fake, 4, 2048, 2, fake, fake, None) == _lib.MOE_ERR_UNSUPPORTED
+
+
+def test_product_path_has_no_oracle_or_fallback():
+    """The package never imports the oracle and has no CPU compute path."""
+    pkg = os.path.join(ROOT, "expert_routing_grouped_moe_gb300")
+    for fn in os.listdir(pkg):
+        if fn.endswith(".py"):
+            src = open(os.path.join(pkg, fn)).read()
+            assert "import oracle" not in src and "from oracle" not in src, fn
