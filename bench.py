@@ -1,0 +1,476 @@
+#!/usr/bin/env python
+"""Benchmark of the MoE-LoRA expert layer: one step = forward + backward of the
+whole layer (route, permute, grouped split-LoRA SwiGLU GEMMs, combine, and the
+backward with dX, routing-weight and LoRA gradients) on one batch.
+
+Default workload: the Qwen3-30B-A3B-shaped layer (T=4096 tokens, d=2048,
+f=768, E=128 experts, top-8, LoRA r=64, alpha=128), synthetic seeded inputs.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Under torchrun (N > 1) every rank runs its own replica of the layer on its own
+batch (weak scaling, no collective on the data path); the elapsed time is the
+maximum over ranks.  Rank 0 prints one JSON line.  ``--impl reference`` times
+the CPU oracle (plain NumPy fp64) on the host cores instead.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "MoE-LoRA layer fwd+bwd tokens/s and TFLOP/s vs BF16 peak; routing GB/s"
+PEAKS_FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+# DRAM traffic per launch of the dominant kernel from one ncu capture
+# (dram__bytes_read.sum + dram__bytes_write.sum), keyed by kernel and workload;
+# None until captured for the current kernel version.
+NCU_TRAFFIC_BYTES = {}
+
+
+def parse_args(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=400)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--config", default="qwen3_30b_a3b")
+    ap.add_argument("--seed", type=int, default=1)
+    ap.add_argument("--e2e-steps", type=int, default=0, help="0: same as --steps (capped)")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-budget-s", type=float, default=20.0)
+    ap.add_argument("--probe-steps", type=int, default=100)
+    return ap.parse_args(argv)
+
+
+# ---------------------------------------------------------------- work model
+
+def layer_counts(cfg):
+    """Algorithmic work of one fwd+bwd step (split-LoRA counts; the dense
+    merged work is not counted)."""
+    T, d, f, r, k = cfg.T, cfg.d, cfg.f, cfg.r, cfg.k
+    N = cfg.rows                                   # routed rows (+ shared rows)
+    F_base = 2 * N * d * 2 * f + 2 * N * f * d     # gate_up + down
+    F_lora = 2 * N * (d * r + r * 2 * f + f * r + r * d)
+    kern = {  # per launch
+        "xa_gu": ("tensor", 2 * N * d * r), "gate_up": ("tensor", 2 * N * d * 2 * f + 2 * N * r * 2 * f),
+        "xa_dn": ("tensor", 2 * N * f * r), "down": ("tensor", 2 * N * f * d + 2 * N * r * d),
+        "u": ("tensor", 2 * N * d * r), "dgrad_dn": ("tensor", 2 * N * d * f + 2 * N * r * f),
+        "v": ("tensor", 2 * N * 2 * f * r), "dgrad_gu": ("tensor", 2 * N * 2 * f * d + 2 * N * r * d),
+        "dB_dn": ("tensor", 2 * N * d * r), "dA_dn": ("tensor", 2 * N * f * r),
+        "dB_gu": ("tensor", 2 * N * 2 * f * r), "dA_gu": ("tensor", 2 * N * d * r),
+        "route": ("hbm", 4 * T * k + 8 * N + 12 * cfg.groups),
+        "permute": ("hbm", 2 * T * d + 2 * N * d + 4 * N),
+        "combine": ("hbm", 2 * N * d + 2 * T * d + 8 * N + 4 * T * k),
+        "dw_reduce": ("hbm", 8 * N),
+    }
+    return {"flops": 2 * F_base + 3 * F_lora, "F_base": F_base, "F_lora": F_lora, "kernels": kern,
+            "launches": {"permute": 2, "combine": 2}}
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as fh:
+            d = json.load(fh)
+        return {k: float(d[k]) for k in PEAKS_FALLBACK}, "measured"
+    except (OSError, KeyError, ValueError):
+        return dict(PEAKS_FALLBACK), "fallback"
+
+
+# ---------------------------------------------------------------- clocks
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons every 200 ms."""
+    FIELDS = ("uuid,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, uuid):
+        self.uuid = uuid
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "--query-gpu=" + self.FIELDS, "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.thread.join(timeout=2)
+        sm, mx, reasons, power = [], None, set(), []
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        for ln in self.lines:
+            parts = [x.strip() for x in ln.split(",")]
+            if len(parts) < 8:
+                continue
+            if self.uuid and parts[0] != self.uuid:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx = float(parts[2])
+                power.append(float(parts[3]))
+            except ValueError:
+                continue
+            for nm, v in zip(names, parts[4:8]):
+                if v.lower() == "active":
+                    reasons.add(nm)
+        loaded = [x for x in sm if mx and x > 0.5 * mx] or sm
+        return {"sm_mhz": statistics.median(loaded) if loaded else None, "sm_max_mhz": mx,
+                "reasons": sorted(reasons), "samples": len(sm),
+                "power_w_max": max(power) if power else None}
+
+
+def gpu_uuid(torch, dev):
+    try:
+        u = str(torch.cuda.get_device_properties(dev).uuid)
+        return u if u.startswith("GPU-") else "GPU-" + u
+    except Exception:
+        return None
+
+
+# ---------------------------------------------------------------- distributed
+
+def dist_setup(torch):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if backend == "nccl":
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend=backend)
+        return dist, rank, world, local
+    return None, rank, world, local
+
+
+def max_over_ranks(torch, dist, value, device):
+    if dist is None:
+        return value
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(dist, torch, device):
+    if dist is not None:
+        if device.type == "cuda":
+            dist.barrier(device_ids=[device.index])
+        else:
+            dist.barrier()
+
+
+# ---------------------------------------------------------------- CPU oracle
+
+def oracle_time_per_token(P, X, ids, w, dY, ntok):
+    import oracle
+    t0 = time.perf_counter()
+    oracle.layer_forward(X[:ntok], ids[:ntok], w[:ntok], P)
+    oracle.layer_backward(X[:ntok], ids[:ntok], w[:ntok], dY[:ntok], P)
+    return (time.perf_counter() - t0) / ntok
+
+
+def oracle_inputs(cfg, weights, act, ids, w):
+    """fp64 copies of the synthetic workload for the oracle (host side)."""
+    import numpy as np
+    import oracle
+    P = oracle.OracleParams.from_arrays(
+        {n: t.double().cpu().numpy() for n, t in weights.items()}, s=cfg.scale, E=cfg.E,
+        shared=cfg.shared)
+    X = act["X"].double().cpu().numpy()
+    dY = act["dY"].double().cpu().numpy()
+    return P, X, np.ascontiguousarray(ids), np.ascontiguousarray(w), dY
+
+
+def cpu_cores():
+    try:
+        from threadpoolctl import threadpool_info
+        nt = [i.get("num_threads") for i in threadpool_info() if i.get("user_api") == "blas"]
+        if nt:
+            return int(max(nt))
+    except Exception:
+        pass
+    return os.cpu_count() or 1
+
+
+def cpu_baseline(cfg, P, X, ids, w, dY, budget_s):
+    """The oracle as it stands on a bounded token sample, as tokens/s."""
+    tpt = oracle_time_per_token(P, X, ids, w, dY, min(cfg.T, 8))
+    ntok = int(max(8, min(cfg.T, budget_s / max(tpt, 1e-9))))
+    t0 = time.perf_counter()
+    import oracle
+    oracle.layer_forward(X[:ntok], ids[:ntok], w[:ntok], P)
+    oracle.layer_backward(X[:ntok], ids[:ntok], w[:ntok], dY[:ntok], P)
+    dt = time.perf_counter() - t0
+    return {"value": ntok / dt, "unit": "tokens/s", "cores": cpu_cores(), "kind": "oracle",
+            "sample": "oracle fp64 forward+backward of the first %d of %d tokens "
+                      "(all %d slots, every expert they route to), %.1f s" % (
+                          ntok, cfg.T, cfg.slots, dt)}
+
+
+# ---------------------------------------------------------------- our arm
+
+def run_ours(args):
+    import torch
+    from expert_routing_grouped_moe_gb300 import (LAUNCHES_BWD, LAUNCHES_FWD, MoELoRALayer,
+                                                  _lib as L, build, synth)
+
+    dist, rank, world, local = dist_setup(torch)
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA GPU (the layer has no CPU path)")
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    build.build()
+    L.load()
+    cfg = synth.CONFIGS[args.config]
+    seed = args.seed + 1000 * rank
+    weights = synth.layer_weights(cfg, seed, device=dev)
+    act = synth.layer_activations(cfg, seed, device=dev)
+    ids = torch.empty(cfg.T, cfg.k, dtype=torch.int32, device=dev)
+    topw = torch.empty(cfg.T, cfg.k, dtype=torch.float32, device=dev)
+    L.moe_router_topk(act["logits"], cfg.k, ids, topw)
+    layer = MoELoRALayer(cfg.T, cfg.d, cfg.f, cfg.E, cfg.k, cfg.r, cfg.alpha, weights,
+                         shared_expert=cfg.shared, device=dev)
+    X, dY = act["X"], act["dY"]
+    stream = torch.cuda.current_stream()
+
+    for _ in range(args.warmup):
+        layer.step(X, ids, topw, dY)
+    torch.cuda.synchronize()
+    if L.moe_status() != L.MOE_OK:
+        raise SystemExit("device status error after warm-up")
+
+    counts = layer_counts(cfg)
+    names = L.kernel_names()
+    probe_steps = min(args.steps, args.probe_steps)
+    probes = {}
+    for n in names:
+        if n in ("router_topk",):
+            continue
+        per = counts["launches"].get(n, 1)
+        probes[n] = L.KernelProbe(n, per * probe_steps)
+
+    sampler = ClockSampler(gpu_uuid(torch, dev))
+    sampler.start()
+    time.sleep(0.3)
+    barrier(dist, torch, dev)
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        layer.step(X, ids, topw, dY)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    barrier(dist, torch, dev)
+    clocks = sampler.stop()
+    ms = e0.elapsed_time(e1) / args.steps
+    ms_max = max_over_ranks(torch, dist, ms, dev)
+    if L.moe_status() != L.MOE_OK:
+        raise SystemExit("device status error in the timed region")
+
+    kstats = {}
+    for n, pr in probes.items():
+        ts = pr.times_ms()
+        pr.disarm()
+        if ts:
+            per = counts["launches"].get(n, 1)
+            mean = sum(ts) / len(ts)
+            kstats[n] = {"ms_per_launch": mean, "launches_per_step": per,
+                         "share": mean * per / ms}
+
+    # ---- end to end through the public API with host buffers
+    e2e_steps = args.e2e_steps or min(args.steps, 200)
+    Xh = X.cpu().pin_memory()
+    dYh = dY.cpu().pin_memory()
+    idsh = ids.cpu().pin_memory()
+    wh = topw.cpu().pin_memory()
+    Yh = torch.empty(cfg.T, cfg.d, dtype=torch.bfloat16).pin_memory()
+    dXh = torch.empty(cfg.T, cfg.d, dtype=torch.bfloat16).pin_memory()
+    Xd, dYd = torch.empty_like(X), torch.empty_like(dY)
+    idsd, wd = torch.empty_like(ids), torch.empty_like(topw)
+    h2d = sum(t.numel() * t.element_size() for t in (Xh, dYh, idsh, wh))
+    d2h = sum(t.numel() * t.element_size() for t in (Yh, dXh))
+
+    def e2e_step():
+        Xd.copy_(Xh, non_blocking=True)
+        idsd.copy_(idsh, non_blocking=True)
+        wd.copy_(wh, non_blocking=True)
+        dYd.copy_(dYh, non_blocking=True)
+        Y = layer.forward(Xd, idsd, wd)
+        Yh.copy_(Y, non_blocking=True)
+        g = layer.backward(dYd)
+        dXh.copy_(g["dX"], non_blocking=True)
+
+    for _ in range(3):
+        e2e_step()
+    torch.cuda.synchronize()
+    barrier(dist, torch, dev)
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = max_over_ranks(torch, dist, e0.elapsed_time(e1) / e2e_steps, dev)
+    barrier(dist, torch, dev)
+
+    if rank != 0:
+        if dist is not None:
+            dist.destroy_process_group()
+        return None
+
+    peaks, peak_src = load_peaks()
+    tokens_s = world * cfg.T / (ms_max / 1e3)
+    tflops = world * counts["flops"] / (ms_max / 1e3) / 1e12
+    # dominant kernel and its roofline
+    dom = max(kstats, key=lambda n: kstats[n]["share"]) if kstats else None
+    roof = None
+    if dom is not None:
+        bound, work = counts["kernels"][dom]
+        dur_s = kstats[dom]["ms_per_launch"] / 1e3
+        if bound == "tensor":
+            ach = work / dur_s / 1e12
+            peak = peaks["bf16_tflops_sustained"]
+            unit = "TFLOP/s"
+        else:
+            ach = work / dur_s / 1e9
+            peak = peaks["hbm_gbs"]
+            unit = "GB/s"
+        roof = {"kernel": dom, "bound": bound, "achieved": ach, "peak": peak, "unit": unit,
+                "frac": ach / peak, "traffic": NCU_TRAFFIC_BYTES.get((dom, args.config)),
+                "work_per_launch": work,
+                "peak_source": "%s (%s)" % (peak_src, "bf16 sustained" if bound == "tensor"
+                                            else "HBM copy")}
+    route = None
+    if "route" in kstats:
+        rb = counts["kernels"]["route"][1]
+        gbs = rb / (kstats["route"]["ms_per_launch"] / 1e3) / 1e9
+        route = {"gbs": gbs, "frac_of_hbm": gbs / peaks["hbm_gbs"], "bytes_per_launch": rb}
+    kernels = {n: {"ms": round(v["ms_per_launch"], 5), "share": round(v["share"], 4)}
+               for n, v in sorted(kstats.items(), key=lambda kv: -kv[1]["share"])}
+    gemm_ms = sum(v["ms_per_launch"] * v["launches_per_step"] for n, v in kstats.items()
+                  if counts["kernels"][n][0] == "tensor")
+
+    cpu = None
+    if world == 1 and not args.no_cpu_baseline:
+        import numpy as np
+        P, Xo, ido, wo, dYo = oracle_inputs(cfg, weights, act, ids.cpu().numpy(),
+                                            topw.cpu().numpy())
+        cpu = cpu_baseline(cfg, P, Xo, ido, wo, dYo, args.cpu_budget_s)
+        del P, Xo, dYo, np
+
+    out = {
+        "metric": METRIC, "value": tokens_s, "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_max,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded; random-init weights of the layer shape)",
+        "config": {"workload": "%s-shaped MoE-LoRA layer fwd+bwd" % cfg.name, "T": cfg.T,
+                   "d": cfg.d, "f": cfg.f, "E": cfg.E, "k": cfg.k, "r": cfg.r,
+                   "alpha": cfg.alpha, "shared_expert": cfg.shared,
+                   "global_batch_tokens": world * cfg.T, "parallelism": "replicas x%d" % world,
+                   "l2": "inputs larger than L2 (%.2f GB of expert weights read per pass)" % (
+                       2 * (cfg.groups * (2 * cfg.f * cfg.d + cfg.d * cfg.f)) / 1e9)},
+        "tflops": tflops,
+        "tflops_frac": tflops / (world * peaks["bf16_tflops_sustained"]),
+        "tflops_frac_of": "%s bf16 sustained %.1f TFLOP/s per GPU" % (
+            peak_src, peaks["bf16_tflops_sustained"]),
+        "gemm_ms_per_step": gemm_ms,
+        "routing": route,
+        "roofline": roof,
+        "kernels": kernels,
+        "cpu_baseline": cpu,
+        "e2e": {"value": world * cfg.T / (e2e_ms / 1e3), "unit": "tokens/s",
+                "ms_per_step": e2e_ms, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "gpu_launches": args.steps * (LAUNCHES_FWD + LAUNCHES_BWD),
+        "clocks": clocks,
+    }
+    if dist is not None:
+        dist.destroy_process_group()
+    return out
+
+
+# ---------------------------------------------------------------- reference arm
+
+def run_reference(args):
+    """The CPU oracle, as it stands, on the host cores; one step = oracle
+    fwd+bwd on a token sample sized so the whole run ends within minutes."""
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return None
+    import numpy as np
+    import oracle
+    from expert_routing_grouped_moe_gb300 import synth
+    cfg = synth.CONFIGS[args.config]
+    weights = synth.layer_weights(cfg, args.seed, device="cpu")
+    act = synth.layer_activations(cfg, args.seed, device="cpu")
+    ids, w = oracle.router_topk(act["logits"].numpy(), cfg.k)
+    P, X, ids, w, dY = oracle_inputs(cfg, weights, act, ids, w)
+    budget = 150.0
+    tpt = oracle_time_per_token(P, X, ids, w, dY, min(cfg.T, 8))
+    ntok = int(max(1, min(cfg.T, budget / (args.steps + args.warmup) / max(tpt, 1e-9))))
+    rng = np.random.default_rng(0)
+    for _ in range(args.warmup):
+        sel = rng.choice(cfg.T, size=ntok, replace=False)
+        oracle.layer_forward(X[sel], ids[sel], w[sel], P)
+        oracle.layer_backward(X[sel], ids[sel], w[sel], dY[sel], P)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        sel = rng.choice(cfg.T, size=ntok, replace=False)
+        oracle.layer_forward(X[sel], ids[sel], w[sel], P)
+        oracle.layer_backward(X[sel], ids[sel], w[sel], dY[sel], P)
+    dt = time.perf_counter() - t0
+    value = args.steps * ntok / dt
+    sample = ("each step: oracle fp64 forward+backward of %d random tokens of the %d-token "
+              "batch" % (ntok, cfg.T))
+    return {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
+        "n_gpus": int(os.environ.get("WORLD_SIZE", "1")), "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": "%s-shaped MoE-LoRA layer fwd+bwd" % cfg.name, "T": cfg.T,
+                   "d": cfg.d, "f": cfg.f, "E": cfg.E, "k": cfg.k, "r": cfg.r},
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cpu_cores(),
+                         "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    out = run_reference(args) if args.impl == "reference" else run_ours(args)
+    if out is not None:
+        print(json.dumps(out), flush=True)
+
+
+if __name__ == "__main__":
+    main()

@@ -29,7 +29,7 @@ EXPORTED = (
     "moe_padded_rows_max", "moe_router_topk", "moe_route_workspace_size", "moe_route",
     "moe_permute", "moe_unpermute_combine", "moe_lora_grouped_mlp_fwd",
     "moe_mlp_bwd_workspace_size", "moe_lora_grouped_mlp_bwd", "moe_status",
-    "moe_last_error", "moe_abi_version",
+    "moe_last_error", "moe_abi_version", "moe_kernel_name", "moe_probe_arm", "moe_probe_count",
 )
 
 
@@ -86,6 +86,10 @@ def load(path: str = LIB_PATH):
             "moe_status": (ctypes.c_int, [_P]),
             "moe_last_error": (ctypes.c_char_p, []),
             "moe_abi_version": (ctypes.c_int, []),
+            "moe_kernel_name": (ctypes.c_char_p, [_I]),
+            "moe_probe_arm": (ctypes.c_int, [ctypes.c_char_p, ctypes.POINTER(_P),
+                                             ctypes.POINTER(_P), _I]),
+            "moe_probe_count": (_I, [ctypes.c_char_p]),
         }
         for name, (res, args) in sig.items():
             fn = getattr(lib, name)
@@ -216,3 +220,42 @@ def moe_lora_grouped_mlp_bwd(dims: MoeDims, dYp, Xp, counts, offsets, tile_off, 
 def moe_status(stream=None) -> int:
     """Synchronise the stream and return (and clear) the device status word."""
     return int(load().moe_status(_stream(stream)))
+
+
+# ------------------------------------------------------------------ tracing
+
+def kernel_names():
+    lib, out, i = load(), [], 0
+    while True:
+        n = lib.moe_kernel_name(i)
+        if n is None:
+            return out
+        out.append(n.decode())
+        i += 1
+
+
+class KernelProbe:
+    """Device time of the next ``n`` launches of one kernel, from CUDA events
+    the library records on the launch stream (see moe_probe_arm)."""
+
+    def __init__(self, kernel: str, n: int):
+        self.kernel = kernel
+        self.start = [torch.cuda.Event(enable_timing=True) for _ in range(n)]
+        self.stop = [torch.cuda.Event(enable_timing=True) for _ in range(n)]
+        s = torch.cuda.current_stream()
+        for e in self.start + self.stop:   # materialise the event handles
+            e.record(s)
+        torch.cuda.synchronize()
+        arr = _P * n
+        self._a = arr(*[e.cuda_event for e in self.start])
+        self._b = arr(*[e.cuda_event for e in self.stop])
+        _check(load().moe_probe_arm(kernel.encode(), self._a, self._b, n), "moe_probe_arm")
+
+    def disarm(self):
+        load().moe_probe_arm(self.kernel.encode(), None, None, 0)
+
+    def times_ms(self):
+        """Durations (ms) of the recorded launches (synchronises)."""
+        n = int(load().moe_probe_count(self.kernel.encode()))
+        torch.cuda.synchronize()
+        return [self.start[i].elapsed_time(self.stop[i]) for i in range(n)]

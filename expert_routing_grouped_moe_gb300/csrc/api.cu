@@ -4,8 +4,10 @@
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
+#include <atomic>
 #include <mutex>
 #include <string>
+#include <vector>
 
 #include "../../include/moe_gb300.h"
 #include "internal.h"
@@ -68,6 +70,53 @@ int device_state(DevState** out) {
   *out = &st;
   return MOE_OK;
 }
+
+// ---- timing probe (tracing): caller-owned CUDA events around kernel launches
+const char* const kKernelNames[] = {
+    "route", "permute", "combine", "router_topk", "xa_gu", "gate_up", "xa_dn", "down",
+    "u", "dgrad_dn", "v", "dgrad_gu", "dB_dn", "dA_dn", "dB_gu", "dA_gu", "dw_reduce"};
+constexpr int kNumKernels = sizeof(kKernelNames) / sizeof(kKernelNames[0]);
+
+struct Probe {
+  std::vector<void*> start, stop;
+  int used = 0;
+};
+Probe g_probe[kNumKernels];
+std::mutex g_probe_mu;
+std::atomic<int> g_probe_armed{0};
+
+int kernel_index(const char* name) {
+  if (name == nullptr) return -1;
+  for (int i = 0; i < kNumKernels; ++i)
+    if (std::strcmp(kKernelNames[i], name) == 0) return i;
+  return -1;
+}
+
+// Records the start event of the next free probe slot of `name`; returns the
+// slot (or -1 when the kernel is not being probed).
+int probe_begin(const char* name, cudaStream_t s) {
+  if (g_probe_armed.load(std::memory_order_relaxed) == 0) return -1;
+  const int id = kernel_index(name);
+  if (id < 0) return -1;
+  std::lock_guard<std::mutex> lk(g_probe_mu);
+  Probe& pr = g_probe[id];
+  if (pr.used >= static_cast<int>(pr.start.size())) return -1;
+  const int slot = pr.used++;
+  cudaEventRecord(static_cast<cudaEvent_t>(pr.start[slot]), s);
+  return id * (1 << 24) + slot;
+}
+void probe_end(int token, cudaStream_t s) {
+  if (token < 0) return;
+  std::lock_guard<std::mutex> lk(g_probe_mu);
+  const Probe& pr = g_probe[token >> 24];
+  cudaEventRecord(static_cast<cudaEvent_t>(pr.stop[token & ((1 << 24) - 1)]), s);
+}
+struct ProbeScope {
+  int token;
+  cudaStream_t s;
+  ProbeScope(const char* name, cudaStream_t st) : token(probe_begin(name, st)), s(st) {}
+  ~ProbeScope() { probe_end(token, s); }
+};
 
 using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
                                    const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
@@ -196,6 +245,7 @@ GemmParams base_params(const moe_dims* dm, const int32_t* offsets, const int32_t
 int run_gemm(const GemmShape& sh, GemmParams& p, int64_t P, int num_sms, cudaStream_t s,
              const char* what) {
   if (!sh.wgrad) p.max_tiles = static_cast<int>(P / kTileM) * p.n_ntiles;
+  ProbeScope probe(what, s);
   cudaError_t e = launch_gemm(sh, p, num_sms, s);
   if (e != cudaSuccess) return cuda_fail(e, what);
   return MOE_OK;
@@ -228,6 +278,35 @@ extern "C" {
 
 int moe_abi_version(void) { return 1; }
 
+int moe_probe_arm(const char* kernel, void* const* start_events, void* const* stop_events,
+                  int32_t n) {
+  const int id = kernel_index(kernel);
+  if (id < 0) return fail(MOE_ERR_INVALID_ARG, "unknown kernel name");
+  if (n < 0 || (n > 0 && (start_events == nullptr || stop_events == nullptr)))
+    return fail(MOE_ERR_INVALID_ARG, "bad event arrays");
+  std::lock_guard<std::mutex> lk(g_probe_mu);
+  Probe& pr = g_probe[id];
+  const bool was = !pr.start.empty();
+  pr.start.assign(start_events, start_events + n);
+  pr.stop.assign(stop_events, stop_events + n);
+  pr.used = 0;
+  const bool now = n > 0;
+  if (now && !was) g_probe_armed.fetch_add(1);
+  if (!now && was) g_probe_armed.fetch_sub(1);
+  return ok();
+}
+
+int32_t moe_probe_count(const char* kernel) {
+  const int id = kernel_index(kernel);
+  if (id < 0) return -1;
+  std::lock_guard<std::mutex> lk(g_probe_mu);
+  return g_probe[id].used;
+}
+
+const char* moe_kernel_name(int32_t i) {
+  return (i >= 0 && i < kNumKernels) ? kKernelNames[i] : nullptr;
+}
+
 const char* moe_last_error(void) { return t_err.c_str(); }
 
 int64_t moe_padded_rows_max(int32_t T, int32_t K, int32_t G) {
@@ -259,6 +338,7 @@ int moe_router_topk(const float* logits, int32_t T, int32_t E, int32_t k, int32_
     return fail(MOE_ERR_INVALID_ARG, "NULL pointer");
   if (T <= 0 || E <= 0 || k <= 0 || k > E) return fail(MOE_ERR_INVALID_ARG, "bad T/E/k");
   if (E > kMaxExperts || k > 32) return fail(MOE_ERR_UNSUPPORTED, "E > 1024 or k > 32");
+  ProbeScope probe("router_topk", stream);
   cudaError_t e = launch_router_topk(logits, T, E, k, ids, weights, stream);
   if (e != cudaSuccess) return cuda_fail(e, "router_topk launch");
   return ok();
@@ -282,6 +362,7 @@ int moe_route(const int32_t* ids, int32_t T, int32_t k, int32_t E, int32_t share
   DevState* st = nullptr;
   int rc = device_state(&st);
   if (rc) return rc;
+  ProbeScope probe("route", stream);
   cudaError_t e = launch_route(ids, T, k, E, shared_expert, counts, offsets, tile_off,
                                sorted_src, dest_pos, static_cast<int32_t*>(ws), st->status,
                                stream);
@@ -300,6 +381,7 @@ int moe_permute(const moe_bf16* src, int32_t T, int32_t d, int32_t K, int32_t G,
   if (G > kMaxExperts + 1) return fail(MOE_ERR_UNSUPPORTED, "too many groups");
   const int64_t P = padded_rows_max(T, K, G);
   if (P >= (int64_t(1) << 31)) return fail(MOE_ERR_UNSUPPORTED, "too many routed rows");
+  ProbeScope probe("permute", stream);
   cudaError_t e =
       launch_permute(src, T, d, K, G, offsets, tile_off, sorted_src, dst, P, stream);
   if (e != cudaSuccess) return cuda_fail(e, "permute launch");
@@ -320,6 +402,7 @@ int moe_unpermute_combine(const moe_bf16* rows, const int32_t* ids, const int32_
   if (k > 32 || E > kMaxExperts) return fail(MOE_ERR_UNSUPPORTED, "k > 32 or E > 1024");
   if ((row_scalars == nullptr) != (slot_out == nullptr))
     return fail(MOE_ERR_INVALID_ARG, "row_scalars and slot_out go together");
+  ProbeScope probe("combine", stream);
   cudaError_t e = launch_combine(rows, ids, dest_pos, offsets, tile_off, T, d, k, E,
                                  shared_expert, weights, row_scalars, slot_out, out, stream);
   if (e != cudaSuccess) return cuda_fail(e, "combine launch");
@@ -489,7 +572,11 @@ int moe_lora_grouped_mlp_bwd(const moe_dims* dims, const moe_bf16* dYp, const mo
     p.fout = j.out; p.fstride = static_cast<int64_t>(j.M) * r; p.transpose_out = j.transpose;
     if ((rc = run_gemm({128, true, true, Epi::kWgrad}, p, P, st->num_sms, s, j.name))) return rc;
   }
-  cudaError_t e = launch_sum_parts(w.dwp, nparts, P, P, dw_rows, s);
+  cudaError_t e;
+  {
+    ProbeScope probe("dw_reduce", s);
+    e = launch_sum_parts(w.dwp, nparts, P, P, dw_rows, s);
+  }
   if (e != cudaSuccess) return cuda_fail(e, "dw reduce");
   return ok();
 }

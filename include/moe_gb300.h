@@ -243,6 +243,27 @@ MOE_API int moe_status(moe_stream_t stream);
 /* Message for the last error returned on this thread ("" if none). */
 MOE_API const char* moe_last_error(void);
 
+/* ------------------------------------------------------------------------ */
+/* Tracing: timing probe                                                     */
+/* ------------------------------------------------------------------------ */
+
+/* Kernel names the probe knows, i = 0, 1, ...; NULL past the last one:
+ * route, permute, combine, router_topk, the grouped GEMMs xa_gu, gate_up,
+ * xa_dn, down, u, dgrad_dn, v, dgrad_gu, the weight-gradient GEMMs dB_dn,
+ * dA_dn, dB_gu, dA_gu, and dw_reduce.  ("route" covers its three kernels.) */
+MOE_API const char* moe_kernel_name(int32_t i);
+
+/* Arms the probe of one kernel: its next n launches record start_events[i]
+ * before and stop_events[i] after the launch on the launch stream (cudaEvent_t
+ * handles, caller-owned, created with timing enabled); later launches are not
+ * recorded.  n = 0 disarms.  The arrays are copied.  Costs nothing when no
+ * kernel is armed. */
+MOE_API int moe_probe_arm(const char* kernel, void* const* start_events,
+                          void* const* stop_events, int32_t n);
+
+/* Launches of `kernel` recorded since it was armed (-1: unknown name). */
+MOE_API int32_t moe_probe_count(const char* kernel);
+
 /* Library ABI version (bumped on any signature change). */
 MOE_API int moe_abi_version(void);
 

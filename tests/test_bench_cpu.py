@@ -1,0 +1,63 @@
+"""Host-side pieces of bench.py (no GPU): the work model, the CPU-baseline
+leg and the reference arm on a small workload."""
+import json
+import subprocess
+import sys
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import bench
+import oracle
+from expert_routing_grouped_moe_gb300 import synth
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def test_layer_counts_qwen3_shape():
+    cfg = synth.CONFIGS["qwen3_30b_a3b"]
+    c = bench.layer_counts(cfg)
+    N = 4096 * 8
+    F_base = 2 * N * 2048 * 1536 + 2 * N * 768 * 2048
+    F_lora = 2 * N * (2048 * 64 + 64 * 1536 + 768 * 64 + 64 * 2048)
+    assert c["flops"] == 2 * F_base + 3 * F_lora
+    assert abs(c["flops"] / 1e9 - 699.1) < 1.0   # ~699 GFLOP per fwd+bwd step
+    assert c["kernels"]["gate_up"] == ("tensor", 2 * N * 2048 * 1536 + 2 * N * 64 * 1536)
+    assert c["kernels"]["route"][0] == "hbm"
+
+
+def test_layer_counts_shared_rows():
+    cfg = synth.CONFIGS["skewed_shared"]
+    c = bench.layer_counts(cfg)
+    N = 16384 * 5
+    assert c["F_base"] == 2 * N * 2048 * 3072 + 2 * N * 1536 * 2048
+
+
+def test_cpu_baseline_small():
+    cfg = synth.CONFIGS["tiny"]
+    wts = synth.layer_weights(cfg, 1)
+    act = synth.layer_activations(cfg, 1)
+    ids, w = oracle.router_topk(act["logits"].numpy(), cfg.k)
+    P, X, ids, w, dY = bench.oracle_inputs(cfg, wts, act, ids, w)
+    out = bench.cpu_baseline(cfg, P, X, ids, w, dY, budget_s=0.2)
+    assert out["value"] > 0 and out["kind"] == "oracle" and out["cores"] >= 1
+    assert "tokens" in out["sample"]
+
+
+def test_reference_arm_json_line():
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference",
+                        "--config", "tiny", "--steps", "2", "--warmup", "1"],
+                       capture_output=True, text=True, timeout=300, cwd=ROOT)
+    assert r.returncode == 0, r.stderr
+    line = json.loads(r.stdout.strip().splitlines()[-1])
+    assert line["impl"] == "reference" and line["unit"] == "tokens/s" and line["value"] > 0
+    assert line["e2e"]["h2d_bytes_per_step"] == 0
+    assert line["cpu_baseline"]["kind"] == "oracle"
+
+
+def test_clock_sampler_parses_lines():
+    s = bench.ClockSampler("GPU-abc")
+    s.proc = None
+    assert s.stop()["sm_mhz"] is None
