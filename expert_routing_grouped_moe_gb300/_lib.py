@@ -30,6 +30,7 @@ EXPORTED = (
     "moe_permute", "moe_unpermute_combine", "moe_lora_grouped_mlp_fwd",
     "moe_mlp_bwd_workspace_size", "moe_lora_grouped_mlp_bwd", "moe_status",
     "moe_last_error", "moe_abi_version", "moe_kernel_name", "moe_probe_arm", "moe_probe_count",
+    "moe_route_noalloc",
 )
 
 
@@ -90,6 +91,7 @@ def load(path: str = LIB_PATH):
             "moe_probe_arm": (ctypes.c_int, [ctypes.c_char_p, ctypes.POINTER(_P),
                                              ctypes.POINTER(_P), _I]),
             "moe_probe_count": (_I, [ctypes.c_char_p]),
+            "moe_route_noalloc": (ctypes.c_int, [_P, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P]),
         }
         for name, (res, args) in sig.items():
             fn = getattr(lib, name)
@@ -168,6 +170,17 @@ def moe_route(ids, E, shared_expert, counts, offsets, tile_off, sorted_src, dest
                             _i32(tile_off, "tile_off"), _i32(sorted_src, "sorted_src"),
                             _i32(dest_pos, "dest_pos"), _ptr(ws, name="ws"),
                             ws.numel() * ws.element_size(), _stream(stream)), "moe_route")
+
+
+def moe_route_noalloc(ids, E, shared_expert, counts, offsets, tile_off, sorted_src, dest_pos,
+                      stream=None):
+    """moe_route with its scratch inside the library (no workspace argument)."""
+    T, k = ids.shape
+    _check(load().moe_route_noalloc(_i32(ids, "ids"), T, k, int(E), 1 if shared_expert else 0,
+                                    _i32(counts, "counts"), _i32(offsets, "offsets"),
+                                    _i32(tile_off, "tile_off"), _i32(sorted_src, "sorted_src"),
+                                    _i32(dest_pos, "dest_pos"), _stream(stream)),
+           "moe_route_noalloc")
 
 
 def moe_permute(src, K, G, offsets, tile_off, sorted_src, dst, stream=None):

@@ -170,6 +170,19 @@ int check_dims(const moe_dims* dm) {
 
 }  // namespace
 
+int device_status_word(int** out) {
+  DevState* st = nullptr;
+  const int rc = device_state(&st);
+  if (rc != MOE_OK) return rc;
+  *out = st->status;
+  return MOE_OK;
+}
+
+int record_error(int code, const char* msg) {
+  t_err = msg != nullptr ? msg : "";
+  return code;
+}
+
 bool make_map_2d(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols,
                  uint32_t box_rows, uint32_t box_cols) {
   EncodeTiledFn fn = encode_fn();

@@ -109,6 +109,12 @@ struct GemmShape {
 cudaError_t launch_gemm(const GemmShape& shape, const GemmParams& p, int num_sms,
                         cudaStream_t s);
 
+// ---- shared host state (api.cu) ----------------------------------------------
+// Address of the current device's status word (looked up once per device).
+int device_status_word(int** out);
+// Sets the message moe_last_error() returns on this thread; returns `code`.
+int record_error(int code, const char* msg);
+
 // ---- tensor maps (api.cu) ----------------------------------------------------
 // 2D bf16 map over [rows, cols] row-major; box (box_cols, box_rows); 128B swizzle.
 bool make_map_2d(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols,

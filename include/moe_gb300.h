@@ -132,6 +132,28 @@ MOE_API int moe_route(const int32_t* ids, int32_t T, int32_t k, int32_t E, int32
               int32_t* sorted_src, int32_t* dest_pos,
               void* ws, size_t ws_bytes, moe_stream_t stream);
 
+/* moe_route without a workspace argument.  The pages have no counterpart to
+ * this call; it exists for callers that cannot allocate device memory: hosts
+ * that own all device memory through their own pool and hand a library only
+ * raw pointers and a stream (plugin interfaces whose enqueue step must not
+ * allocate, serving runtimes that forbid allocation after start-up).
+ * Same arguments and results as moe_route, minus ws / ws_bytes.  The routing
+ * histogram lives in a 2 MiB array inside this library, which every GPU that
+ * loads the library holds until the process exits; this call itself never
+ * allocates or frees memory.  Limit: E + shared_expert groups times
+ * ceil(T * (k + shared_expert) / 2048) histogram entries must fit in 2^19
+ * (e.g. 128 experts with up to 8,388,608 routed rows); larger problems return
+ * MOE_ERR_WORKSPACE -- use moe_route with a workspace for them.
+ * The first call on a device looks up the array's device address (once per
+ * device, with that device current); make that first call before any stream
+ * capture.  All calls share the one array: calls whose work overlaps on the
+ * GPU (other streams, other threads) race on it and must be serialised by the
+ * caller.  The array is never cleared; no result depends on its old contents. */
+MOE_API int moe_route_noalloc(const int32_t* ids, int32_t T, int32_t k, int32_t E,
+                              int32_t shared_expert, int32_t* counts, int32_t* offsets,
+                              int32_t* tile_off, int32_t* sorted_src, int32_t* dest_pos,
+                              moe_stream_t stream);
+
 /* Row permute (article step 5, "slice the token list by offsets"): for every
  * permuted row p of group g with rank q = p - MOE_TILE_M*tile_off[g]:
  *   dst[p,:] = src[sorted_src[offsets[g] + q] / K, :]   if q < counts[g]
