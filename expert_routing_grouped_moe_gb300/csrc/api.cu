@@ -224,7 +224,7 @@ BwdWs bwd_layout(const moe_dims* dm, void* base) {
   const size_t P = static_cast<size_t>(padded_rows_max(dm->T, K, G));
   const size_t nr = align_up(2 * P * dm->r * 2);
   const size_t ndh = align_up(2 * P * 2 * static_cast<size_t>(dm->f) * 2);
-  const size_t nparts = (dm->f + 255) / 256;
+  const size_t nparts = static_cast<size_t>(kDwPartsPerTile) * ((dm->f + 255) / 256);
   const size_t ndw = align_up(nparts * P * 4);
   BwdWs w{};
   uint8_t* b = static_cast<uint8_t*>(base);
@@ -519,7 +519,8 @@ int moe_lora_grouped_mlp_bwd(const moe_dims* dims, const moe_bf16* dYp, const mo
   const int64_t P = padded_rows_max(dims->T, dims->k + dims->shared_expert, G);
   const GemmParams base = base_params(dims, offsets, tile_off, sorted_src, topk_w, st->status);
   cudaStream_t s = stream;
-  const int nparts = (f + 255) / 256;
+  const int ntiles_f = (f + 255) / 256;
+  const int nparts = kDwPartsPerTile * ntiles_f;
 
   const int64_t Pr = P * r, P2f = P * 2 * f;
   {  // u = dYp B_dn -> pairs us = s*u, uw = s*w*u, xw = w * (s xa_dn)
@@ -534,7 +535,7 @@ int moe_lora_grouped_mlp_bwd(const moe_dims* dims, const moe_bf16* dYp, const mo
     SLICE(p, 0, dYp, P, d, MAP3(p.sl[0].b, W_dn, G, d, f, 64, 64), d);
     SLICE(p, 1, w.us, P, r, MAP3(p.sl[1].b, A_dn, G, r, f, 64, 64), r);
     SLICE(p, 2, w.us + Pr, P, r, MAP3(p.sl[2].b, A_dn, G, r, f, 64, 64), r);
-    p.nslices = 3; p.N = f; p.n_ntiles = nparts;
+    p.nslices = 3; p.N = f; p.n_ntiles = ntiles_f;
     p.fin = h; p.out0 = w.dh; p.ld0 = 2 * f; p.pair = P2f; p.fout = w.dwp; p.fstride = P;
     if ((rc = run_gemm({256, true, false, Epi::kDgradDn}, p, P, st->num_sms, s, "dgrad_dn")))
       return rc;

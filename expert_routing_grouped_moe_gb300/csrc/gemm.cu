@@ -14,14 +14,18 @@
 //               rows of A[rows, M]^T [B_hi | B_lo][rows, 128] -- the per-expert
 //               dA / dB reductions, one CTA per output tile, deterministic.
 //
-// Warp roles (192 threads, one CTA per SM, persistent over tiles):
+// Warp roles (320 threads, one CTA per SM, persistent over tiles):
 //   warp 0      TMA producer: 128B-swizzled A and B tiles into a STAGES-deep
 //               shared-memory ring (mbarrier full/empty handshake)
 //   warp 1      allocates TMEM (2 x BN fp32 columns: double-buffered
 //               accumulators); lane 0 issues tcgen05.mma and tcgen05.commit
-//   warps 2-5   epilogue: tcgen05.ld from TMEM (warp w reads lanes 32*(w%4)..),
+//   warps 2-9   epilogue, two warps per TMEM lane quadrant (warp w reads lanes
+//               32*(w%4)..), each owning half of the tile's columns: tcgen05.ld,
 //               fused SwiGLU / routing-weight scale / SwiGLU backward / LoRA
-//               outputs, stores to global memory; then frees the accumulator.
+//               outputs.  Wide row traffic goes through a per-warp swizzled
+//               shared-memory staging tile so that global loads and stores are
+//               full 128-byte lines.  The accumulator is then freed, so the
+//               epilogue of one tile overlaps the mainloop of the next.
 //
 // Every wait is bounded (see mbar_wait): on timeout the CTA raises an abort
 // flag, drains its own copies and MMAs in flight, frees TMEM, records
@@ -36,26 +40,32 @@ namespace {
 
 constexpr int BM = 128;
 constexpr int BK = 64;  // bf16 elements per 128-byte swizzle row
-constexpr int kThreads = 192;
+constexpr int kEpiWarps = 8;
+constexpr int kThreads = 64 + 32 * kEpiWarps;
 constexpr uint32_t kAStageBytes = BM * BK * 2;  // 16 KB
 constexpr uint32_t kChunkBytes = 64 * 128;      // one [64][64] bf16 swizzle block
+constexpr uint32_t kStgBytes = 32 * 128;        // staging tile per epilogue warp
+constexpr uint32_t kRingBytes = 192 * 1024;
 
 template <int BN>
 struct Cfg {
   static constexpr uint32_t kBStageBytes = BN * BK * 2;
   static constexpr uint32_t kStageBytes = kAStageBytes + kBStageBytes;
-  static constexpr int kStages = BN >= 256 ? 4 : (BN >= 128 ? 6 : 8);
-  static constexpr uint32_t kTmemCols = 2 * BN;  // power of two >= 32
-  static constexpr size_t kSmemBytes =
-      1024 /*alignment slack*/ + static_cast<size_t>(kStages) * kStageBytes + 256 /*barriers*/ +
-      (kMaxExperts + 2) * sizeof(int);
+  static constexpr int kStages = kRingBytes / kStageBytes;  // 4 / 6 / 8 for BN 256 / 128 / 64
+  static constexpr uint32_t kTmemCols = 2 * BN;              // power of two >= 32
+  static constexpr size_t kSmemBytes = 1024 /*alignment slack*/ +
+                                       static_cast<size_t>(kStages) * kStageBytes +
+                                       kEpiWarps * kStgBytes + 256 /*barriers*/;
 };
 
-__device__ __forceinline__ int group_of_tile(const int* s_tile_off, int G, int mt) {
+// Group owning permuted M tile mt: the largest g with tile_off[g] <= mt
+// (non-empty because mt < tile_off[G]).
+__device__ __forceinline__ int group_of_tile(const int32_t* __restrict__ tile_off, int G,
+                                             int mt) {
   int lo = 0, hi = G - 1;
   while (lo < hi) {
     const int mid = (lo + hi + 1) >> 1;
-    if (s_tile_off[mid] <= mt) lo = mid;
+    if (__ldg(tile_off + mid) <= mt) lo = mid;
     else hi = mid - 1;
   }
   return lo;
@@ -63,9 +73,8 @@ __device__ __forceinline__ int group_of_tile(const int* s_tile_off, int G, int m
 
 // Routing weight of permuted row p in group g (0 for padding rows, 1 for the
 // shared-expert slot).
-__device__ __forceinline__ float row_weight(const GemmParams& p, const int* s_tile_off, int g,
-                                            int64_t row) {
-  const int q = static_cast<int>(row - static_cast<int64_t>(s_tile_off[g]) * BM);
+__device__ __forceinline__ float row_weight(const GemmParams& p, int g, int64_t row) {
+  const int q = static_cast<int>(row - static_cast<int64_t>(__ldg(p.tile_off + g)) * BM);
   const int off = __ldg(p.offsets + g);
   const int cnt = __ldg(p.offsets + g + 1) - off;
   if (q >= cnt) return 0.f;
@@ -80,15 +89,21 @@ __device__ __forceinline__ void store8(uint16_t* dst, const float (&v)[8]) {
                                               pack_bf16x2(v[4], v[5]), pack_bf16x2(v[6], v[7]));
 }
 // hi = bf16(v), lo = bf16(v - hi): the pair holds ~16 significant bits of v.
-__device__ __forceinline__ void store8_pair(uint16_t* hi, int64_t pair, const float (&v)[8]) {
+__device__ __forceinline__ void split8(const float* v, uint4& hi, uint4& lo) {
   uint32_t h[4], l[4];
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
     h[i] = pack_bf16x2(v[2 * i], v[2 * i + 1]);
     l[i] = pack_bf16x2(v[2 * i] - bf16lo(h[i]), v[2 * i + 1] - bf16hi(h[i]));
   }
-  *reinterpret_cast<uint4*>(hi) = make_uint4(h[0], h[1], h[2], h[3]);
-  *reinterpret_cast<uint4*>(hi + pair) = make_uint4(l[0], l[1], l[2], l[3]);
+  hi = make_uint4(h[0], h[1], h[2], h[3]);
+  lo = make_uint4(l[0], l[1], l[2], l[3]);
+}
+__device__ __forceinline__ void store8_pair(uint16_t* hi, int64_t pair, const float (&v)[8]) {
+  uint4 a, b;
+  split8(v, a, b);
+  *reinterpret_cast<uint4*>(hi) = a;
+  *reinterpret_cast<uint4*>(hi + pair) = b;
 }
 __device__ __forceinline__ void load8(const uint16_t* src, float (&v)[8]) {
   const uint4 x = __ldg(reinterpret_cast<const uint4*>(src));
@@ -99,18 +114,87 @@ __device__ __forceinline__ void load8(const uint16_t* src, float (&v)[8]) {
     v[2 * i + 1] = bf16hi(w[i]);
   }
 }
-__device__ __forceinline__ void load8f(const float* src, float (&v)[8]) {
-  const float4 a = __ldg(reinterpret_cast<const float4*>(src));
-  const float4 b = __ldg(reinterpret_cast<const float4*>(src) + 1);
-  v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
-  v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
-}
-__device__ __forceinline__ void store8f(float* dst, const float (&v)[8]) {
-  reinterpret_cast<float4*>(dst)[0] = make_float4(v[0], v[1], v[2], v[3]);
-  reinterpret_cast<float4*>(dst)[1] = make_float4(v[4], v[5], v[6], v[7]);
+__device__ __forceinline__ uint4 f4_as_u4(float a, float b, float c, float d) {
+  return make_uint4(__float_as_uint(a), __float_as_uint(b), __float_as_uint(c),
+                    __float_as_uint(d));
 }
 
 __device__ __forceinline__ float sigmoidf_(float z) { return 1.f / (1.f + __expf(-z)); }
+
+// ------------------------------------------------------------ staging tile
+// A warp's staging tile is 32 rows x 128 bytes (8 chunks of 16 B) with the
+// chunk index XOR-swizzled by the row, so both a thread writing its own row
+// and a warp reading 4 rows x 8 chunks touch every bank group once.
+__device__ __forceinline__ uint32_t stg_at(uint32_t stg, int r, int c) {
+  return stg + r * 128 + (((c ^ r) & 7) << 4);
+}
+__device__ __forceinline__ void sts128(uint32_t a, const uint4& v) {
+  asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(a), "r"(v.x), "r"(v.y), "r"(v.z),
+               "r"(v.w)
+               : "memory");
+}
+__device__ __forceinline__ uint4 lds128(uint32_t a) {
+  uint4 v;
+  asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "r"(a)
+               : "memory");
+  return v;
+}
+
+// The 8 chunks of a staging row split into `nplanes` planes of `cpp` chunks
+// (cpp * nplanes <= 8); plane i of row r lives at base[i] + r * ld (bytes),
+// of which the first `valid` bytes exist (the rest of the plane is masked).
+struct Planes {
+  char* b0;
+  char* b1;
+  char* b2;
+  char* b3;
+  int64_t ld;
+  int cpp_log2;
+  int nplanes;
+  int valid;
+  int nrows = 32;  // rows of the tile that exist
+};
+__device__ __forceinline__ char* plane_base(const Planes& pl, int plane) {
+  return plane == 0 ? pl.b0 : plane == 1 ? pl.b1 : plane == 2 ? pl.b2 : pl.b3;
+}
+
+// Coalesced store of the warp's staging tile: 4 rows x 8 chunks per step.
+__device__ __forceinline__ void stg_flush(uint32_t stg, int lane, const Planes& pl) {
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const int r = i * 4 + (lane >> 3);
+    const int c = lane & 7;
+    const int plane = c >> pl.cpp_log2;
+    const int sub = c & ((1 << pl.cpp_log2) - 1);
+    const uint4 v = lds128(stg_at(stg, r, c));
+    if (plane < pl.nplanes && sub * 16 < pl.valid && r < pl.nrows)
+      *reinterpret_cast<uint4*>(plane_base(pl, plane) + r * pl.ld + sub * 16) = v;
+  }
+}
+// Coalesced load into registers (issue), then into the staging tile (commit).
+__device__ __forceinline__ void stg_fetch(uint4 (&regs)[8], int lane, const Planes& pl) {
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const int r = i * 4 + (lane >> 3);
+    const int c = lane & 7;
+    const int plane = c >> pl.cpp_log2;
+    const int sub = c & ((1 << pl.cpp_log2) - 1);
+    regs[i] = (plane < pl.nplanes && sub * 16 < pl.valid)
+                  ? __ldg(reinterpret_cast<const uint4*>(plane_base(pl, plane) + r * pl.ld +
+                                                         sub * 16))
+                  : make_uint4(0, 0, 0, 0);
+  }
+}
+__device__ __forceinline__ void stg_commit(uint32_t stg, int lane, const uint4 (&regs)[8]) {
+#pragma unroll
+  for (int i = 0; i < 8; ++i) sts128(stg_at(stg, i * 4 + (lane >> 3), lane & 7), regs[i]);
+}
+
+__device__ __forceinline__ int clamp_bytes(int64_t v, int hi) {
+  return v <= 0 ? 0 : (v >= hi ? hi : static_cast<int>(v));
+}
 
 // Tile coordinates shared by all roles.
 struct TileInfo {
@@ -123,12 +207,12 @@ struct TileInfo {
 };
 
 template <bool WGRAD>
-__device__ __forceinline__ TileInfo tile_info(const GemmParams& p, const int* s_tile_off, int t) {
+__device__ __forceinline__ TileInfo tile_info(const GemmParams& p, int t) {
   TileInfo ti;
   if (!WGRAD) {
     ti.mt = t / p.n_ntiles;
     ti.nt = t - ti.mt * p.n_ntiles;
-    ti.g = group_of_tile(s_tile_off, p.G, ti.mt);
+    ti.g = group_of_tile(p.tile_off, p.G, ti.mt);
     ti.nk = 0;
     for (int s = 0; s < p.nslices; ++s) ti.nk += (p.sl[s].K + BK - 1) / BK;
     ti.rt = 0;
@@ -137,9 +221,10 @@ __device__ __forceinline__ TileInfo tile_info(const GemmParams& p, const int* s_
     ti.g = t / p.n_ntiles;
     ti.mt = t - ti.g * p.n_ntiles;
     ti.nt = 0;
-    ti.rt = s_tile_off[ti.g + 1] - s_tile_off[ti.g];
+    const int t0 = __ldg(p.tile_off + ti.g);
+    ti.rt = __ldg(p.tile_off + ti.g + 1) - t0;
     ti.nk = ti.rt * (BM / BK) * p.nslices;
-    ti.rb = static_cast<int64_t>(s_tile_off[ti.g]) * BM;
+    ti.rb = static_cast<int64_t>(t0) * BM;
   }
   return ti;
 }
@@ -158,6 +243,252 @@ __device__ __forceinline__ void rows_kblock(const GemmParams& p, int kb, int& s,
   kext = p.sl[s].K - kc;
 }
 
+// ------------------------------------------------------------- epilogues
+// Each epilogue warp owns 32 accumulator rows (TMEM quadrant q) and one half
+// (hf) of the tile's columns.  `tq` is the TMEM address of its rows' column 0,
+// `row0` the permuted row of its first row, `lane` its row within the 32.
+
+template <int BN>
+__device__ __forceinline__ void epi_swiglu(const GemmParams& p, const TileInfo& ti, uint32_t tq,
+                                           int hf, int64_t row0, int lane, uint32_t stg) {
+  // accumulator columns [0, BN/2) = gate, [BN/2, BN) = up of the same features;
+  // this warp: features hf*BN/4 + [0, BN/4)
+  const int f = p.N;
+#pragma unroll 1
+  for (int sub = 0; sub < BN / 4; sub += 16) {
+    const int cg = hf * (BN / 4) + sub;
+    float g[16], u[16], a[16];
+    tmem_ld16(tq + cg, g);
+    tmem_ld16(tq + BN / 2 + cg, u);
+#pragma unroll
+    for (int i = 0; i < 16; ++i) a[i] = g[i] * sigmoidf_(g[i]) * u[i];
+    const int j0 = ti.nt * (BN / 2) + cg;
+    // h (fp32): [gate 16 | up 16]
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      sts128(stg_at(stg, lane, c), f4_as_u4(g[4 * c], g[4 * c + 1], g[4 * c + 2], g[4 * c + 3]));
+      sts128(stg_at(stg, lane, 4 + c),
+             f4_as_u4(u[4 * c], u[4 * c + 1], u[4 * c + 2], u[4 * c + 3]));
+    }
+    __syncwarp();
+    {
+      float* hb = p.fout + row0 * p.ld0;
+      Planes pl{reinterpret_cast<char*>(hb + j0), reinterpret_cast<char*>(hb + f + j0), nullptr,
+                nullptr, p.ld0 * 4, 2, 2, clamp_bytes(static_cast<int64_t>(f - j0) * 4, 64)};
+      stg_flush(stg, lane, pl);
+    }
+    __syncwarp();
+    // act pair (bf16): [hi 16 | lo 16]
+    uint4 h0, l0, h1, l1;
+    split8(a, h0, l0);
+    split8(a + 8, h1, l1);
+    sts128(stg_at(stg, lane, 0), h0);
+    sts128(stg_at(stg, lane, 1), h1);
+    sts128(stg_at(stg, lane, 2), l0);
+    sts128(stg_at(stg, lane, 3), l1);
+    __syncwarp();
+    {
+      uint16_t* ab = p.out0 + row0 * static_cast<int64_t>(f) + j0;
+      Planes pl{reinterpret_cast<char*>(ab), reinterpret_cast<char*>(ab + p.pair), nullptr,
+                nullptr, static_cast<int64_t>(f) * 2, 1, 2,
+                clamp_bytes(static_cast<int64_t>(f - j0) * 2, 32)};
+      stg_flush(stg, lane, pl);
+    }
+    __syncwarp();
+  }
+}
+
+template <int BN, bool SCALE>
+__device__ __forceinline__ void epi_store(const GemmParams& p, const TileInfo& ti, uint32_t tq,
+                                          int hf, int64_t row0, int lane, uint32_t stg) {
+  const float w = SCALE ? row_weight(p, ti.g, row0 + lane) : 1.f;
+#pragma unroll 1
+  for (int c0 = hf * (BN / 2); c0 < (hf + 1) * (BN / 2); c0 += 64) {
+#pragma unroll
+    for (int q4 = 0; q4 < 4; ++q4) {
+      float v[16];
+      tmem_ld16(tq + c0 + 16 * q4, v);
+      float a[8], b[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        a[i] = w * v[i];
+        b[i] = w * v[8 + i];
+      }
+      sts128(stg_at(stg, lane, 2 * q4),
+             make_uint4(pack_bf16x2(a[0], a[1]), pack_bf16x2(a[2], a[3]),
+                        pack_bf16x2(a[4], a[5]), pack_bf16x2(a[6], a[7])));
+      sts128(stg_at(stg, lane, 2 * q4 + 1),
+             make_uint4(pack_bf16x2(b[0], b[1]), pack_bf16x2(b[2], b[3]),
+                        pack_bf16x2(b[4], b[5]), pack_bf16x2(b[6], b[7])));
+    }
+    __syncwarp();
+    const int j0 = ti.nt * BN + c0;
+    Planes pl{reinterpret_cast<char*>(p.out0 + row0 * p.ld0 + j0), nullptr, nullptr, nullptr,
+              p.ld0 * 2, 3, 1, clamp_bytes(static_cast<int64_t>(p.N - j0) * 2, 128)};
+    stg_flush(stg, lane, pl);
+    __syncwarp();
+  }
+}
+
+template <int BN>
+__device__ __forceinline__ void epi_dgrad_dn(const GemmParams& p, const TileInfo& ti, uint32_t tq,
+                                             int hf, int64_t row0, int lane, uint32_t stg) {
+  // acc = g = dY W_dn + s (dY B_dn) A_dn (unscaled by the routing weight);
+  // this warp: columns hf*BN/2 + [0, BN/2) in chunks of 16
+  const int f = p.N;
+  const float w = row_weight(p, ti.g, row0 + lane);
+  const float* hb = p.fin + row0 * p.ld0;     // h [rows, 2f] fp32
+  uint16_t* db = p.out0 + row0 * p.ld0;       // dh pair [rows, 2f]
+  constexpr int kSubs = (BN / 2) / 16;
+  auto h_planes = [&](int j0) {
+    return Planes{reinterpret_cast<char*>(const_cast<float*>(hb + j0)),
+                  reinterpret_cast<char*>(const_cast<float*>(hb + f + j0)), nullptr, nullptr,
+                  p.ld0 * 4, 2, 2, clamp_bytes(static_cast<int64_t>(f - j0) * 4, 64)};
+  };
+  const int jbase = ti.nt * BN + hf * (BN / 2);
+  uint4 pre[8];
+  stg_fetch(pre, lane, h_planes(jbase));
+  stg_commit(stg, lane, pre);
+  __syncwarp();
+  float dot = 0.f;
+#pragma unroll 1
+  for (int sub = 0; sub < kSubs; ++sub) {
+    const int j0 = jbase + sub * 16;
+    float gt[16], up[16], gr[16];
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      const uint4 x = lds128(stg_at(stg, lane, c));
+      const uint4 y = lds128(stg_at(stg, lane, 4 + c));
+      gt[4 * c] = __uint_as_float(x.x); gt[4 * c + 1] = __uint_as_float(x.y);
+      gt[4 * c + 2] = __uint_as_float(x.z); gt[4 * c + 3] = __uint_as_float(x.w);
+      up[4 * c] = __uint_as_float(y.x); up[4 * c + 1] = __uint_as_float(y.y);
+      up[4 * c + 2] = __uint_as_float(y.z); up[4 * c + 3] = __uint_as_float(y.w);
+    }
+    if (sub + 1 < kSubs) stg_fetch(pre, lane, h_planes(j0 + 16));  // next chunk in flight
+    tmem_ld16(tq + hf * (BN / 2) + sub * 16, gr);
+    float dg[16], du[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      const float sg = sigmoidf_(gt[i]);
+      const float sl = gt[i] * sg;
+      dot = fmaf(sl * up[i], gr[i], dot);
+      const float da = w * gr[i];
+      dg[i] = da * up[i] * sg * (1.f + gt[i] * (1.f - sg));
+      du[i] = da * sl;
+    }
+    __syncwarp();
+    uint4 a0, a1, b0, b1;
+    split8(dg, a0, b0);
+    split8(dg + 8, a1, b1);
+    sts128(stg_at(stg, lane, 0), a0);
+    sts128(stg_at(stg, lane, 1), a1);
+    sts128(stg_at(stg, lane, 2), b0);
+    sts128(stg_at(stg, lane, 3), b1);
+    split8(du, a0, b0);
+    split8(du + 8, a1, b1);
+    sts128(stg_at(stg, lane, 4), a0);
+    sts128(stg_at(stg, lane, 5), a1);
+    sts128(stg_at(stg, lane, 6), b0);
+    sts128(stg_at(stg, lane, 7), b1);
+    __syncwarp();
+    {
+      Planes pl{reinterpret_cast<char*>(db + j0), reinterpret_cast<char*>(db + p.pair + j0),
+                reinterpret_cast<char*>(db + f + j0),
+                reinterpret_cast<char*>(db + p.pair + f + j0), p.ld0 * 2, 1, 4,
+                clamp_bytes(static_cast<int64_t>(f - j0) * 2, 32)};
+      stg_flush(stg, lane, pl);
+    }
+    __syncwarp();
+    if (sub + 1 < kSubs) {
+      stg_commit(stg, lane, pre);
+      __syncwarp();
+    }
+  }
+  p.fout[static_cast<int64_t>(ti.nt * kDwPartsPerTile + hf) * p.fstride + row0 + lane] = dot;
+}
+
+template <int BN>
+__device__ __forceinline__ void epi_lora(const GemmParams& p, const TileInfo& ti, uint32_t tq,
+                                         int hf, int64_t row0, int lane) {
+  const int64_t row = row0 + lane;
+  const bool need_w = p.out1 != nullptr || p.out2 != nullptr;
+  const float w = need_w ? row_weight(p, ti.g, row) : 0.f;
+  const float s = p.scale;
+#pragma unroll 1
+  for (int c0 = hf * (BN / 2); c0 < (hf + 1) * (BN / 2); c0 += 16) {
+    float v16[16];
+    tmem_ld16(tq + c0, v16);
+#pragma unroll
+    for (int h8 = 0; h8 < 2; ++h8) {
+      const int j = ti.nt * BN + c0 + h8 * 8;
+      if (j < p.N) {
+        const int64_t o = row * p.ld0 + j;
+        float ov[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) ov[i] = s * v16[h8 * 8 + i];
+        store8_pair(p.out0 + o, p.pair, ov);
+        if (p.out1 != nullptr) {
+#pragma unroll
+          for (int i = 0; i < 8; ++i) ov[i] *= w;
+          store8_pair(p.out1 + o, p.pair, ov);
+        }
+        if (p.out2 != nullptr) {
+          float ah[8], al[8];
+          load8(p.aux0 + o, ah);
+          load8(p.aux0 + p.pair + o, al);
+#pragma unroll
+          for (int i = 0; i < 8; ++i) ah[i] = w * (ah[i] + al[i]);
+          store8_pair(p.out2 + o, p.pair, ah);
+        }
+      }
+    }
+  }
+}
+
+__device__ __forceinline__ void epi_wgrad(const GemmParams& p, const TileInfo& ti, uint32_t tq,
+                                          int hf, int q, int lane, uint32_t stg) {
+  // columns [0,64) = A * B_hi, [64,128) = A * B_lo; this warp: n in hf*32 + [0,32)
+  const int m0 = ti.mt * BM + q * 32;
+  const int m = m0 + lane;
+  const bool has = ti.nk > 0;
+  float* fo = p.fout + static_cast<int64_t>(ti.g) * p.fstride;
+  float v[32];
+#pragma unroll
+  for (int c0 = 0; c0 < 32; c0 += 16) {
+    float vh[16], vl[16];
+    if (has) {
+      tmem_ld16(tq + hf * 32 + c0, vh);
+      tmem_ld16(tq + 64 + hf * 32 + c0, vl);
+    } else {
+#pragma unroll
+      for (int i = 0; i < 16; ++i) vh[i] = vl[i] = 0.f;
+    }
+#pragma unroll
+    for (int i = 0; i < 16; ++i) v[c0 + i] = vh[i] + vl[i];
+  }
+  if (p.transpose_out) {
+    // fout[g][n][m]: consecutive lanes write consecutive m (128-byte lines)
+    if (m < p.M) {
+#pragma unroll
+      for (int i = 0; i < 32; ++i) {
+        const int n = hf * 32 + i;
+        if (n < p.N) fo[static_cast<int64_t>(n) * p.M + m] = v[i];
+      }
+    }
+  } else {
+    // fout[g][m][n]: stage the warp's 32 rows x 32 columns, store whole lines
+#pragma unroll
+    for (int c = 0; c < 8; ++c)
+      sts128(stg_at(stg, lane, c), f4_as_u4(v[4 * c], v[4 * c + 1], v[4 * c + 2], v[4 * c + 3]));
+    __syncwarp();
+    Planes pl{reinterpret_cast<char*>(fo + static_cast<int64_t>(m0) * p.N + hf * 32), nullptr,
+              nullptr, nullptr, static_cast<int64_t>(p.N) * 4, 3, 1,
+              clamp_bytes(static_cast<int64_t>(p.N - hf * 32) * 4, 128), p.M - m0};
+    stg_flush(stg, lane, pl);
+    __syncwarp();
+  }
+}
+
 template <int BN, bool B_MN, bool WGRAD, int EPI>
 __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant__ GemmParams p) {
   using C = Cfg<BN>;
@@ -167,14 +498,14 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
   const uint32_t raw_addr = smem_u32(smem_raw);
   uint8_t* smem = smem_raw + ((1024 - (raw_addr & 1023)) & 1023);
   uint8_t* ring = smem;
-  uint64_t* full_bar = reinterpret_cast<uint64_t*>(ring + S * C::kStageBytes);
+  uint8_t* stage_tiles = ring + S * C::kStageBytes;
+  uint64_t* full_bar = reinterpret_cast<uint64_t*>(stage_tiles + kEpiWarps * kStgBytes);
   uint64_t* empty_bar = full_bar + S;
   uint64_t* tfull_bar = empty_bar + S;
   uint64_t* tempty_bar = tfull_bar + 2;
   uint64_t* drain_bar = tempty_bar + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain_bar + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
-  int* s_tile_off = reinterpret_cast<int*>(tmem_slot + 4);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -186,7 +517,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(tfull_bar + i, 1);
-      mbar_init(tempty_bar + i, 4 * 32);
+      mbar_init(tempty_bar + i, kEpiWarps * 32);
     }
     mbar_init(drain_bar, 1);
     *abort_flag = 0;
@@ -206,13 +537,12 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
     tmem_alloc(tmem_slot, C::kTmemCols);
     tmem_relinquish();
   }
-  for (int i = threadIdx.x; i <= p.G; i += kThreads) s_tile_off[i] = __ldg(p.tile_off + i);
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
 
   const int num_tiles =
-      WGRAD ? p.G * p.n_ntiles : min(s_tile_off[p.G] * p.n_ntiles, p.max_tiles);
+      WGRAD ? p.G * p.n_ntiles : min(__ldg(p.tile_off + p.G) * p.n_ntiles, p.max_tiles);
 
   if (warp == 0 && lane == 0) {
     // ------------------------------------------------------------ producer
@@ -223,7 +553,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
     for (int i = 0; i < S; ++i) armed[i] = -1;
     bool ok = true;
     for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
-      const TileInfo ti = tile_info<WGRAD>(p, s_tile_off, t);
+      const TileInfo ti = tile_info<WGRAD>(p, t);
       for (int kb = 0; kb < ti.nk; ++kb) {
         if (!mbar_wait(empty_bar + stage, phase ^ 1u, abort_flag, kWaitTimeoutNs)) {
           ok = false;
@@ -284,7 +614,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
     int local = 0;
     bool ok = true;
     for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x, ++local) {
-      const TileInfo ti = tile_info<WGRAD>(p, s_tile_off, t);
+      const TileInfo ti = tile_info<WGRAD>(p, t);
       const int buf = local & 1;
       const uint32_t use = static_cast<uint32_t>(local >> 1);
       if (!mbar_wait(tempty_bar + buf, (use & 1u) ^ 1u, abort_flag, kWaitTimeoutNs)) break;
@@ -329,162 +659,32 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
     mbar_wait(drain_bar, 0, &never, 200000000ull);
   } else if (warp >= 2) {
     // ----------------------------------------------------------- epilogue
-    const int q = warp & 3;               // TMEM lane quadrant of this warp
-    const int r_in_tile = q * 32 + lane;  // accumulator row
+    const int ew = warp - 2;
+    const int q = warp & 3;   // TMEM lane quadrant of this warp
+    const int hf = ew >> 2;   // column half owned by this warp
+    const uint32_t stg = smem_u32(stage_tiles + ew * kStgBytes);
     int local = 0;
     for (int t = blockIdx.x; t < num_tiles; t += gridDim.x, ++local) {
-      const TileInfo ti = tile_info<WGRAD>(p, s_tile_off, t);
+      const TileInfo ti = tile_info<WGRAD>(p, t);
       const int buf = local & 1;
       const uint32_t use = static_cast<uint32_t>(local >> 1);
       if (!mbar_wait(tfull_bar + buf, use & 1u, abort_flag, kWaitTimeoutNs)) break;
       tc_fence_after();
-      const uint32_t tbase =
+      const uint32_t tq =
           tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(buf * BN);
-
+      const int64_t row0 = static_cast<int64_t>(ti.mt) * BM + q * 32;
       if constexpr (WGRAD) {
-        // columns [0,64) = A * B_hi, [64,128) = A * B_lo
-        const int m = ti.mt * BM + r_in_tile;
-        const bool has = ti.nk > 0;
-        float* fo = p.fout + static_cast<int64_t>(ti.g) * p.fstride;
-#pragma unroll 1
-        for (int c0 = 0; c0 < 64; c0 += 16) {
-          float vh[16], vl[16];
-          if (has) {
-            tmem_ld16(tbase + c0, vh);
-            tmem_ld16(tbase + 64 + c0, vl);
-          } else {
-#pragma unroll
-            for (int i = 0; i < 16; ++i) vh[i] = vl[i] = 0.f;
-          }
-          if (m < p.M) {
-#pragma unroll
-            for (int i = 0; i < 16; ++i) {
-              const int n = c0 + i;
-              if (n < p.N) {
-                const float v = vh[i] + vl[i];
-                if (p.transpose_out) fo[static_cast<int64_t>(n) * p.M + m] = v;
-                else fo[static_cast<int64_t>(m) * p.N + n] = v;
-              }
-            }
-          }
-        }
-      } else {
-        const int64_t row = static_cast<int64_t>(ti.mt) * BM + r_in_tile;
-        if constexpr (EPI == static_cast<int>(Epi::kSwiGLU)) {
-          // accumulator columns [0, BN/2) = gate, [BN/2, BN) = up of the same features
-          const int f = p.N;
-          float* hrow = p.fout + row * p.ld0;                         // h [rows, 2f] fp32
-          uint16_t* arow = p.out0 + row * static_cast<int64_t>(f);    // act pair [rows, f]
-#pragma unroll 1
-          for (int c0 = 0; c0 < BN / 2; c0 += 16) {
-            float g16[16], u16[16];
-            tmem_ld16(tbase + c0, g16);
-            tmem_ld16(tbase + BN / 2 + c0, u16);
-#pragma unroll
-            for (int h8 = 0; h8 < 2; ++h8) {
-              const int j = ti.nt * (BN / 2) + c0 + h8 * 8;
-              if (j < f) {
-                float gv[8], uv[8], av[8];
-#pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                  gv[i] = g16[h8 * 8 + i];
-                  uv[i] = u16[h8 * 8 + i];
-                  av[i] = gv[i] * sigmoidf_(gv[i]) * uv[i];
-                }
-                store8f(hrow + j, gv);
-                store8f(hrow + f + j, uv);
-                store8_pair(arow + j, p.pair, av);
-              }
-            }
-          }
-        } else if constexpr (EPI == static_cast<int>(Epi::kScaleW) ||
-                             EPI == static_cast<int>(Epi::kStore)) {
-          const float w =
-              EPI == static_cast<int>(Epi::kScaleW) ? row_weight(p, s_tile_off, ti.g, row) : 1.f;
-          uint16_t* orow = p.out0 + row * p.ld0;
-#pragma unroll 1
-          for (int c0 = 0; c0 < BN; c0 += 16) {
-            float v16[16];
-            tmem_ld16(tbase + c0, v16);
-#pragma unroll
-            for (int h8 = 0; h8 < 2; ++h8) {
-              const int j = ti.nt * BN + c0 + h8 * 8;
-              if (j < p.N) {
-                float ov[8];
-#pragma unroll
-                for (int i = 0; i < 8; ++i) ov[i] = w * v16[h8 * 8 + i];
-                store8(orow + j, ov);
-              }
-            }
-          }
-        } else if constexpr (EPI == static_cast<int>(Epi::kLoRA)) {
-          const bool need_w = p.out1 != nullptr || p.out2 != nullptr;
-          const float w = need_w ? row_weight(p, s_tile_off, ti.g, row) : 0.f;
-          const float s = p.scale;
-#pragma unroll 1
-          for (int c0 = 0; c0 < BN; c0 += 16) {
-            float v16[16];
-            tmem_ld16(tbase + c0, v16);
-#pragma unroll
-            for (int h8 = 0; h8 < 2; ++h8) {
-              const int j = ti.nt * BN + c0 + h8 * 8;
-              if (j < p.N) {
-                const int64_t o = row * p.ld0 + j;
-                float ov[8];
-#pragma unroll
-                for (int i = 0; i < 8; ++i) ov[i] = s * v16[h8 * 8 + i];
-                store8_pair(p.out0 + o, p.pair, ov);
-                if (p.out1 != nullptr) {
-#pragma unroll
-                  for (int i = 0; i < 8; ++i) ov[i] *= w;
-                  store8_pair(p.out1 + o, p.pair, ov);
-                }
-                if (p.out2 != nullptr) {
-                  float ah[8], al[8];
-                  load8(p.aux0 + o, ah);
-                  load8(p.aux0 + p.pair + o, al);
-#pragma unroll
-                  for (int i = 0; i < 8; ++i) ah[i] = w * (ah[i] + al[i]);
-                  store8_pair(p.out2 + o, p.pair, ah);
-                }
-              }
-            }
-          }
-        } else if constexpr (EPI == static_cast<int>(Epi::kDgradDn)) {
-          // acc = g = dY W_dn + s (dY B_dn) A_dn (unscaled by the routing weight)
-          const int f = p.N;
-          const float w = row_weight(p, s_tile_off, ti.g, row);
-          const float* hrow = p.fin + row * p.ld0;  // h [rows, 2f] fp32
-          uint16_t* drow = p.out0 + row * p.ld0;    // dh pair [rows, 2f]
-          float dot = 0.f;
-#pragma unroll 1
-          for (int c0 = 0; c0 < BN; c0 += 16) {
-            float v16[16];
-            tmem_ld16(tbase + c0, v16);
-#pragma unroll
-            for (int h8 = 0; h8 < 2; ++h8) {
-              const int j = ti.nt * BN + c0 + h8 * 8;
-              if (j < f) {
-                float gt[8], up[8], dg[8], du[8];
-                load8f(hrow + j, gt);
-                load8f(hrow + f + j, up);
-#pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                  const float gr = v16[h8 * 8 + i];
-                  const float sg = sigmoidf_(gt[i]);
-                  const float sl = gt[i] * sg;
-                  dot = fmaf(sl * up[i], gr, dot);
-                  const float da = w * gr;
-                  dg[i] = da * up[i] * sg * (1.f + gt[i] * (1.f - sg));
-                  du[i] = da * sl;
-                }
-                store8_pair(drow + j, p.pair, dg);
-                store8_pair(drow + f + j, p.pair, du);
-              }
-            }
-          }
-          p.fout[static_cast<int64_t>(ti.nt) * p.fstride + row] = dot;
-        }
+        epi_wgrad(p, ti, tq, hf, q, lane, stg);
+      } else if constexpr (EPI == static_cast<int>(Epi::kSwiGLU)) {
+        epi_swiglu<BN>(p, ti, tq, hf, row0, lane, stg);
+      } else if constexpr (EPI == static_cast<int>(Epi::kScaleW)) {
+        epi_store<BN, true>(p, ti, tq, hf, row0, lane, stg);
+      } else if constexpr (EPI == static_cast<int>(Epi::kStore)) {
+        epi_store<BN, false>(p, ti, tq, hf, row0, lane, stg);
+      } else if constexpr (EPI == static_cast<int>(Epi::kLoRA)) {
+        epi_lora<BN>(p, ti, tq, hf, row0, lane);
+      } else if constexpr (EPI == static_cast<int>(Epi::kDgradDn)) {
+        epi_dgrad_dn<BN>(p, ti, tq, hf, row0, lane, stg);
       }
       tc_fence_before();
       mbar_arrive(tempty_bar + buf);
@@ -502,6 +702,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
 template <int BN, bool B_MN, bool WGRAD, int EPI>
 cudaError_t launch_one(const GemmParams& p, int num_sms, cudaStream_t s) {
   using C = Cfg<BN>;
+  static_assert(C::kSmemBytes <= 232448, "shared memory budget");
   auto kern = gemm_kernel<BN, B_MN, WGRAD, EPI>;
   cudaError_t e =
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,

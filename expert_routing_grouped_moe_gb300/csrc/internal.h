@@ -62,6 +62,9 @@ enum class Epi : int {
 };
 
 constexpr int kMaxSlices = 4;
+// The down-projection dgrad writes one routing-weight-gradient partial per
+// 256-column tile and column half (two epilogue warps share each row).
+constexpr int kDwPartsPerTile = 2;
 
 // One K-slice of a contraction: D += A_slice * B_slice^T over K columns.
 struct GemmSlice {

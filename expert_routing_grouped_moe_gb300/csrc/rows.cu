@@ -47,19 +47,26 @@ __global__ void __launch_bounds__(256) permute_kernel(
   __syncthreads();
   if (s_cnt < 0) return;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  // each lane moves 8 vectors of a row per step (a 4 KB row of d = 2048 in one
+  // step): all loads issued before the stores
   for (int r = warp * 16; r < warp * 16 + 16; ++r) {
     const int q = s_first + r;
     const int64_t p = static_cast<int64_t>(mt) * kTileM + r;
     uint4* drow = dst + p * d8;
-    if (q < s_cnt) {
-      const int t = __ldg(sorted_src + s_off + q) / K;
-      const uint4* srow = src + static_cast<int64_t>(t) * d8;
-#pragma unroll 4
-      for (int v = lane; v < d8; v += 32) drow[v] = __ldg(srow + v);
-    } else {
-      const uint4 z = make_uint4(0, 0, 0, 0);
-#pragma unroll 4
-      for (int v = lane; v < d8; v += 32) drow[v] = z;
+    const uint4* srow = nullptr;
+    if (q < s_cnt) srow = src + static_cast<int64_t>(__ldg(sorted_src + s_off + q) / K) * d8;
+    for (int v0 = 0; v0 < d8; v0 += 256) {
+      uint4 x[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const int v = v0 + i * 32 + lane;
+        x[i] = (srow != nullptr && v < d8) ? __ldg(srow + v) : make_uint4(0, 0, 0, 0);
+      }
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const int v = v0 + i * 32 + lane;
+        if (v < d8) drow[v] = x[i];
+      }
     }
   }
 }
@@ -110,11 +117,20 @@ __global__ void __launch_bounds__(256) combine_kernel(
   }
   __syncwarp();
   uint4* orow = out + static_cast<int64_t>(t) * d8;
+  // slot rows in groups of 8: all 8 loads of a group in flight at once
   for (int v = lane; v < d8; v += 32) {
     float a[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-    for (int j = 0; j < K; ++j) {
-      const int64_t pr = s_row[warp][j];
-      if (pr >= 0) acc_bf16x8(a, __ldg(rows + pr * d8 + v), s_c[warp][j]);
+    for (int j0 = 0; j0 < K; j0 += 8) {
+      uint4 x[8];
+#pragma unroll
+      for (int jj = 0; jj < 8; ++jj) {
+        const int j = j0 + jj;
+        const int64_t pr = j < K ? s_row[warp][j] : -1;
+        x[jj] = pr >= 0 ? __ldg(rows + pr * d8 + v) : make_uint4(0, 0, 0, 0);
+      }
+#pragma unroll
+      for (int jj = 0; jj < 8; ++jj)
+        if (j0 + jj < K) acc_bf16x8(a, x[jj], s_c[warp][j0 + jj]);
     }
     orow[v] = make_uint4(pack2(a[0], a[1]), pack2(a[2], a[3]), pack2(a[4], a[5]),
                          pack2(a[6], a[7]));
