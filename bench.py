@@ -50,6 +50,7 @@ def parse_args(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget-s", type=float, default=20.0)
     ap.add_argument("--probe-steps", type=int, default=100)
+    ap.add_argument("--no-route-sweep", action="store_true")
     return ap.parse_args(argv)
 
 
@@ -237,6 +238,125 @@ def cpu_baseline(cfg, P, X, ids, w, dY, budget_s):
                           ntok, cfg.T, cfg.slots, dt)}
 
 
+# ---------------------------------------------------------------- e2e / sweep
+
+def run_e2e(torch, layer, X, dY, ids, topw, cfg, steps, main):
+    """ms per step of forward+backward through the public API, inputs copied
+    from pinned host buffers and Y, dX copied back every step."""
+    Xh, dYh = X.cpu().pin_memory(), dY.cpu().pin_memory()
+    idsh, wh = ids.cpu().pin_memory(), topw.cpu().pin_memory()
+    Yh = torch.empty(cfg.T, cfg.d, dtype=torch.bfloat16).pin_memory()
+    dXh = torch.empty(cfg.T, cfg.d, dtype=torch.bfloat16).pin_memory()
+    dev_in = [(torch.empty_like(X), torch.empty_like(dY), torch.empty_like(ids),
+               torch.empty_like(topw)) for _ in range(2)]
+    cs = torch.cuda.Stream()
+    in_ready = [torch.cuda.Event() for _ in range(2)]
+    buf_free = [torch.cuda.Event() for _ in range(2)]
+    fwd_done, bwd_done, y_out, dx_out = (torch.cuda.Event() for _ in range(4))
+    for e in buf_free:
+        e.record(main)
+    y_out.record(main)
+    dx_out.record(main)
+
+    def h2d(i):
+        b = i % 2
+        cs.wait_event(buf_free[b])
+        Xd, dYd, idd, wd = dev_in[b]
+        with torch.cuda.stream(cs):
+            Xd.copy_(Xh, non_blocking=True)
+            idd.copy_(idsh, non_blocking=True)
+            wd.copy_(wh, non_blocking=True)
+            dYd.copy_(dYh, non_blocking=True)
+        in_ready[b].record(cs)
+
+    def step(i):
+        b = i % 2
+        Xd, dYd, idd, wd = dev_in[b]
+        main.wait_event(in_ready[b])
+        main.wait_event(y_out)            # the previous Y has left the device
+        Y = layer.forward(Xd, idd, wd)
+        fwd_done.record(main)
+        cs.wait_event(fwd_done)
+        with torch.cuda.stream(cs):
+            Yh.copy_(Y, non_blocking=True)
+        y_out.record(cs)
+        main.wait_event(dx_out)
+        g = layer.backward(dYd)
+        bwd_done.record(main)
+        buf_free[b].record(main)
+        cs.wait_event(bwd_done)
+        with torch.cuda.stream(cs):
+            dXh.copy_(g["dX"], non_blocking=True)
+        dx_out.record(cs)
+
+    def run(n):
+        h2d(0)
+        for i in range(n):
+            if i + 1 < n:
+                h2d(i + 1)
+            step(i)
+        main.wait_stream(cs)
+
+    run(3)
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(main)
+    cs.wait_event(e0)
+    run(steps)
+    e1.record(main)
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) / steps
+
+
+def routing_sweep(torch, L, synth, dev, peaks, points=((1 << 20, 128, 8), (1 << 18, 64, 4)),
+                  d=2048, reps=5):
+    """Route, permute and combine throughput (algorithmic GB/s) on the routing
+    workload's large points: T tokens, E experts, top-k, bf16 rows of d."""
+    out = []
+    for T, E, k in points:
+        ids = synth.topk_ids(T, E, k, "uniform", seed=7, device=dev)
+        w = synth.combine_weights(T, k, seed=7, device=dev)
+        X = synth.hidden_rows(T, d, seed=7, device=dev)
+        N = T * k
+        counts = torch.empty(E, dtype=torch.int32, device=dev)
+        offsets = torch.empty(E + 1, dtype=torch.int32, device=dev)
+        tile_off = torch.empty(E + 1, dtype=torch.int32, device=dev)
+        src = torch.empty(N, dtype=torch.int32, device=dev)
+        dst = torch.empty(N, dtype=torch.int32, device=dev)
+        ws = torch.empty(L.moe_route_workspace_size(T, k, E), dtype=torch.uint8, device=dev)
+        Xp = torch.empty(N, d, dtype=torch.bfloat16, device=dev)
+        Y = torch.empty(T, d, dtype=torch.bfloat16, device=dev)
+        calls = {
+            "route": (lambda: L.moe_route(ids, E, False, counts, offsets, tile_off, src, dst, ws),
+                      4 * T * k + 8 * N + 12 * E),
+            "permute": (lambda: L.moe_permute(X, k, dst, Xp),
+                        2 * T * d + 2 * N * d + 4 * N),
+            "combine": (lambda: L.moe_unpermute_combine(Xp, dst, k, False, Y, weights=w),
+                        2 * N * d + 2 * T * d + 8 * N + 4 * T * k),
+        }
+        res = {"T": T, "E": E, "k": k, "d": d}
+        for name, (fn, nbytes) in calls.items():
+            fn()
+            torch.cuda.synchronize()
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record()
+            for _ in range(reps):
+                fn()
+            e1.record()
+            torch.cuda.synchronize()
+            ms = e0.elapsed_time(e1) / reps
+            gbs = nbytes / (ms / 1e3) / 1e9
+            res[name] = {"ms": ms, "gbs": gbs, "frac_of_hbm": gbs / peaks["hbm_gbs"]}
+        out.append(res)
+        del Xp, Y, X
+        torch.cuda.empty_cache()
+    if L.moe_status() != L.MOE_OK:
+        raise SystemExit("device status error in the routing sweep")
+    return out
+
+
 # ---------------------------------------------------------------- our arm
 
 def run_ours(args):
@@ -308,40 +428,20 @@ def run_ours(args):
             kstats[n] = {"ms_per_launch": mean, "launches_per_step": per,
                          "share": mean * per / ms}
 
-    # ---- end to end through the public API with host buffers
+    # ---- end to end through the public API with host buffers.  Every step
+    # copies its inputs (X, ids, w, dY) in from pinned host memory and its
+    # results (Y, dX) back out; the copies run on a second stream and overlap
+    # the neighbouring step's compute (double-buffered device inputs).
     e2e_steps = args.e2e_steps or min(args.steps, 200)
-    Xh = X.cpu().pin_memory()
-    dYh = dY.cpu().pin_memory()
-    idsh = ids.cpu().pin_memory()
-    wh = topw.cpu().pin_memory()
-    Yh = torch.empty(cfg.T, cfg.d, dtype=torch.bfloat16).pin_memory()
-    dXh = torch.empty(cfg.T, cfg.d, dtype=torch.bfloat16).pin_memory()
-    Xd, dYd = torch.empty_like(X), torch.empty_like(dY)
-    idsd, wd = torch.empty_like(ids), torch.empty_like(topw)
-    h2d = sum(t.numel() * t.element_size() for t in (Xh, dYh, idsh, wh))
-    d2h = sum(t.numel() * t.element_size() for t in (Yh, dXh))
-
-    def e2e_step():
-        Xd.copy_(Xh, non_blocking=True)
-        idsd.copy_(idsh, non_blocking=True)
-        wd.copy_(wh, non_blocking=True)
-        dYd.copy_(dYh, non_blocking=True)
-        Y = layer.forward(Xd, idsd, wd)
-        Yh.copy_(Y, non_blocking=True)
-        g = layer.backward(dYd)
-        dXh.copy_(g["dX"], non_blocking=True)
-
-    for _ in range(3):
-        e2e_step()
-    torch.cuda.synchronize()
+    e2e_ms = run_e2e(torch, layer, X, dY, ids, topw, cfg, e2e_steps, stream)
+    e2e_ms = max_over_ranks(torch, dist, e2e_ms, dev)
+    h2d = (X.numel() * X.element_size() + dY.numel() * dY.element_size()
+           + ids.numel() * ids.element_size() + topw.numel() * topw.element_size())
+    d2h = 2 * cfg.T * cfg.d * 2
     barrier(dist, torch, dev)
-    e0.record(stream)
-    for _ in range(e2e_steps):
-        e2e_step()
-    e1.record(stream)
-    torch.cuda.synchronize()
-    e2e_ms = max_over_ranks(torch, dist, e0.elapsed_time(e1) / e2e_steps, dev)
-    barrier(dist, torch, dev)
+
+    route_sweep = routing_sweep(torch, L, synth, dev, peaks=load_peaks()[0]) \
+        if (rank == 0 and not args.no_route_sweep) else None
 
     if rank != 0:
         if dist is not None:
@@ -405,6 +505,7 @@ def run_ours(args):
             peak_src, peaks["bf16_tflops_sustained"]),
         "gemm_ms_per_step": gemm_ms,
         "routing": route,
+        "routing_sweep": route_sweep,
         "roofline": roof,
         "kernels": kernels,
         "cpu_baseline": cpu,

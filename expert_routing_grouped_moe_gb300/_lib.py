@@ -26,7 +26,7 @@ MOE_ERR_BAD_IDS = -5
 MOE_ERR_TIMEOUT = -6
 
 EXPORTED = (
-    "moe_padded_rows_max", "moe_router_topk", "moe_route_workspace_size", "moe_route",
+    "moe_router_topk", "moe_route_workspace_size", "moe_route",
     "moe_permute", "moe_unpermute_combine", "moe_lora_grouped_mlp_fwd",
     "moe_mlp_bwd_workspace_size", "moe_lora_grouped_mlp_bwd", "moe_status",
     "moe_last_error", "moe_abi_version", "moe_kernel_name", "moe_probe_arm", "moe_probe_count",
@@ -73,13 +73,12 @@ def load(path: str = LIB_PATH):
                                "expert_routing_grouped_moe_gb300.build.build()" % path)
         lib = ctypes.CDLL(path)
         sig = {
-            "moe_padded_rows_max": (ctypes.c_int64, [_I, _I, _I]),
             "moe_router_topk": (ctypes.c_int, [_P, _I, _I, _I, _P, _P, _P]),
             "moe_route_workspace_size": (_SZ, [_I, _I, _I]),
             "moe_route": (ctypes.c_int, [_P, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _SZ, _P]),
-            "moe_permute": (ctypes.c_int, [_P, _I, _I, _I, _I, _P, _P, _P, _P, _P]),
-            "moe_unpermute_combine": (ctypes.c_int, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I,
-                                                     _P, _P, _P, _P, _P]),
+            "moe_permute": (ctypes.c_int, [_P, _I, _I, _I, _P, _P, _P]),
+            "moe_unpermute_combine": (ctypes.c_int, [_P, _P, _I, _I, _I, _I, _P, _P, _P, _P,
+                                                     _P]),
             "moe_lora_grouped_mlp_fwd": (ctypes.c_int, [ctypes.POINTER(MoeDims)] + [_P] * 18),
             "moe_mlp_bwd_workspace_size": (_SZ, [ctypes.POINTER(MoeDims)]),
             "moe_lora_grouped_mlp_bwd": (ctypes.c_int, [ctypes.POINTER(MoeDims)] + [_P] * 24
@@ -145,13 +144,6 @@ def make_dims(T, d, f, E, k, r, lora_scale, shared_expert=False) -> MoeDims:
 
 # ---------------------------------------------------------------- C ABI calls
 
-def moe_padded_rows_max(T, K, G) -> int:
-    v = load().moe_padded_rows_max(int(T), int(K), int(G))
-    if v < 0:
-        raise ValueError("bad sizes")
-    return int(v)
-
-
 def moe_router_topk(logits, k, ids, weights, stream=None):
     T, E = logits.shape
     _check(load().moe_router_topk(_f32(logits, "logits"), T, E, int(k), _i32(ids, "ids"),
@@ -183,22 +175,19 @@ def moe_route_noalloc(ids, E, shared_expert, counts, offsets, tile_off, sorted_s
            "moe_route_noalloc")
 
 
-def moe_permute(src, K, G, offsets, tile_off, sorted_src, dst, stream=None):
+def moe_permute(src, K, dest_pos, dst, stream=None):
     T, d = src.shape
-    _check(load().moe_permute(_bf(src, "src"), T, d, int(K), int(G), _i32(offsets, "offsets"),
-                              _i32(tile_off, "tile_off"), _i32(sorted_src, "sorted_src"),
+    _check(load().moe_permute(_bf(src, "src"), T, d, int(K), _i32(dest_pos, "dest_pos"),
                               _bf(dst, "dst"), _stream(stream)), "moe_permute")
 
 
-def moe_unpermute_combine(rows, ids, dest_pos, offsets, tile_off, E, shared_expert, out,
-                          weights=None, row_scalars=None, slot_out=None, stream=None):
-    T, k = ids.shape
-    d = out.shape[1]
+def moe_unpermute_combine(rows, dest_pos, k, shared_expert, out, weights=None, row_scalars=None,
+                          slot_out=None, stream=None):
+    T, d = out.shape
     _check(load().moe_unpermute_combine(
-        _bf(rows, "rows"), _i32(ids, "ids"), _i32(dest_pos, "dest_pos"),
-        _i32(offsets, "offsets"), _i32(tile_off, "tile_off"), T, d, k, int(E),
-        1 if shared_expert else 0, _f32(weights, "weights"), _f32(row_scalars, "row_scalars"),
-        _f32(slot_out, "slot_out"), _bf(out, "out"), _stream(stream)), "moe_unpermute_combine")
+        _bf(rows, "rows"), _i32(dest_pos, "dest_pos"), T, d, int(k), 1 if shared_expert else 0,
+        _f32(weights, "weights"), _f32(row_scalars, "row_scalars"), _f32(slot_out, "slot_out"),
+        _bf(out, "out"), _stream(stream)), "moe_unpermute_combine")
 
 
 def moe_lora_grouped_mlp_fwd(dims: MoeDims, Xp, counts, offsets, tile_off, sorted_src, topk_w,

@@ -139,9 +139,9 @@ EncodeTiledFn encode_fn() {
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-int64_t padded_rows_max(int64_t T, int64_t K, int64_t G) {
-  const int64_t n = T * K + G * (kTileM - 1);
-  return (n + kTileM - 1) / kTileM * kTileM;
+// Upper bound on the 128-row tiles of all groups: sum_g ceil(counts[g] / 128).
+int64_t max_row_tiles(int64_t T, int64_t K, int64_t G) {
+  return (T * K + G * (kTileM - 1) + kTileM - 1) / kTileM;
 }
 
 int check_dims(const moe_dims* dm) {
@@ -157,7 +157,7 @@ int check_dims(const moe_dims* dm) {
     return fail(MOE_ERR_INVALID_ARG, "d, f and r must be multiples of 8");
   if (dm->r > 64) return fail(MOE_ERR_UNSUPPORTED, "LoRA rank r=%d > 64", dm->r);
   const int64_t K = dm->k + dm->shared_expert, G = dm->E + dm->shared_expert;
-  if (padded_rows_max(dm->T, K, G) >= (int64_t(1) << 31))
+  if (max_row_tiles(dm->T, K, G) * kTileM >= (int64_t(1) << 31))
     return fail(MOE_ERR_UNSUPPORTED, "too many routed rows");
   return MOE_OK;
 }
@@ -221,7 +221,8 @@ size_t align_up(size_t x) { return (x + 1023) & ~size_t(1023); }
 
 BwdWs bwd_layout(const moe_dims* dm, void* base) {
   const int64_t K = dm->k + dm->shared_expert, G = dm->E + dm->shared_expert;
-  const size_t P = static_cast<size_t>(padded_rows_max(dm->T, K, G));
+  (void)G;
+  const size_t P = static_cast<size_t>(dm->T) * static_cast<size_t>(K);  // routed rows N
   const size_t nr = align_up(2 * P * dm->r * 2);
   const size_t ndh = align_up(2 * P * 2 * static_cast<size_t>(dm->f) * 2);
   const size_t nparts = static_cast<size_t>(kDwPartsPerTile) * ((dm->f + 255) / 256);
@@ -255,9 +256,9 @@ GemmParams base_params(const moe_dims* dm, const int32_t* offsets, const int32_t
   return p;
 }
 
-int run_gemm(const GemmShape& sh, GemmParams& p, int64_t P, int num_sms, cudaStream_t s,
+int run_gemm(const GemmShape& sh, GemmParams& p, int64_t row_tiles, int num_sms, cudaStream_t s,
              const char* what) {
-  if (!sh.wgrad) p.max_tiles = static_cast<int>(P / kTileM) * p.n_ntiles;
+  if (!sh.wgrad) p.max_tiles = static_cast<int>(row_tiles) * p.n_ntiles;
   ProbeScope probe(what, s);
   cudaError_t e = launch_gemm(sh, p, num_sms, s);
   if (e != cudaSuccess) return cuda_fail(e, what);
@@ -322,11 +323,6 @@ const char* moe_kernel_name(int32_t i) {
 
 const char* moe_last_error(void) { return t_err.c_str(); }
 
-int64_t moe_padded_rows_max(int32_t T, int32_t K, int32_t G) {
-  if (T <= 0 || K <= 0 || G <= 0) return -1;
-  return padded_rows_max(T, K, G);
-}
-
 size_t moe_route_workspace_size(int32_t T, int32_t K, int32_t G) {
   if (T <= 0 || K <= 0 || G <= 0) return 0;
   return route_ws_bytes(static_cast<int64_t>(T) * K, G);
@@ -367,7 +363,7 @@ int moe_route(const int32_t* ids, int32_t T, int32_t k, int32_t E, int32_t share
   if (k > E) return fail(MOE_ERR_INVALID_ARG, "k=%d > E=%d", k, E);
   if (E > kMaxExperts || k > 32) return fail(MOE_ERR_UNSUPPORTED, "E > 1024 or k > 32");
   const int64_t K = k + shared_expert, G = E + shared_expert;
-  if (padded_rows_max(T, K, G) >= (int64_t(1) << 31))
+  if (max_row_tiles(T, K, G) * kTileM >= (int64_t(1) << 31))
     return fail(MOE_ERR_UNSUPPORTED, "too many routed rows");
   if (!aligned16(ws)) return fail(MOE_ERR_INVALID_ARG, "ws not 16-byte aligned");
   if (ws_bytes < moe_route_workspace_size(T, static_cast<int32_t>(K), static_cast<int32_t>(G)))
@@ -383,41 +379,38 @@ int moe_route(const int32_t* ids, int32_t T, int32_t k, int32_t E, int32_t share
   return ok();
 }
 
-int moe_permute(const moe_bf16* src, int32_t T, int32_t d, int32_t K, int32_t G,
-                const int32_t* offsets, const int32_t* tile_off, const int32_t* sorted_src,
+int moe_permute(const moe_bf16* src, int32_t T, int32_t d, int32_t K, const int32_t* dest_pos,
                 moe_bf16* dst, moe_stream_t stream) {
   MOE_CHECK_PTR(src);
   MOE_CHECK_PTR(dst);
-  if (!offsets || !tile_off || !sorted_src) return fail(MOE_ERR_INVALID_ARG, "NULL pointer");
-  if (T <= 0 || d <= 0 || K <= 0 || G <= 0) return fail(MOE_ERR_INVALID_ARG, "bad sizes");
+  if (!dest_pos) return fail(MOE_ERR_INVALID_ARG, "NULL pointer");
+  if (T <= 0 || d <= 0 || K <= 0) return fail(MOE_ERR_INVALID_ARG, "bad sizes");
   if (d % 8) return fail(MOE_ERR_INVALID_ARG, "d must be a multiple of 8");
-  if (G > kMaxExperts + 1) return fail(MOE_ERR_UNSUPPORTED, "too many groups");
-  const int64_t P = padded_rows_max(T, K, G);
-  if (P >= (int64_t(1) << 31)) return fail(MOE_ERR_UNSUPPORTED, "too many routed rows");
+  if (K > 33) return fail(MOE_ERR_UNSUPPORTED, "more than 33 slots per token");
+  if (static_cast<int64_t>(T) * K >= (int64_t(1) << 31))
+    return fail(MOE_ERR_UNSUPPORTED, "too many routed rows");
   ProbeScope probe("permute", stream);
-  cudaError_t e =
-      launch_permute(src, T, d, K, G, offsets, tile_off, sorted_src, dst, P, stream);
+  cudaError_t e = launch_permute(src, T, d, K, dest_pos, dst, stream);
   if (e != cudaSuccess) return cuda_fail(e, "permute launch");
   return ok();
 }
 
-int moe_unpermute_combine(const moe_bf16* rows, const int32_t* ids, const int32_t* dest_pos,
-                          const int32_t* offsets, const int32_t* tile_off, int32_t T, int32_t d,
-                          int32_t k, int32_t E, int32_t shared_expert, const float* weights,
+int moe_unpermute_combine(const moe_bf16* rows, const int32_t* dest_pos, int32_t T, int32_t d,
+                          int32_t k, int32_t shared_expert, const float* weights,
                           const float* row_scalars, float* slot_out, moe_bf16* out,
                           moe_stream_t stream) {
   MOE_CHECK_PTR(rows);
   MOE_CHECK_PTR(out);
-  if (!ids || !dest_pos || !offsets || !tile_off) return fail(MOE_ERR_INVALID_ARG, "NULL pointer");
-  if (T <= 0 || d <= 0 || k <= 0 || E <= 0 || (shared_expert != 0 && shared_expert != 1))
+  if (!dest_pos) return fail(MOE_ERR_INVALID_ARG, "NULL pointer");
+  if (T <= 0 || d <= 0 || k <= 0 || (shared_expert != 0 && shared_expert != 1))
     return fail(MOE_ERR_INVALID_ARG, "bad sizes");
   if (d % 8) return fail(MOE_ERR_INVALID_ARG, "d must be a multiple of 8");
-  if (k > 32 || E > kMaxExperts) return fail(MOE_ERR_UNSUPPORTED, "k > 32 or E > 1024");
+  if (k > 32) return fail(MOE_ERR_UNSUPPORTED, "k > 32");
   if ((row_scalars == nullptr) != (slot_out == nullptr))
     return fail(MOE_ERR_INVALID_ARG, "row_scalars and slot_out go together");
   ProbeScope probe("combine", stream);
-  cudaError_t e = launch_combine(rows, ids, dest_pos, offsets, tile_off, T, d, k, E,
-                                 shared_expert, weights, row_scalars, slot_out, out, stream);
+  cudaError_t e = launch_combine(rows, dest_pos, T, d, k, shared_expert, weights, row_scalars,
+                                 slot_out, out, stream);
   if (e != cudaSuccess) return cuda_fail(e, "combine launch");
   return ok();
 }
@@ -444,40 +437,41 @@ int moe_lora_grouped_mlp_fwd(const moe_dims* dims, const moe_bf16* Xp, const int
   if (rc) return rc;
   const int d = dims->d, f = dims->f, r = dims->r;
   const int G = dims->E + dims->shared_expert;
-  const int64_t P = padded_rows_max(dims->T, dims->k + dims->shared_expert, G);
+  const int64_t N = static_cast<int64_t>(dims->T) * (dims->k + dims->shared_expert);
+  const int64_t R = max_row_tiles(dims->T, dims->k + dims->shared_expert, G);
   const GemmParams base = base_params(dims, offsets, tile_off, sorted_src, topk_w, st->status);
   cudaStream_t s = stream;
 
-  const int64_t Pf = P * f, Pr = P * r;
+  const int64_t Nf = N * f, Nr = N * r;
   {  // xa_gu pair = s * Xp A_gu^T
     GemmParams p = base;
-    SLICE(p, 0, Xp, P, d, MAP3(p.sl[0].b, A_gu, G, r, d, 64, 64), d);
-    p.nslices = 1; p.N = r; p.n_ntiles = (r + 63) / 64; p.out0 = xa_gu; p.ld0 = r; p.pair = Pr;
-    if ((rc = run_gemm({64, false, false, Epi::kLoRA}, p, P, st->num_sms, s, "xa_gu"))) return rc;
+    SLICE(p, 0, Xp, N, d, MAP3(p.sl[0].b, A_gu, G, r, d, 64, 64), d);
+    p.nslices = 1; p.N = r; p.n_ntiles = (r + 63) / 64; p.out0 = xa_gu; p.ld0 = r; p.pair = Nr;
+    if ((rc = run_gemm({64, false, false, Epi::kLoRA}, p, R, st->num_sms, s, "xa_gu"))) return rc;
   }
   {  // h = Xp W_gu^T + (s xa) B_gu^T (fp32) ; act pair = silu(gate) * up
     GemmParams p = base;
-    SLICE(p, 0, Xp, P, d, MAP3(p.sl[0].b, W_gu, G, 2 * f, d, 128, 64), d);
-    SLICE(p, 1, xa_gu, P, r, MAP3(p.sl[1].b, B_gu, G, 2 * f, r, 128, 64), r);
-    SLICE(p, 2, xa_gu + Pr, P, r, MAP3(p.sl[2].b, B_gu, G, 2 * f, r, 128, 64), r);
+    SLICE(p, 0, Xp, N, d, MAP3(p.sl[0].b, W_gu, G, 2 * f, d, 128, 64), d);
+    SLICE(p, 1, xa_gu, N, r, MAP3(p.sl[1].b, B_gu, G, 2 * f, r, 128, 64), r);
+    SLICE(p, 2, xa_gu + Nr, N, r, MAP3(p.sl[2].b, B_gu, G, 2 * f, r, 128, 64), r);
     p.nslices = 3; p.N = f; p.n_ntiles = (f + 127) / 128; p.b_split = f;
-    p.fout = h; p.ld0 = 2 * f; p.out0 = act; p.pair = Pf;
-    if ((rc = run_gemm({256, false, false, Epi::kSwiGLU}, p, P, st->num_sms, s, "gate_up")))
+    p.fout = h; p.ld0 = 2 * f; p.out0 = act; p.pair = Nf;
+    if ((rc = run_gemm({256, false, false, Epi::kSwiGLU}, p, R, st->num_sms, s, "gate_up")))
       return rc;
   }
   {  // xa_dn pair = s * act A_dn^T   (act = hi + lo)
     GemmParams p = base;
-    SLICE(p, 0, act, P, f, MAP3(p.sl[0].b, A_dn, G, r, f, 64, 64), f);
-    SLICE(p, 1, act + Pf, P, f, MAP3(p.sl[1].b, A_dn, G, r, f, 64, 64), f);
-    p.nslices = 2; p.N = r; p.n_ntiles = (r + 63) / 64; p.out0 = xa_dn; p.ld0 = r; p.pair = Pr;
-    if ((rc = run_gemm({64, false, false, Epi::kLoRA}, p, P, st->num_sms, s, "xa_dn"))) return rc;
+    SLICE(p, 0, act, N, f, MAP3(p.sl[0].b, A_dn, G, r, f, 64, 64), f);
+    SLICE(p, 1, act + Nf, N, f, MAP3(p.sl[1].b, A_dn, G, r, f, 64, 64), f);
+    p.nslices = 2; p.N = r; p.n_ntiles = (r + 63) / 64; p.out0 = xa_dn; p.ld0 = r; p.pair = Nr;
+    if ((rc = run_gemm({64, false, false, Epi::kLoRA}, p, R, st->num_sms, s, "xa_dn"))) return rc;
   }
   {  // Yp = w * (act W_dn^T + (s xa_dn) B_dn^T)
     GemmParams p = base;
-    SLICE(p, 0, act, P, f, MAP3(p.sl[0].b, W_dn, G, d, f, 256, 64), f);
-    SLICE(p, 1, xa_dn, P, r, MAP3(p.sl[1].b, B_dn, G, d, r, 256, 64), r);
+    SLICE(p, 0, act, N, f, MAP3(p.sl[0].b, W_dn, G, d, f, 256, 64), f);
+    SLICE(p, 1, xa_dn, N, r, MAP3(p.sl[1].b, B_dn, G, d, r, 256, 64), r);
     p.nslices = 2; p.N = d; p.n_ntiles = (d + 255) / 256; p.out0 = Yp; p.ld0 = d;
-    if ((rc = run_gemm({256, false, false, Epi::kScaleW}, p, P, st->num_sms, s, "down")))
+    if ((rc = run_gemm({256, false, false, Epi::kScaleW}, p, R, st->num_sms, s, "down")))
       return rc;
   }
   return ok();
@@ -516,43 +510,44 @@ int moe_lora_grouped_mlp_bwd(const moe_dims* dims, const moe_bf16* dYp, const mo
   if (rc) return rc;
   const int d = dims->d, f = dims->f, r = dims->r;
   const int G = dims->E + dims->shared_expert;
-  const int64_t P = padded_rows_max(dims->T, dims->k + dims->shared_expert, G);
+  const int64_t N = static_cast<int64_t>(dims->T) * (dims->k + dims->shared_expert);
+  const int64_t R = max_row_tiles(dims->T, dims->k + dims->shared_expert, G);
   const GemmParams base = base_params(dims, offsets, tile_off, sorted_src, topk_w, st->status);
   cudaStream_t s = stream;
   const int ntiles_f = (f + 255) / 256;
   const int nparts = kDwPartsPerTile * ntiles_f;
 
-  const int64_t Pr = P * r, P2f = P * 2 * f;
+  const int64_t Nr = N * r, N2f = N * 2 * f;
   {  // u = dYp B_dn -> pairs us = s*u, uw = s*w*u, xw = w * (s xa_dn)
     GemmParams p = base;
-    SLICE(p, 0, dYp, P, d, MAP3(p.sl[0].b, B_dn, G, d, r, 64, 64), d);
-    p.nslices = 1; p.N = r; p.n_ntiles = (r + 63) / 64; p.ld0 = r; p.pair = Pr;
+    SLICE(p, 0, dYp, N, d, MAP3(p.sl[0].b, B_dn, G, d, r, 64, 64), d);
+    p.nslices = 1; p.N = r; p.n_ntiles = (r + 63) / 64; p.ld0 = r; p.pair = Nr;
     p.out0 = w.us; p.out1 = w.uw; p.out2 = w.xw; p.aux0 = xa_dn;
-    if ((rc = run_gemm({64, true, false, Epi::kLoRA}, p, P, st->num_sms, s, "u"))) return rc;
+    if ((rc = run_gemm({64, true, false, Epi::kLoRA}, p, R, st->num_sms, s, "u"))) return rc;
   }
   {  // g = dYp W_dn + us A_dn ; SwiGLU backward from fp32 h -> dh pair ; dw partials
     GemmParams p = base;
-    SLICE(p, 0, dYp, P, d, MAP3(p.sl[0].b, W_dn, G, d, f, 64, 64), d);
-    SLICE(p, 1, w.us, P, r, MAP3(p.sl[1].b, A_dn, G, r, f, 64, 64), r);
-    SLICE(p, 2, w.us + Pr, P, r, MAP3(p.sl[2].b, A_dn, G, r, f, 64, 64), r);
+    SLICE(p, 0, dYp, N, d, MAP3(p.sl[0].b, W_dn, G, d, f, 64, 64), d);
+    SLICE(p, 1, w.us, N, r, MAP3(p.sl[1].b, A_dn, G, r, f, 64, 64), r);
+    SLICE(p, 2, w.us + Nr, N, r, MAP3(p.sl[2].b, A_dn, G, r, f, 64, 64), r);
     p.nslices = 3; p.N = f; p.n_ntiles = ntiles_f;
-    p.fin = h; p.out0 = w.dh; p.ld0 = 2 * f; p.pair = P2f; p.fout = w.dwp; p.fstride = P;
-    if ((rc = run_gemm({256, true, false, Epi::kDgradDn}, p, P, st->num_sms, s, "dgrad_dn")))
+    p.fin = h; p.out0 = w.dh; p.ld0 = 2 * f; p.pair = N2f; p.fout = w.dwp; p.fstride = N;
+    if ((rc = run_gemm({256, true, false, Epi::kDgradDn}, p, R, st->num_sms, s, "dgrad_dn")))
       return rc;
   }
   {  // v = dh B_gu (dh = hi + lo) -> vs pair = s*v
     GemmParams p = base;
-    SLICE(p, 0, w.dh, P, 2 * f, MAP3(p.sl[0].b, B_gu, G, 2 * f, r, 64, 64), 2 * f);
-    SLICE(p, 1, w.dh + P2f, P, 2 * f, MAP3(p.sl[1].b, B_gu, G, 2 * f, r, 64, 64), 2 * f);
-    p.nslices = 2; p.N = r; p.n_ntiles = (r + 63) / 64; p.ld0 = r; p.pair = Pr; p.out0 = w.vs;
-    if ((rc = run_gemm({64, true, false, Epi::kLoRA}, p, P, st->num_sms, s, "v"))) return rc;
+    SLICE(p, 0, w.dh, N, 2 * f, MAP3(p.sl[0].b, B_gu, G, 2 * f, r, 64, 64), 2 * f);
+    SLICE(p, 1, w.dh + N2f, N, 2 * f, MAP3(p.sl[1].b, B_gu, G, 2 * f, r, 64, 64), 2 * f);
+    p.nslices = 2; p.N = r; p.n_ntiles = (r + 63) / 64; p.ld0 = r; p.pair = Nr; p.out0 = w.vs;
+    if ((rc = run_gemm({64, true, false, Epi::kLoRA}, p, R, st->num_sms, s, "v"))) return rc;
   }
   {  // dXp = dh W_gu + vs A_gu   (high halves: dX is an output, not a row reduction)
     GemmParams p = base;
-    SLICE(p, 0, w.dh, P, 2 * f, MAP3(p.sl[0].b, W_gu, G, 2 * f, d, 64, 64), 2 * f);
-    SLICE(p, 1, w.vs, P, r, MAP3(p.sl[1].b, A_gu, G, r, d, 64, 64), r);
+    SLICE(p, 0, w.dh, N, 2 * f, MAP3(p.sl[0].b, W_gu, G, 2 * f, d, 64, 64), 2 * f);
+    SLICE(p, 1, w.vs, N, r, MAP3(p.sl[1].b, A_gu, G, r, d, 64, 64), r);
     p.nslices = 2; p.N = d; p.n_ntiles = (d + 255) / 256; p.out0 = dXp; p.ld0 = d;
-    if ((rc = run_gemm({256, true, false, Epi::kStore}, p, P, st->num_sms, s, "dgrad_gu")))
+    if ((rc = run_gemm({256, true, false, Epi::kStore}, p, R, st->num_sms, s, "dgrad_gu")))
       return rc;
   }
   // per-group LoRA gradients: sum over the group's rows of A^T [B_hi | B_lo],
@@ -561,7 +556,7 @@ int moe_lora_grouped_mlp_bwd(const moe_dims* dims, const moe_bf16* dYp, const mo
     const moe_bf16* a;
     int a_pair;  // 1: a is a hi/lo pair buffer
     int M;
-    const uint16_t* b;  // hi/lo pair buffer [2, P, r]
+    const uint16_t* b;  // hi/lo pair buffer [2, N, r]
     float* out;
     int transpose;
     const char* name;
@@ -574,22 +569,22 @@ int moe_lora_grouped_mlp_bwd(const moe_dims* dims, const moe_bf16* dYp, const mo
   };
   for (const WgradJob& j : jobs) {
     GemmParams p = base;
-    MAP2(p.sl[0].a, j.a, P, j.M, 64, 64);
+    MAP2(p.sl[0].a, j.a, N, j.M, 64, 64);
     p.nslices = 1;
     if (j.a_pair) {
-      MAP2(p.sl[1].a, j.a + P * static_cast<int64_t>(j.M), P, j.M, 64, 64);
+      MAP2(p.sl[1].a, j.a + N * static_cast<int64_t>(j.M), N, j.M, 64, 64);
       p.nslices = 2;
     }
-    MAP2(p.wb_hi, j.b, P, r, 64, 64);
-    MAP2(p.wb_lo, j.b + Pr, P, r, 64, 64);
+    MAP2(p.wb_hi, j.b, N, r, 64, 64);
+    MAP2(p.wb_lo, j.b + Nr, N, r, 64, 64);
     p.M = j.M; p.N = r; p.n_ntiles = (j.M + 127) / 128;
     p.fout = j.out; p.fstride = static_cast<int64_t>(j.M) * r; p.transpose_out = j.transpose;
-    if ((rc = run_gemm({128, true, true, Epi::kWgrad}, p, P, st->num_sms, s, j.name))) return rc;
+    if ((rc = run_gemm({128, true, true, Epi::kWgrad}, p, R, st->num_sms, s, j.name))) return rc;
   }
   cudaError_t e;
   {
     ProbeScope probe("dw_reduce", s);
-    e = launch_sum_parts(w.dwp, nparts, P, P, dw_rows, s);
+    e = launch_sum_parts(w.dwp, nparts, N, N, dw_rows, s);
   }
   if (e != cudaSuccess) return cuda_fail(e, "dw reduce");
   return ok();

@@ -71,23 +71,15 @@ __device__ __forceinline__ int group_of_tile(const int32_t* __restrict__ tile_of
   return lo;
 }
 
-// Routing weight of permuted row p in group g (0 for padding rows, 1 for the
+// Routing weight of permuted row p (a valid sorted position; 1 for the
 // shared-expert slot).
-__device__ __forceinline__ float row_weight(const GemmParams& p, int g, int64_t row) {
-  const int q = static_cast<int>(row - static_cast<int64_t>(__ldg(p.tile_off + g)) * BM);
-  const int off = __ldg(p.offsets + g);
-  const int cnt = __ldg(p.offsets + g + 1) - off;
-  if (q >= cnt) return 0.f;
-  const int i = __ldg(p.sorted_src + off + q);
+__device__ __forceinline__ float row_weight(const GemmParams& p, int64_t row) {
+  const int i = __ldg(p.sorted_src + row);
   const int t = i / p.K;
   const int j = i - t * p.K;
   return j < p.k ? __ldg(p.topk_w + static_cast<int64_t>(t) * p.k + j) : 1.f;
 }
 
-__device__ __forceinline__ void store8(uint16_t* dst, const float (&v)[8]) {
-  *reinterpret_cast<uint4*>(dst) = make_uint4(pack_bf16x2(v[0], v[1]), pack_bf16x2(v[2], v[3]),
-                                              pack_bf16x2(v[4], v[5]), pack_bf16x2(v[6], v[7]));
-}
 // hi = bf16(v), lo = bf16(v - hi): the pair holds ~16 significant bits of v.
 __device__ __forceinline__ void split8(const float* v, uint4& hi, uint4& lo) {
   uint32_t h[4], l[4];
@@ -181,7 +173,7 @@ __device__ __forceinline__ void stg_fetch(uint4 (&regs)[8], int lane, const Plan
     const int c = lane & 7;
     const int plane = c >> pl.cpp_log2;
     const int sub = c & ((1 << pl.cpp_log2) - 1);
-    regs[i] = (plane < pl.nplanes && sub * 16 < pl.valid)
+    regs[i] = (plane < pl.nplanes && sub * 16 < pl.valid && r < pl.nrows)
                   ? __ldg(reinterpret_cast<const uint4*>(plane_base(pl, plane) + r * pl.ld +
                                                          sub * 16))
                   : make_uint4(0, 0, 0, 0);
@@ -199,11 +191,12 @@ __device__ __forceinline__ int clamp_bytes(int64_t v, int hi) {
 // Tile coordinates shared by all roles.
 struct TileInfo {
   int g;       // expert group
-  int mt;      // rows mode: permuted M tile; wgrad: M tile of the weight dimension
+  int mt;      // rows mode: M tile (tile_off numbering); wgrad: M tile of the weight dimension
   int nt;      // rows mode: N tile
   int nk;      // K blocks in total
-  int rt;      // wgrad: row tiles of the group (K blocks per slice = 2 * rt)
-  int64_t rb;  // wgrad: first permuted row of the group
+  int row0;    // first permuted row: of the tile (rows mode) / of the group (wgrad)
+  int nvalid;  // rows mode: rows of the group in this tile (<= 128); wgrad: group rows
+  int nkb;     // wgrad: 64-row K blocks per slice
 };
 
 template <bool WGRAD>
@@ -215,16 +208,20 @@ __device__ __forceinline__ TileInfo tile_info(const GemmParams& p, int t) {
     ti.g = group_of_tile(p.tile_off, p.G, ti.mt);
     ti.nk = 0;
     for (int s = 0; s < p.nslices; ++s) ti.nk += (p.sl[s].K + BK - 1) / BK;
-    ti.rt = 0;
-    ti.rb = 0;
+    const int local = ti.mt - __ldg(p.tile_off + ti.g);
+    const int off = __ldg(p.offsets + ti.g);
+    const int cnt = __ldg(p.offsets + ti.g + 1) - off;
+    ti.row0 = off + local * BM;
+    ti.nvalid = min(BM, cnt - local * BM);
+    ti.nkb = 0;
   } else {
     ti.g = t / p.n_ntiles;
     ti.mt = t - ti.g * p.n_ntiles;
     ti.nt = 0;
-    const int t0 = __ldg(p.tile_off + ti.g);
-    ti.rt = __ldg(p.tile_off + ti.g + 1) - t0;
-    ti.nk = ti.rt * (BM / BK) * p.nslices;
-    ti.rb = static_cast<int64_t>(t0) * BM;
+    ti.row0 = __ldg(p.offsets + ti.g);
+    ti.nvalid = __ldg(p.offsets + ti.g + 1) - ti.row0;
+    ti.nkb = (ti.nvalid + BK - 1) / BK;
+    ti.nk = ti.nkb * p.nslices;
   }
   return ti;
 }
@@ -250,7 +247,8 @@ __device__ __forceinline__ void rows_kblock(const GemmParams& p, int kb, int& s,
 
 template <int BN>
 __device__ __forceinline__ void epi_swiglu(const GemmParams& p, const TileInfo& ti, uint32_t tq,
-                                           int hf, int64_t row0, int lane, uint32_t stg) {
+                                           int hf, int64_t row0, int nrows, int lane,
+                                           uint32_t stg) {
   // accumulator columns [0, BN/2) = gate, [BN/2, BN) = up of the same features;
   // this warp: features hf*BN/4 + [0, BN/4)
   const int f = p.N;
@@ -274,7 +272,7 @@ __device__ __forceinline__ void epi_swiglu(const GemmParams& p, const TileInfo& 
     {
       float* hb = p.fout + row0 * p.ld0;
       Planes pl{reinterpret_cast<char*>(hb + j0), reinterpret_cast<char*>(hb + f + j0), nullptr,
-                nullptr, p.ld0 * 4, 2, 2, clamp_bytes(static_cast<int64_t>(f - j0) * 4, 64)};
+                nullptr, p.ld0 * 4, 2, 2, clamp_bytes(static_cast<int64_t>(f - j0) * 4, 64), nrows};
       stg_flush(stg, lane, pl);
     }
     __syncwarp();
@@ -291,7 +289,7 @@ __device__ __forceinline__ void epi_swiglu(const GemmParams& p, const TileInfo& 
       uint16_t* ab = p.out0 + row0 * static_cast<int64_t>(f) + j0;
       Planes pl{reinterpret_cast<char*>(ab), reinterpret_cast<char*>(ab + p.pair), nullptr,
                 nullptr, static_cast<int64_t>(f) * 2, 1, 2,
-                clamp_bytes(static_cast<int64_t>(f - j0) * 2, 32)};
+                clamp_bytes(static_cast<int64_t>(f - j0) * 2, 32), nrows};
       stg_flush(stg, lane, pl);
     }
     __syncwarp();
@@ -300,8 +298,9 @@ __device__ __forceinline__ void epi_swiglu(const GemmParams& p, const TileInfo& 
 
 template <int BN, bool SCALE>
 __device__ __forceinline__ void epi_store(const GemmParams& p, const TileInfo& ti, uint32_t tq,
-                                          int hf, int64_t row0, int lane, uint32_t stg) {
-  const float w = SCALE ? row_weight(p, ti.g, row0 + lane) : 1.f;
+                                          int hf, int64_t row0, int nrows, int lane,
+                                          uint32_t stg) {
+  const float w = SCALE ? (lane < nrows ? row_weight(p, row0 + lane) : 0.f) : 1.f;
 #pragma unroll 1
   for (int c0 = hf * (BN / 2); c0 < (hf + 1) * (BN / 2); c0 += 64) {
 #pragma unroll
@@ -324,7 +323,7 @@ __device__ __forceinline__ void epi_store(const GemmParams& p, const TileInfo& t
     __syncwarp();
     const int j0 = ti.nt * BN + c0;
     Planes pl{reinterpret_cast<char*>(p.out0 + row0 * p.ld0 + j0), nullptr, nullptr, nullptr,
-              p.ld0 * 2, 3, 1, clamp_bytes(static_cast<int64_t>(p.N - j0) * 2, 128)};
+              p.ld0 * 2, 3, 1, clamp_bytes(static_cast<int64_t>(p.N - j0) * 2, 128), nrows};
     stg_flush(stg, lane, pl);
     __syncwarp();
   }
@@ -332,18 +331,19 @@ __device__ __forceinline__ void epi_store(const GemmParams& p, const TileInfo& t
 
 template <int BN>
 __device__ __forceinline__ void epi_dgrad_dn(const GemmParams& p, const TileInfo& ti, uint32_t tq,
-                                             int hf, int64_t row0, int lane, uint32_t stg) {
+                                             int hf, int64_t row0, int nrows, int lane,
+                                             uint32_t stg) {
   // acc = g = dY W_dn + s (dY B_dn) A_dn (unscaled by the routing weight);
   // this warp: columns hf*BN/2 + [0, BN/2) in chunks of 16
   const int f = p.N;
-  const float w = row_weight(p, ti.g, row0 + lane);
+  const float w = lane < nrows ? row_weight(p, row0 + lane) : 0.f;
   const float* hb = p.fin + row0 * p.ld0;     // h [rows, 2f] fp32
   uint16_t* db = p.out0 + row0 * p.ld0;       // dh pair [rows, 2f]
   constexpr int kSubs = (BN / 2) / 16;
   auto h_planes = [&](int j0) {
     return Planes{reinterpret_cast<char*>(const_cast<float*>(hb + j0)),
                   reinterpret_cast<char*>(const_cast<float*>(hb + f + j0)), nullptr, nullptr,
-                  p.ld0 * 4, 2, 2, clamp_bytes(static_cast<int64_t>(f - j0) * 4, 64)};
+                  p.ld0 * 4, 2, 2, clamp_bytes(static_cast<int64_t>(f - j0) * 4, 64), nrows};
   };
   const int jbase = ti.nt * BN + hf * (BN / 2);
   uint4 pre[8];
@@ -395,7 +395,7 @@ __device__ __forceinline__ void epi_dgrad_dn(const GemmParams& p, const TileInfo
       Planes pl{reinterpret_cast<char*>(db + j0), reinterpret_cast<char*>(db + p.pair + j0),
                 reinterpret_cast<char*>(db + f + j0),
                 reinterpret_cast<char*>(db + p.pair + f + j0), p.ld0 * 2, 1, 4,
-                clamp_bytes(static_cast<int64_t>(f - j0) * 2, 32)};
+                clamp_bytes(static_cast<int64_t>(f - j0) * 2, 32), nrows};
       stg_flush(stg, lane, pl);
     }
     __syncwarp();
@@ -404,15 +404,17 @@ __device__ __forceinline__ void epi_dgrad_dn(const GemmParams& p, const TileInfo
       __syncwarp();
     }
   }
-  p.fout[static_cast<int64_t>(ti.nt * kDwPartsPerTile + hf) * p.fstride + row0 + lane] = dot;
+  if (lane < nrows)
+    p.fout[static_cast<int64_t>(ti.nt * kDwPartsPerTile + hf) * p.fstride + row0 + lane] = dot;
 }
 
 template <int BN>
 __device__ __forceinline__ void epi_lora(const GemmParams& p, const TileInfo& ti, uint32_t tq,
-                                         int hf, int64_t row0, int lane) {
+                                         int hf, int64_t row0, int nrows, int lane) {
   const int64_t row = row0 + lane;
+  const bool valid = lane < nrows;
   const bool need_w = p.out1 != nullptr || p.out2 != nullptr;
-  const float w = need_w ? row_weight(p, ti.g, row) : 0.f;
+  const float w = (need_w && valid) ? row_weight(p, row) : 0.f;
   const float s = p.scale;
 #pragma unroll 1
   for (int c0 = hf * (BN / 2); c0 < (hf + 1) * (BN / 2); c0 += 16) {
@@ -421,7 +423,7 @@ __device__ __forceinline__ void epi_lora(const GemmParams& p, const TileInfo& ti
 #pragma unroll
     for (int h8 = 0; h8 < 2; ++h8) {
       const int j = ti.nt * BN + c0 + h8 * 8;
-      if (j < p.N) {
+      if (valid && j < p.N) {
         const int64_t o = row * p.ld0 + j;
         float ov[8];
 #pragma unroll
@@ -569,7 +571,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
           rows_kblock(p, kb, s, kc, kext);
           const CUtensorMap* ma = &p.sl[s].a;
           const CUtensorMap* mb = &p.sl[s].b;
-          tma_load_2d(sa, ma, fb, kc, ti.mt * BM);
+          tma_load_2d(sa, ma, fb, kc, ti.row0);
           if (!B_MN) {
             if (p.b_split) {
               const int n0 = ti.nt * (BN / 2);
@@ -584,9 +586,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
               tma_load_3d(sb + c * kChunkBytes, mb, fb, ti.nt * BN + c * 64, kc, ti.g);
           }
         } else {
-          const int per = ti.rt * (BM / BK);
-          const int s = kb / per;
-          const int row = static_cast<int>(ti.rb) + (kb - s * per) * BK;
+          const int s = kb / ti.nkb;
+          const int row = ti.row0 + (kb - s * ti.nkb) * BK;
           tma_load_2d(sa, &p.sl[s].a, fb, ti.mt * BM, row);
           tma_load_2d(sa + kChunkBytes, &p.sl[s].a, fb, ti.mt * BM + 64, row);
           tma_load_2d(sb, &p.wb_hi, fb, 0, row);
@@ -606,8 +607,11 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
           mbar_wait(full_bar + i, static_cast<uint32_t>(armed[i]), &never, 200000000ull);
         }
     }
-  } else if (warp == 1 && lane == 0) {
+  } else if (warp == 1 && (WGRAD || lane == 0)) {
     // --------------------------------------------------------- MMA issuer
+    // Lane 0 waits and issues.  In the weight-gradient kernel the whole warp
+    // runs this loop and zeroes the rows past a group's end in the group's
+    // last K block; elsewhere lane 0 runs it alone.
     constexpr uint32_t idesc = idesc_bf16(BM, BN, WGRAD, B_MN || WGRAD);
     int stage = 0;
     uint32_t phase = 0;
@@ -617,46 +621,77 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
       const TileInfo ti = tile_info<WGRAD>(p, t);
       const int buf = local & 1;
       const uint32_t use = static_cast<uint32_t>(local >> 1);
-      if (!mbar_wait(tempty_bar + buf, (use & 1u) ^ 1u, abort_flag, kWaitTimeoutNs)) break;
+      int w_ok = 1;
+      if (lane == 0) w_ok = mbar_wait(tempty_bar + buf, (use & 1u) ^ 1u, abort_flag, kWaitTimeoutNs);
+      if constexpr (WGRAD) w_ok = __shfl_sync(0xffffffffu, w_ok, 0);
+      if (!w_ok) break;
       tc_fence_after();
       const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(buf * BN);
       uint32_t accum = 0;
       for (int kb = 0; kb < ti.nk; ++kb) {
-        if (!mbar_wait(full_bar + stage, phase, abort_flag, kWaitTimeoutNs)) {
+        int f_ok = 1;
+        if (lane == 0) f_ok = mbar_wait(full_bar + stage, phase, abort_flag, kWaitTimeoutNs);
+        if constexpr (WGRAD) f_ok = __shfl_sync(0xffffffffu, f_ok, 0);
+        if (!f_ok) {
           ok = false;
           break;
         }
-        tc_fence_after();
         const uint32_t sa = smem_u32(ring + stage * C::kStageBytes);
         const uint32_t sb = sa + kAStageBytes;
-        int nk16 = 4;
-        if (!WGRAD) {
-          int s, kc, kext;
-          rows_kblock(p, kb, s, kc, kext);
-          nk16 = min(4, (kext + 15) / 16);
+        if (WGRAD) {
+          const int b = kb % ti.nkb;
+          const int tail = ti.nvalid - b * BK;
+          if (tail < BK) {
+            // rows [tail, 64) of this block belong to the next group (or lie
+            // past the buffer): zero them in the A and B tiles (4 chunks)
+            const int n = (BK - tail) * 32;
+            for (int i = lane; i < n; i += 32) {
+              const int line = tail + (i >> 5);
+              const int piece = i & 31;
+              const uint32_t base = (piece >> 4) ? sb : sa;
+              sts128(base + ((piece >> 3) & 1) * kChunkBytes + line * 128 + (piece & 7) * 16,
+                     make_uint4(0, 0, 0, 0));
+            }
+            fence_proxy_async_smem();
+            __syncwarp();
+          }
         }
-        for (int kk = 0; kk < nk16; ++kk) {
-          uint64_t ad, bd;
-          if (!WGRAD) ad = sdesc_sw128(sa + kk * 32, 16, 1024);
-          else ad = sdesc_sw128(sa + kk * 2048, kChunkBytes, 1024);
-          if (!B_MN && !WGRAD) bd = sdesc_sw128(sb + kk * 32, 16, 1024);
-          else bd = sdesc_sw128(sb + kk * 2048, kChunkBytes, 1024);
-          tc_mma_bf16(d_tmem, ad, bd, idesc, accum);
-          accum = 1;
+        if (lane == 0) {
+          tc_fence_after();
+          int nk16 = 4;
+          if (!WGRAD) {
+            int s, kc, kext;
+            rows_kblock(p, kb, s, kc, kext);
+            nk16 = min(4, (kext + 15) / 16);
+          }
+          for (int kk = 0; kk < nk16; ++kk) {
+            uint64_t ad, bd;
+            if (!WGRAD) ad = sdesc_sw128(sa + kk * 32, 16, 1024);
+            else ad = sdesc_sw128(sa + kk * 2048, kChunkBytes, 1024);
+            if (!B_MN && !WGRAD) bd = sdesc_sw128(sb + kk * 32, 16, 1024);
+            else bd = sdesc_sw128(sb + kk * 2048, kChunkBytes, 1024);
+            tc_mma_bf16(d_tmem, ad, bd, idesc, accum);
+            accum = 1;
+          }
+          tc_commit(empty_bar + stage);
         }
-        tc_commit(empty_bar + stage);
+        if constexpr (WGRAD) __syncwarp();
         if (++stage == S) {
           stage = 0;
           phase ^= 1u;
         }
       }
       if (!ok) break;
-      tc_commit(tfull_bar + buf);
+      if (lane == 0) tc_commit(tfull_bar + buf);
+      if constexpr (WGRAD) __syncwarp();
     }
-    // all MMAs issued by this thread complete before TMEM is released
-    tc_commit(drain_bar);
-    volatile int never = 0;
-    mbar_wait(drain_bar, 0, &never, 200000000ull);
+    // all MMAs issued by this warp complete before TMEM is released
+    if (lane == 0) {
+      tc_commit(drain_bar);
+      volatile int never = 0;
+      mbar_wait(drain_bar, 0, &never, 200000000ull);
+    }
+    if constexpr (WGRAD) __syncwarp();
   } else if (warp >= 2) {
     // ----------------------------------------------------------- epilogue
     const int ew = warp - 2;
@@ -672,19 +707,22 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
       tc_fence_after();
       const uint32_t tq =
           tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(buf * BN);
-      const int64_t row0 = static_cast<int64_t>(ti.mt) * BM + q * 32;
+      // rows of this warp that belong to the tile's group (the rest of a
+      // 128-row tile runs past the group's end and is not stored)
+      const int64_t row0 = static_cast<int64_t>(ti.row0) + q * 32;
+      const int nrows = WGRAD ? 32 : max(0, min(32, ti.nvalid - q * 32));
       if constexpr (WGRAD) {
         epi_wgrad(p, ti, tq, hf, q, lane, stg);
       } else if constexpr (EPI == static_cast<int>(Epi::kSwiGLU)) {
-        epi_swiglu<BN>(p, ti, tq, hf, row0, lane, stg);
+        epi_swiglu<BN>(p, ti, tq, hf, row0, nrows, lane, stg);
       } else if constexpr (EPI == static_cast<int>(Epi::kScaleW)) {
-        epi_store<BN, true>(p, ti, tq, hf, row0, lane, stg);
+        epi_store<BN, true>(p, ti, tq, hf, row0, nrows, lane, stg);
       } else if constexpr (EPI == static_cast<int>(Epi::kStore)) {
-        epi_store<BN, false>(p, ti, tq, hf, row0, lane, stg);
+        epi_store<BN, false>(p, ti, tq, hf, row0, nrows, lane, stg);
       } else if constexpr (EPI == static_cast<int>(Epi::kLoRA)) {
-        epi_lora<BN>(p, ti, tq, hf, row0, lane);
+        epi_lora<BN>(p, ti, tq, hf, row0, nrows, lane);
       } else if constexpr (EPI == static_cast<int>(Epi::kDgradDn)) {
-        epi_dgrad_dn<BN>(p, ti, tq, hf, row0, lane, stg);
+        epi_dgrad_dn<BN>(p, ti, tq, hf, row0, nrows, lane, stg);
       }
       tc_fence_before();
       mbar_arrive(tempty_bar + buf);

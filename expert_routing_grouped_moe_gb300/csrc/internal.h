@@ -20,10 +20,16 @@ constexpr int kErrTimeout = -6;
 // ---- routing (route.cu) ----------------------------------------------------
 constexpr int kRouteThreads = 256;                  // 8 warps per CTA
 constexpr int kRouteWarps = kRouteThreads / 32;
-constexpr int kRoutePerLane = 8;                    // assignments per lane
-constexpr int kRouteChunk = kRouteThreads * kRoutePerLane;  // assignments per CTA
 
-inline int route_ctas(int64_t n) { return static_cast<int>((n + kRouteChunk - 1) / kRouteChunk); }
+// Assignments per lane, growing with the problem so that large routing
+// problems use fewer, fuller CTAs (each CTA handles 256 * per-lane assignments).
+inline int route_per_lane(int64_t n) {
+  return n >= (int64_t(1) << 19) ? 16 : n >= (int64_t(1) << 17) ? 8 : 4;
+}
+inline int route_chunk(int64_t n) { return kRouteThreads * route_per_lane(n); }
+inline int route_ctas(int64_t n) {
+  return static_cast<int>((n + route_chunk(n) - 1) / route_chunk(n));
+}
 inline size_t route_ws_bytes(int64_t n, int G) {
   // per-(group, CTA) histogram, int32
   return static_cast<size_t>(G) * static_cast<size_t>(route_ctas(n > 0 ? n : 1)) * 4u;
@@ -36,13 +42,11 @@ cudaError_t launch_route(const int32_t* ids, int T, int k, int E, int shared, in
                          int32_t* dest_pos, int32_t* hist, int* status, cudaStream_t s);
 
 // ---- row gather / combine (rows.cu) ------------------------------------------
-cudaError_t launch_permute(const uint16_t* src, int T, int d, int K, int G,
-                           const int32_t* offsets, const int32_t* tile_off,
-                           const int32_t* sorted_src, uint16_t* dst, int64_t max_rows,
-                           cudaStream_t s);
-cudaError_t launch_combine(const uint16_t* rows, const int32_t* ids, const int32_t* dest_pos,
-                           const int32_t* offsets, const int32_t* tile_off, int T, int d, int k,
-                           int E, int shared, const float* weights, const float* row_scalars,
+// Permuted rows are in sorted order: row p holds sorted position p, N = T * K rows.
+cudaError_t launch_permute(const uint16_t* src, int T, int d, int K, const int32_t* dest_pos,
+                           uint16_t* dst, cudaStream_t s);
+cudaError_t launch_combine(const uint16_t* rows, const int32_t* dest_pos, int T, int d, int k,
+                           int shared, const float* weights, const float* row_scalars,
                            float* slot_out, uint16_t* out, cudaStream_t s);
 cudaError_t launch_sum_parts(const float* parts, int nparts, int64_t stride, int64_t n,
                              float* out, cudaStream_t s);
@@ -98,6 +102,7 @@ struct GemmParams {
   int64_t fstride;    // stride between dw partial slices, or group stride of fout
   int transpose_out;  // wgrad: write fout[g][n][m] instead of fout[g][m][n]
   int max_tiles;      // upper bound of tiles (host-known), rows mode
+  int nrows;          // rows of the permuted buffers (N = T * K)
   int* status;
 };
 

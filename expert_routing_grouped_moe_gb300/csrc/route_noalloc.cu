@@ -15,9 +15,9 @@
 namespace moe {
 namespace {
 
-// Scratch for the routing histogram: G * ceil(N / kRouteChunk) int32 entries.
-// 2 MiB covers, e.g., 128 experts with up to 8,388,608 routed rows
-// (1M tokens x top-8).
+// Scratch for the routing histogram: moe_route_workspace_size() bytes, G groups
+// times one int32 per routing CTA.  2 MiB covers, e.g., up to 256 experts with
+// 8,388,608 routed rows (1M tokens x top-8).
 constexpr size_t kNoAllocHistInts = size_t(1) << 19;
 static __device__ __align__(256) int32_t g_route_scratch[kNoAllocHistInts];
 

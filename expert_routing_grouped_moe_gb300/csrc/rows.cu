@@ -1,11 +1,15 @@
-// Row permute (gather into the expert-grouped, tile-padded layout) and
-// combine (gather-reduce back to token order).  Both are pure HBM streams:
-// one warp moves a row as 16-byte vectors.
+// Row permute (gather into expert-grouped sorted order) and combine
+// (gather-reduce back to token order).  Both are pure HBM streams: one warp
+// moves a row as 16-byte vectors, all of a row's loads issued before its
+// stores.
 //
 // Permute is step 5 of the routing pass in the Unsloth x NVIDIA article,
-// section "Optimisation 3" (slice the token list by offsets).  Combine is the
-// top-k mixture Y[t] = sum_j w[t,j] * out(t,j), summed in fp32 in slot order
-// with no atomics, so results are deterministic.
+// section "Optimisation 3" (slice the token list by offsets): permuted row p
+// is the token of sorted position p, so expert g's rows are the contiguous
+// slice [offsets[g], offsets[g+1]); it is done as a scatter of each token's
+// row to the sorted positions of its slots.  Combine is the top-k mixture
+// Y[t] = sum_j w[t,j] * out(t,j), summed in fp32 in slot order with no
+// atomics, so results are deterministic.
 #include <algorithm>
 #include <cstdint>
 
@@ -14,54 +18,29 @@
 namespace moe {
 namespace {
 
-
-// Group owning permuted tile mt: the largest g with tile_off[g] <= mt (that
-// group is non-empty because mt < tile_off[G]).
-__device__ __forceinline__ int group_of_tile(const int32_t* __restrict__ tile_off, int G, int mt) {
-  int lo = 0, hi = G - 1;
-  while (lo < hi) {
-    const int mid = (lo + hi + 1) >> 1;
-    if (__ldg(tile_off + mid) <= mt) lo = mid;
-    else hi = mid - 1;
-  }
-  return lo;
-}
-
-// One CTA per 128-row tile of the permuted layout; 8 warps x 16 rows.
-__global__ void __launch_bounds__(256) permute_kernel(
-    const uint4* __restrict__ src, int d8, int K, int G, const int32_t* __restrict__ offsets,
-    const int32_t* __restrict__ tile_off, const int32_t* __restrict__ sorted_src,
-    uint4* __restrict__ dst) {
-  __shared__ int s_first, s_cnt, s_off;
-  const int mt = blockIdx.x;
-  if (threadIdx.x == 0) {
-    if (mt >= __ldg(tile_off + G)) {
-      s_cnt = -1;
-    } else {
-      const int g = group_of_tile(tile_off, G, mt);
-      s_first = (mt - __ldg(tile_off + g)) * kTileM;
-      s_off = __ldg(offsets + g);
-      s_cnt = __ldg(offsets + g + 1) - s_off;
-    }
-  }
-  __syncthreads();
-  if (s_cnt < 0) return;
+// One warp per token: the token's row is read once and written to the
+// permuted rows of its K slots, dst[dest_pos[t*K + j]] = src[t].  Reading each
+// source row once keeps the traffic at T*d + N*d elements even when X does not
+// fit in L2.
+__global__ void __launch_bounds__(256) permute_kernel(const uint4* __restrict__ src, int T,
+                                                     int d8, int K,
+                                                     const int32_t* __restrict__ dest_pos,
+                                                     uint4* __restrict__ dst) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  // each lane moves 8 vectors of a row per step (a 4 KB row of d = 2048 in one
-  // step): all loads issued before the stores
-  for (int r = warp * 16; r < warp * 16 + 16; ++r) {
-    const int q = s_first + r;
-    const int64_t p = static_cast<int64_t>(mt) * kTileM + r;
-    uint4* drow = dst + p * d8;
-    const uint4* srow = nullptr;
-    if (q < s_cnt) srow = src + static_cast<int64_t>(__ldg(sorted_src + s_off + q) / K) * d8;
-    for (int v0 = 0; v0 < d8; v0 += 256) {
-      uint4 x[8];
+  const int t = blockIdx.x * 8 + warp;
+  if (t >= T) return;
+  const uint4* srow = src + static_cast<int64_t>(t) * d8;
+  for (int v0 = 0; v0 < d8; v0 += 256) {
+    uint4 x[8];
 #pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        const int v = v0 + i * 32 + lane;
-        x[i] = (srow != nullptr && v < d8) ? __ldg(srow + v) : make_uint4(0, 0, 0, 0);
-      }
+    for (int i = 0; i < 8; ++i) {
+      const int v = v0 + i * 32 + lane;
+      x[i] = v < d8 ? __ldg(srow + v) : make_uint4(0, 0, 0, 0);
+    }
+    for (int j = 0; j < K; ++j) {
+      const int p = __ldg(dest_pos + static_cast<int64_t>(t) * K + j);
+      if (p < 0) continue;
+      uint4* drow = dst + static_cast<int64_t>(p) * d8;
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
         const int v = v0 + i * 32 + lane;
@@ -88,32 +67,26 @@ __device__ __forceinline__ uint32_t pack2(float lo, float hi) {
 
 constexpr int kMaxSlots = 33;
 
-// One warp per token, 8 tokens per CTA.
+// One warp per token, 8 tokens per CTA.  Row of slot j = dest_pos[t*K + j].
 __global__ void __launch_bounds__(256) combine_kernel(
-    const uint4* __restrict__ rows, const int32_t* __restrict__ ids,
-    const int32_t* __restrict__ dest_pos, const int32_t* __restrict__ offsets,
-    const int32_t* __restrict__ tile_off, int T, int d8, int k, int E, int shared,
-    const float* __restrict__ weights, const float* __restrict__ row_scalars,
+    const uint4* __restrict__ rows, const int32_t* __restrict__ dest_pos, int T, int d8, int k,
+    int shared, const float* __restrict__ weights, const float* __restrict__ row_scalars,
     float* __restrict__ slot_out, uint4* __restrict__ out) {
-  __shared__ int64_t s_row[8][kMaxSlots];
+  __shared__ int s_row[8][kMaxSlots];
   __shared__ float s_c[8][kMaxSlots];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int t = blockIdx.x * 8 + warp;
   if (t >= T) return;
   const int K = k + shared;
   for (int j = lane; j < K; j += 32) {
-    const int g = j < k ? __ldg(ids + static_cast<int64_t>(t) * k + j) : E;
     const int dp = __ldg(dest_pos + static_cast<int64_t>(t) * K + j);
-    int64_t prow = -1;
     float c = 0.f;
-    if (dp >= 0 && g >= 0 && g <= E) {
-      prow = static_cast<int64_t>(__ldg(tile_off + g)) * kTileM + dp - __ldg(offsets + g);
+    if (dp >= 0)
       c = (weights != nullptr && j < k) ? __ldg(weights + static_cast<int64_t>(t) * k + j) : 1.f;
-    }
-    s_row[warp][j] = prow;
+    s_row[warp][j] = dp;
     s_c[warp][j] = c;
     if (slot_out != nullptr && row_scalars != nullptr && j < k)
-      slot_out[static_cast<int64_t>(t) * k + j] = prow >= 0 ? __ldg(row_scalars + prow) : 0.f;
+      slot_out[static_cast<int64_t>(t) * k + j] = dp >= 0 ? __ldg(row_scalars + dp) : 0.f;
   }
   __syncwarp();
   uint4* orow = out + static_cast<int64_t>(t) * d8;
@@ -125,8 +98,9 @@ __global__ void __launch_bounds__(256) combine_kernel(
 #pragma unroll
       for (int jj = 0; jj < 8; ++jj) {
         const int j = j0 + jj;
-        const int64_t pr = j < K ? s_row[warp][j] : -1;
-        x[jj] = pr >= 0 ? __ldg(rows + pr * d8 + v) : make_uint4(0, 0, 0, 0);
+        const int pr = j < K ? s_row[warp][j] : -1;
+        x[jj] = pr >= 0 ? __ldg(rows + static_cast<int64_t>(pr) * d8 + v)
+                        : make_uint4(0, 0, 0, 0);
       }
 #pragma unroll
       for (int jj = 0; jj < 8; ++jj)
@@ -149,26 +123,21 @@ __global__ void sum_parts_kernel(const float* __restrict__ parts, int nparts, in
 
 }  // namespace
 
-cudaError_t launch_permute(const uint16_t* src, int T, int d, int K, int G,
-                           const int32_t* offsets, const int32_t* tile_off,
-                           const int32_t* sorted_src, uint16_t* dst, int64_t max_rows,
-                           cudaStream_t s) {
-  (void)T;
-  const int tiles = static_cast<int>(max_rows / kTileM);
-  if (tiles == 0) return cudaSuccess;
-  permute_kernel<<<tiles, 256, 0, s>>>(reinterpret_cast<const uint4*>(src), d / 8, K, G, offsets,
-                                       tile_off, sorted_src, reinterpret_cast<uint4*>(dst));
+cudaError_t launch_permute(const uint16_t* src, int T, int d, int K, const int32_t* dest_pos,
+                           uint16_t* dst, cudaStream_t s) {
+  if (T == 0) return cudaSuccess;
+  permute_kernel<<<(T + 7) / 8, 256, 0, s>>>(reinterpret_cast<const uint4*>(src), T, d / 8, K,
+                                             dest_pos, reinterpret_cast<uint4*>(dst));
   return cudaGetLastError();
 }
 
-cudaError_t launch_combine(const uint16_t* rows, const int32_t* ids, const int32_t* dest_pos,
-                           const int32_t* offsets, const int32_t* tile_off, int T, int d, int k,
-                           int E, int shared, const float* weights, const float* row_scalars,
+cudaError_t launch_combine(const uint16_t* rows, const int32_t* dest_pos, int T, int d, int k,
+                           int shared, const float* weights, const float* row_scalars,
                            float* slot_out, uint16_t* out, cudaStream_t s) {
   if (T == 0) return cudaSuccess;
-  combine_kernel<<<(T + 7) / 8, 256, 0, s>>>(
-      reinterpret_cast<const uint4*>(rows), ids, dest_pos, offsets, tile_off, T, d / 8, k, E,
-      shared, weights, row_scalars, slot_out, reinterpret_cast<uint4*>(out));
+  combine_kernel<<<(T + 7) / 8, 256, 0, s>>>(reinterpret_cast<const uint4*>(rows), dest_pos, T,
+                                             d / 8, k, shared, weights, row_scalars, slot_out,
+                                             reinterpret_cast<uint4*>(out));
   return cudaGetLastError();
 }
 

@@ -29,15 +29,14 @@ class MoELoRALayer:
         self.shared = bool(shared_expert)
         self.G = E + (1 if shared_expert else 0)
         self.K = k + (1 if shared_expert else 0)
-        self.N = T * self.K
-        self.P = L.moe_padded_rows_max(T, self.K, self.G)
+        self.N = T * self.K          # permuted rows, in sorted order
         dev = torch.device(device)
         self.w = {n: weights[n].contiguous() for n in ("W_gu", "A_gu", "B_gu", "W_dn", "A_dn",
                                                           "B_dn")}
         i32 = dict(dtype=torch.int32, device=dev)
         bf = dict(dtype=torch.bfloat16, device=dev)
         f32 = dict(dtype=torch.float32, device=dev)
-        P, G = self.P, self.G
+        P, G = self.N, self.G
         self.counts = torch.zeros(G, **i32)
         self.offsets = torch.zeros(G + 1, **i32)
         self.tile_off = torch.zeros(G + 1, **i32)
@@ -76,23 +75,21 @@ class MoELoRALayer:
         """Y [T,d] bf16 for token rows X [T,d], top-k ids [T,k], weights [T,k]."""
         self._ids, self._topk_w = ids, topk_w
         self.route(ids, stream)
-        L.moe_permute(X, self.K, self.G, self.offsets, self.tile_off, self.sorted_src, self.Xp,
-                      stream)
+        L.moe_permute(X, self.K, self.dest_pos, self.Xp, stream)
         w = self.w
         L.moe_lora_grouped_mlp_fwd(self.dims, self.Xp, self.counts, self.offsets, self.tile_off,
                                    self.sorted_src, topk_w, w["W_gu"], w["A_gu"], w["B_gu"],
                                    w["W_dn"], w["A_dn"], w["B_dn"], self.Yp, self.h, self.act,
                                    self.xa_gu, self.xa_dn, stream)
-        L.moe_unpermute_combine(self.Yp, ids, self.dest_pos, self.offsets, self.tile_off, self.E,
-                                self.shared, self.Y, stream=stream)
+        L.moe_unpermute_combine(self.Yp, self.dest_pos, self.k, self.shared, self.Y,
+                                stream=stream)
         return self.Y
 
     def backward(self, dY, stream=None):
         """dX [T,d] bf16, dw [T,k] fp32 and the four fp32 LoRA gradients."""
         if self._ids is None:
             raise RuntimeError("backward before forward")
-        L.moe_permute(dY, self.K, self.G, self.offsets, self.tile_off, self.sorted_src, self.dYp,
-                      stream)
+        L.moe_permute(dY, self.K, self.dest_pos, self.dYp, stream)
         w, g = self.w, self.grads
         L.moe_lora_grouped_mlp_bwd(self.dims, self.dYp, self.Xp, self.counts, self.offsets,
                                    self.tile_off, self.sorted_src, self._topk_w, w["W_gu"],
@@ -100,24 +97,11 @@ class MoELoRALayer:
                                    self.act, self.xa_gu, self.xa_dn, self.dXp, self.dw_rows,
                                    g["dA_gu"], g["dB_gu"], g["dA_dn"], g["dB_dn"], self.bwd_ws,
                                    stream)
-        L.moe_unpermute_combine(self.dXp, self._ids, self.dest_pos, self.offsets, self.tile_off,
-                                self.E, self.shared, self.dX, row_scalars=self.dw_rows,
-                                slot_out=self.dw, stream=stream)
+        L.moe_unpermute_combine(self.dXp, self.dest_pos, self.k, self.shared, self.dX,
+                                row_scalars=self.dw_rows, slot_out=self.dw, stream=stream)
         return {"dX": self.dX, "dw": self.dw, **g}
 
     def step(self, X, ids, topk_w, dY, stream=None):
         """One forward + backward pass of the layer (the hot path)."""
         self.forward(X, ids, topk_w, stream)
         return self.backward(dY, stream)
-
-    # -------------------------------------------------------------- helpers
-    def padded_row_of(self):
-        """Permuted row of each flat assignment [N] (host-side index helper for
-        tests): tile_off[g]*128 + dest_pos - offsets[g]."""
-        ids = self._ids.reshape(self.T, self.k).to(torch.int64)
-        if self.shared:
-            ids = torch.cat([ids, torch.full((self.T, 1), self.E, dtype=torch.int64,
-                                             device=ids.device)], 1)
-        g = ids.reshape(-1)
-        return (self.tile_off.to(torch.int64)[g] * L.TILE_M + self.dest_pos.to(torch.int64)
-                - self.offsets.to(torch.int64)[g])

@@ -44,13 +44,13 @@
  *   G = E + shared_expert expert groups, K = k + shared_expert slots per token,
  *   N = T * K routed rows (flat index i = t*K + j; slot j = k is the shared one).
  *
- * Permuted ("padded") row layout used between calls
- *   Expert g's rows are the rows routed to it in stable order (ascending flat
- *   index).  In permuted buffers each group starts on a multiple of
- *   MOE_TILE_M rows: group g occupies rows [MOE_TILE_M * tile_off[g],
- *   MOE_TILE_M * tile_off[g+1]); its first counts[g] rows are real, the rest are
- *   zero padding.  The number of permuted rows is MOE_TILE_M * tile_off[G], at
- *   most moe_padded_rows_max(); allocate that many rows.
+ * Permuted row layout used between calls
+ *   Permuted buffers have N rows in sorted order: row p holds sorted position
+ *   p, so expert g's rows are the contiguous slice [offsets[g], offsets[g+1])
+ *   (article step 5, "slice the token list by offsets").  The grouped GEMMs
+ *   cut each slice into 128-row tiles (MOE_TILE_M) that start at offsets[g];
+ *   tile_off numbers those tiles.  A tile's last rows may run into the next
+ *   expert's slice: they are computed but never stored.
  */
 #ifndef MOE_GB300_H
 #define MOE_GB300_H
@@ -81,7 +81,7 @@ typedef enum {
   MOE_ERR_TIMEOUT = -6      /* (device) a pipeline wait gave up */
 } moe_status_t;
 
-#define MOE_TILE_M 128      /* row granularity of the permuted layout */
+#define MOE_TILE_M 128      /* rows per grouped-GEMM tile */
 #define MOE_MAX_EXPERTS 1024
 
 typedef struct moe_dims {
@@ -89,10 +89,6 @@ typedef struct moe_dims {
   float lora_scale;        /* s = alpha / r */
   int32_t shared_expert;   /* 0 or 1 */
 } moe_dims;
-
-/* Upper bound on permuted rows: T*K + G*(MOE_TILE_M-1) rounded to whole tiles.
- * Returns -1 on bad arguments. */
-MOE_API int64_t moe_padded_rows_max(int32_t T, int32_t K, int32_t G);
 
 /* ------------------------------------------------------------------------ */
 /* Router (upstream of the layer; the docs keep the router frozen).          */
@@ -140,10 +136,10 @@ MOE_API int moe_route(const int32_t* ids, int32_t T, int32_t k, int32_t E, int32
  * Same arguments and results as moe_route, minus ws / ws_bytes.  The routing
  * histogram lives in a 2 MiB array inside this library, which every GPU that
  * loads the library holds until the process exits; this call itself never
- * allocates or frees memory.  Limit: E + shared_expert groups times
- * ceil(T * (k + shared_expert) / 2048) histogram entries must fit in 2^19
- * (e.g. 128 experts with up to 8,388,608 routed rows); larger problems return
- * MOE_ERR_WORKSPACE -- use moe_route with a workspace for them.
+ * allocates or frees memory.  Limit: the histogram moe_route would need,
+ * moe_route_workspace_size(T, k + shared_expert, E + shared_expert), must not
+ * exceed 2 MiB (e.g. up to 256 experts with 8,388,608 routed rows); larger
+ * problems return MOE_ERR_WORKSPACE -- use moe_route with a workspace for them.
  * The first call on a device looks up the array's device address (once per
  * device, with that device current); make that first call before any stream
  * capture.  All calls share the one array: calls whose work overlaps on the
@@ -154,32 +150,28 @@ MOE_API int moe_route_noalloc(const int32_t* ids, int32_t T, int32_t k, int32_t 
                               int32_t* tile_off, int32_t* sorted_src, int32_t* dest_pos,
                               moe_stream_t stream);
 
-/* Row permute (article step 5, "slice the token list by offsets"): for every
- * permuted row p of group g with rank q = p - MOE_TILE_M*tile_off[g]:
- *   dst[p,:] = src[sorted_src[offsets[g] + q] / K, :]   if q < counts[g]
- *   dst[p,:] = 0                                         otherwise (padding)
- *   src [T,d] bf16;  dst [moe_padded_rows_max(T,K,G), d] bf16; rows past
- *   MOE_TILE_M*tile_off[G] are not touched.  Used for X (forward) and for the
- *   upstream gradient dY (backward). */
-MOE_API int moe_permute(const moe_bf16* src, int32_t T, int32_t d, int32_t K, int32_t G,
-                const int32_t* offsets, const int32_t* tile_off,
-                const int32_t* sorted_src, moe_bf16* dst, moe_stream_t stream);
+/* Row permute (article step 5, "slice the token list by offsets"): every
+ * token's row goes to the sorted positions of its slots,
+ *   dst[dest_pos[t*K + j], :] = src[t, :]   for j < K, dest_pos >= 0,
+ * i.e. dst[p] = src[sorted_src[p] / K] for every valid sorted position p.
+ *   src [T,d] bf16 (each row read once);  dst [N,d] bf16 (N = T*K).  Used for
+ *   X (forward) and for the upstream gradient dY (backward).  K <= 33. */
+MOE_API int moe_permute(const moe_bf16* src, int32_t T, int32_t d, int32_t K,
+                        const int32_t* dest_pos, moe_bf16* dst, moe_stream_t stream);
 
-/* Combine (unpermute + reduce): for every token t, with p(t,j) the permuted
- * row of slot j (group g = id of slot j, p = MOE_TILE_M*tile_off[g] +
- * dest_pos[t*K+j] - offsets[g]):
+/* Combine (unpermute + reduce): for every token t, with p(t,j) = dest_pos[t*K+j]
+ * the permuted row of slot j:
  *   out[t,:] = bf16( sum_{j<K} c_j * rows[p(t,j),:] ),  fp32 sum in j order,
  *   c_j = weights[t,j] for j < k and 1 for the shared slot, or c_j = 1 when
  *   weights is NULL (rows already scaled, or a gradient sum);
  *   slot_out[t,j] = row_scalars[p(t,j)] for j < k when both are non-NULL.
- *   rows [.,d] bf16 permuted; ids [T,k]; out [T,d] bf16;
- *   row_scalars [moe_padded_rows_max] fp32 or NULL; slot_out [T,k] fp32 or NULL.
- * Assignments with dest_pos = -1 (bad ids) contribute nothing. */
-MOE_API int moe_unpermute_combine(const moe_bf16* rows, const int32_t* ids, const int32_t* dest_pos,
-                          const int32_t* offsets, const int32_t* tile_off,
-                          int32_t T, int32_t d, int32_t k, int32_t E, int32_t shared_expert,
-                          const float* weights, const float* row_scalars, float* slot_out,
-                          moe_bf16* out, moe_stream_t stream);
+ *   rows [N,d] bf16; out [T,d] bf16; weights [T,k] fp32 or NULL;
+ *   row_scalars [N] fp32 or NULL; slot_out [T,k] fp32 or NULL.
+ * Slots with dest_pos = -1 (out-of-range ids) contribute nothing. */
+MOE_API int moe_unpermute_combine(const moe_bf16* rows, const int32_t* dest_pos, int32_t T,
+                                  int32_t d, int32_t k, int32_t shared_expert,
+                                  const float* weights, const float* row_scalars,
+                                  float* slot_out, moe_bf16* out, moe_stream_t stream);
 
 /* ------------------------------------------------------------------------ */
 /* Grouped split-LoRA SwiGLU expert MLP (docs: "Faster LoRA MoE training",    */
@@ -189,7 +181,7 @@ MOE_API int moe_unpermute_combine(const moe_bf16* rows, const int32_t* ids, cons
  *   W_gu [G,2f,d]  rows [0,f) gate, rows [f,2f) up   A_gu [G,r,d]  B_gu [G,2f,r]
  *   W_dn [G,d,f]                                      A_dn [G,r,f]  B_dn [G,d,r]
  * Per permuted row p of group g with routing weight w_p (w of its slot; 1 for
- * the shared slot; 0 for padding):
+ * the shared slot):
  *   xa   = Xp A_gu^T             h = Xp W_gu^T + s xa B_gu^T      [.,2f]
  *   act  = silu(h[:, :f]) * h[:, f:]                               [.,f]
  *   xa_dn = act A_dn^T           o = act W_dn^T + s xa_dn B_dn^T  [.,d]
@@ -202,11 +194,11 @@ MOE_API int moe_unpermute_combine(const moe_bf16* rows, const int32_t* ids, cons
  * such intermediates as "pair" buffers [2, P, cols] of bf16 with
  * value = pair[0] + pair[1] (pair[0] = bf16(v), pair[1] = bf16(v - pair[0])).
  * The tensor cores consume a pair as two bf16 operands (extra K steps).
- * Here P = moe_padded_rows_max(T, K, G). */
+ * Here P = N = T * K (permuted rows). */
 
 /* Forward.  Inputs: Xp (moe_permute of X), the routing outputs (counts is
- * not read; offsets, tile_off and sorted_src locate each row's routing
- * weight), topk weights [T,k] fp32, the six weight tensors.  Outputs:
+ * not read; offsets and tile_off define the tiles, sorted_src locates each
+ * row's routing weight), topk weights [T,k] fp32, the six weight tensors.  Outputs:
  *   Yp    [P,d]    bf16  w-scaled expert outputs (feed moe_unpermute_combine
  *                        with weights = NULL)
  *   h     [P,2f]   fp32  saved gate|up pre-activations

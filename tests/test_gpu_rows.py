@@ -1,4 +1,4 @@
-"""GPU parity of the row permute (bit-exact copy into the tile-padded grouped
+"""GPU parity of the row permute (bit-exact gather into expert-grouped sorted
 layout) and the combine (weighted gather-reduce, bf16 tolerance)."""
 import numpy as np
 import pytest
@@ -34,25 +34,15 @@ def routed(ids, E, shared=False):
 
 
 def expected_layout(ids_np, E, shared):
-    """Host-side: permuted row of every flat index and the source token of
-    every permuted row (-1 = padding), from the oracle's routing."""
+    """Host-side, from the oracle's routing: the source token of every
+    permuted row (row p = sorted position p) and the permuted row of every
+    flat index (its sorted position)."""
     T = ids_np.shape[0]
     if shared:
         ids_np = np.concatenate([ids_np, np.full((T, 1), E, dtype=ids_np.dtype)], 1)
     K = ids_np.shape[1]
-    G = E + int(shared)
-    rt = oracle.route(ids_np, G)
-    tiles = (rt["counts"] + 127) // 128
-    tile_off = np.concatenate([[0], np.cumsum(tiles)])
-    P = int(tile_off[-1]) * 128
-    src_tok = np.full(P, -1, dtype=np.int64)
-    prow = np.empty(T * K, dtype=np.int64)
-    for g in range(G):
-        seg = rt["sorted_src"][rt["offsets"][g]:rt["offsets"][g + 1]]
-        rows = tile_off[g] * 128 + np.arange(seg.size)
-        src_tok[rows] = seg // K
-        prow[seg] = rows
-    return src_tok, prow, P
+    rt = oracle.route(ids_np, E + int(shared))
+    return rt["sorted_src"] // K, rt["dest_pos"], T * K
 
 
 @pytest.mark.parametrize("T,E,k,dist,shared,d", [
@@ -63,17 +53,13 @@ def test_permute_bit_exact(T, E, k, dist, shared, d):
     ids = synth.topk_ids(T, E, k, dist, seed=2, device=DEV)
     X = synth.hidden_rows(T, d, seed=2, device=DEV)
     r, K, G = routed(ids, E, shared)
-    Pmax = L.moe_padded_rows_max(T, K, G)
-    Xp = torch.full((Pmax, d), 7.0, dtype=torch.bfloat16, device=DEV)
-    L.moe_permute(X, K, G, r["offsets"], r["tile_off"], r["sorted_src"], Xp)
+    Xp = torch.full((T * K, d), 7.0, dtype=torch.bfloat16, device=DEV)
+    L.moe_permute(X, K, r["dest_pos"], Xp)
     torch.cuda.synchronize()
-    src_tok, _, P = expected_layout(ids.cpu().numpy(), E, shared)
+    src_tok, _, N = expected_layout(ids.cpu().numpy(), E, shared)
     got = Xp.view(torch.int16).cpu().numpy()
     Xb = X.view(torch.int16).cpu().numpy()
-    exp = np.zeros((P, d), dtype=np.int16)
-    exp[src_tok >= 0] = Xb[src_tok[src_tok >= 0]]
-    np.testing.assert_array_equal(got[:P], exp)
-    assert np.all(got[P:] == torch.tensor(7.0, dtype=torch.bfloat16).view(torch.int16).item())
+    np.testing.assert_array_equal(got, Xb[src_tok])
 
 
 @pytest.mark.parametrize("T,E,k,dist,shared,d,weighted", [
@@ -82,14 +68,14 @@ def test_permute_bit_exact(T, E, k, dist, shared, d):
 def test_combine(T, E, k, dist, shared, d, weighted):
     ids = synth.topk_ids(T, E, k, dist, seed=4, device=DEV)
     r, K, G = routed(ids, E, shared)
-    Pmax = L.moe_padded_rows_max(T, K, G)
-    rows = synth.hidden_rows(Pmax, d, seed=5, device=DEV)
+    N = T * K
+    rows = synth.hidden_rows(N, d, seed=5, device=DEV)
     w = synth.combine_weights(T, k, seed=6, device=DEV) if weighted else None
-    scal = torch.randn(Pmax, generator=torch.Generator(DEV).manual_seed(3), device=DEV)
+    scal = torch.randn(N, generator=torch.Generator(DEV).manual_seed(3), device=DEV)
     out = torch.empty(T, d, dtype=torch.bfloat16, device=DEV)
     slot = torch.empty(T, k, dtype=torch.float32, device=DEV)
-    L.moe_unpermute_combine(rows, ids, r["dest_pos"], r["offsets"], r["tile_off"], E, shared,
-                            out, weights=w, row_scalars=scal, slot_out=slot)
+    L.moe_unpermute_combine(rows, r["dest_pos"], k, shared, out, weights=w, row_scalars=scal,
+                            slot_out=slot)
     torch.cuda.synchronize()
     _, prow, _ = expected_layout(ids.cpu().numpy(), E, shared)
     prow = prow.reshape(T, K)
@@ -110,12 +96,10 @@ def test_permute_combine_full_size_sampled(T, E, k, dist):
     X = synth.hidden_rows(T, d, seed=8, device=DEV)
     w = synth.combine_weights(T, k, seed=8, device=DEV)
     r, K, G = routed(ids, E)
-    Pmax = L.moe_padded_rows_max(T, K, G)
-    Xp = torch.empty(Pmax, d, dtype=torch.bfloat16, device=DEV)
-    L.moe_permute(X, K, G, r["offsets"], r["tile_off"], r["sorted_src"], Xp)
+    Xp = torch.empty(T * K, d, dtype=torch.bfloat16, device=DEV)
+    L.moe_permute(X, K, r["dest_pos"], Xp)
     Y = torch.empty(T, d, dtype=torch.bfloat16, device=DEV)
-    L.moe_unpermute_combine(Xp, ids, r["dest_pos"], r["offsets"], r["tile_off"], E, False, Y,
-                            weights=w)
+    L.moe_unpermute_combine(Xp, r["dest_pos"], k, False, Y, weights=w)
     torch.cuda.synchronize()
     # properties that hold at any size: the round trip gives sum_j w_j * X[t]
     rng = np.random.default_rng(0)
@@ -124,12 +108,8 @@ def test_permute_combine_full_size_sampled(T, E, k, dist):
     ws = w.cpu().numpy()[toks].astype(np.float64).sum(1, keepdims=True)
     assert_close_bf16(to64(Y[torch.from_numpy(toks).to(DEV)]), ws * Xs, "roundtrip")
     # and each sampled permuted row is the right token row, bit for bit
-    src_tok, prow, P = expected_layout(ids.cpu().numpy(), E, False)
-    prows = rng.choice(P, size=256, replace=False)
+    src_tok, _, N = expected_layout(ids.cpu().numpy(), E, False)
+    prows = rng.choice(N, size=256, replace=False)
     got = Xp[torch.from_numpy(prows).to(DEV)].view(torch.int16).cpu().numpy()
-    Xb = X.view(torch.int16)
-    for i, p in enumerate(prows):
-        if src_tok[p] >= 0:
-            np.testing.assert_array_equal(got[i], Xb[int(src_tok[p])].cpu().numpy())
-        else:
-            assert np.all(got[i] == 0)
+    ref = X.view(torch.int16)[torch.from_numpy(src_tok[prows]).to(DEV)].cpu().numpy()
+    np.testing.assert_array_equal(got, ref)

@@ -39,8 +39,6 @@ def test_library_exports_every_declared_symbol(lib):
 
 def test_sizes(lib):
     assert lib.moe_abi_version() == 1
-    assert lib.moe_padded_rows_max(256, 2, 8) == ((256 * 2 + 8 * 127 + 127) // 128) * 128
-    assert lib.moe_padded_rows_max(0, 2, 8) == -1
     assert lib.moe_route_workspace_size(4096, 8, 128) >= 128 * 4
     assert lib.moe_route_workspace_size(0, 8, 128) == 0
 
@@ -98,11 +96,13 @@ def test_rows_and_router_argument_errors(lib):
     from expert_routing_grouped_moe_gb300 import _lib
     P = ctypes.c_void_p
     fake = P(1 << 20)
-    assert lib.moe_permute(fake, 4, 12, 2, 8, fake, fake, fake, fake, None) == _lib.MOE_ERR_INVALID_ARG
-    assert lib.moe_permute(fake, 4, 16, 2, 8, None, fake, fake, fake, None) == _lib.MOE_ERR_INVALID_ARG
+    assert lib.moe_permute(fake, 4, 12, 2, fake, fake, None) == _lib.MOE_ERR_INVALID_ARG
+    assert lib.moe_permute(fake, 4, 16, 2, None, fake, None) == _lib.MOE_ERR_INVALID_ARG
     # row_scalars without slot_out
-    assert lib.moe_unpermute_combine(fake, fake, fake, fake, fake, 4, 16, 2, 8, 0, None, fake,
-                                     None, fake, None) == _lib.MOE_ERR_INVALID_ARG
+    assert lib.moe_unpermute_combine(fake, fake, 4, 16, 2, 0, None, fake, None, fake,
+                                     None) == _lib.MOE_ERR_INVALID_ARG
+    assert lib.moe_unpermute_combine(fake, fake, 4, 16, 2, 2, None, None, None, fake,
+                                     None) == _lib.MOE_ERR_INVALID_ARG
     assert lib.moe_router_topk(fake, 4, 8, 9, fake, fake, None) == _lib.MOE_ERR_INVALID_ARG
     assert lib.moe_router_topk(fake, 4, 2048, 2, fake, fake, None) == _lib.MOE_ERR_UNSUPPORTED
 

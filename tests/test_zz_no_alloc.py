@@ -77,7 +77,7 @@ def test_no_alloc_route_matches_route_twice_in_a_row(first, second):
 
 
 def test_no_alloc_route_rejects_too_large():
-    T, k, E = 1 << 20, 8, 129    # 129 groups x 4096 chunks > 2^19 entries
+    T, k, E = 1 << 20, 8, 1024   # its histogram would need 4 MiB
     ids = torch.zeros(1, 1, dtype=torch.int32, device=DEV)
     lib = L.load()
     dummy = ctypes.c_void_p(ids.data_ptr())
