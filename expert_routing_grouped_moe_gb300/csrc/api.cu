@@ -43,6 +43,10 @@ struct DevState {
   bool init = false;
   int* status = nullptr;
   int num_sms = 0;
+  // second stream for the backward's weight-gradient GEMMs (created on first use)
+  std::mutex aux_mu;
+  cudaStream_t aux = nullptr;
+  cudaEvent_t ev[4] = {nullptr, nullptr, nullptr, nullptr};
 };
 constexpr int kMaxDevices = 64;
 DevState g_dev[kMaxDevices];
@@ -117,6 +121,29 @@ struct ProbeScope {
   ProbeScope(const char* name, cudaStream_t st) : token(probe_begin(name, st)), s(st) {}
   ~ProbeScope() { probe_end(token, s); }
 };
+
+// The device's second stream and its fork/join events, created once.  Callers
+// hold st->aux_mu while enqueueing work that uses them.
+int aux_stream(DevState* st, cudaStream_t* out) {
+  if (st->aux == nullptr) {
+    cudaError_t e = cudaStreamCreateWithFlags(&st->aux, cudaStreamNonBlocking);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaStreamCreateWithFlags");
+    for (cudaEvent_t& ev : st->ev) {
+      e = cudaEventCreateWithFlags(&ev, cudaEventDisableTiming);
+      if (e != cudaSuccess) return cuda_fail(e, "cudaEventCreateWithFlags");
+    }
+  }
+  *out = st->aux;
+  return MOE_OK;
+}
+
+// `waiter` waits for the work enqueued on `from` so far.
+int stream_dep(cudaEvent_t ev, cudaStream_t from, cudaStream_t waiter) {
+  cudaError_t e = cudaEventRecord(ev, from);
+  if (e == cudaSuccess) e = cudaStreamWaitEvent(waiter, ev, 0);
+  if (e != cudaSuccess) return cuda_fail(e, "stream dependency");
+  return MOE_OK;
+}
 
 using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
                                    const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
@@ -518,40 +545,9 @@ int moe_lora_grouped_mlp_bwd(const moe_dims* dims, const moe_bf16* dYp, const mo
   const int nparts = kDwPartsPerTile * ntiles_f;
 
   const int64_t Nr = N * r, N2f = N * 2 * f;
-  {  // u = dYp B_dn -> pairs us = s*u, uw = s*w*u, xw = w * (s xa_dn)
-    GemmParams p = base;
-    SLICE(p, 0, dYp, N, d, MAP3(p.sl[0].b, B_dn, G, d, r, 64, 64), d);
-    p.nslices = 1; p.N = r; p.n_ntiles = (r + 63) / 64; p.ld0 = r; p.pair = Nr;
-    p.out0 = w.us; p.out1 = w.uw; p.out2 = w.xw; p.aux0 = xa_dn;
-    if ((rc = run_gemm({64, true, false, Epi::kLoRA}, p, R, st->num_sms, s, "u"))) return rc;
-  }
-  {  // g = dYp W_dn + us A_dn ; SwiGLU backward from fp32 h -> dh pair ; dw partials
-    GemmParams p = base;
-    SLICE(p, 0, dYp, N, d, MAP3(p.sl[0].b, W_dn, G, d, f, 64, 64), d);
-    SLICE(p, 1, w.us, N, r, MAP3(p.sl[1].b, A_dn, G, r, f, 64, 64), r);
-    SLICE(p, 2, w.us + Nr, N, r, MAP3(p.sl[2].b, A_dn, G, r, f, 64, 64), r);
-    p.nslices = 3; p.N = f; p.n_ntiles = ntiles_f;
-    p.fin = h; p.out0 = w.dh; p.ld0 = 2 * f; p.pair = N2f; p.fout = w.dwp; p.fstride = N;
-    if ((rc = run_gemm({256, true, false, Epi::kDgradDn}, p, R, st->num_sms, s, "dgrad_dn")))
-      return rc;
-  }
-  {  // v = dh B_gu (dh = hi + lo) -> vs pair = s*v
-    GemmParams p = base;
-    SLICE(p, 0, w.dh, N, 2 * f, MAP3(p.sl[0].b, B_gu, G, 2 * f, r, 64, 64), 2 * f);
-    SLICE(p, 1, w.dh + N2f, N, 2 * f, MAP3(p.sl[1].b, B_gu, G, 2 * f, r, 64, 64), 2 * f);
-    p.nslices = 2; p.N = r; p.n_ntiles = (r + 63) / 64; p.ld0 = r; p.pair = Nr; p.out0 = w.vs;
-    if ((rc = run_gemm({64, true, false, Epi::kLoRA}, p, R, st->num_sms, s, "v"))) return rc;
-  }
-  {  // dXp = dh W_gu + vs A_gu   (high halves: dX is an output, not a row reduction)
-    GemmParams p = base;
-    SLICE(p, 0, w.dh, N, 2 * f, MAP3(p.sl[0].b, W_gu, G, 2 * f, d, 64, 64), 2 * f);
-    SLICE(p, 1, w.vs, N, r, MAP3(p.sl[1].b, A_gu, G, r, d, 64, 64), r);
-    p.nslices = 2; p.N = d; p.n_ntiles = (d + 255) / 256; p.out0 = dXp; p.ld0 = d;
-    if ((rc = run_gemm({256, true, false, Epi::kStore}, p, R, st->num_sms, s, "dgrad_gu")))
-      return rc;
-  }
   // per-group LoRA gradients: sum over the group's rows of A^T [B_hi | B_lo],
-  // A from one exact bf16 source or a hi/lo pair
+  // A from one exact bf16 source or a hi/lo pair.  They run on the device's
+  // second stream, each as soon as its inputs exist, beside the dgrad chain.
   struct WgradJob {
     const moe_bf16* a;
     int a_pair;  // 1: a is a hi/lo pair buffer
@@ -567,7 +563,7 @@ int moe_lora_grouped_mlp_bwd(const moe_dims* dims, const moe_bf16* dYp, const mo
       {w.dh, 1, 2 * f, xa_gu, dB_gu, 0, "dB_gu"},
       {Xp, 0, d, w.vs, dA_gu, 1, "dA_gu"},
   };
-  for (const WgradJob& j : jobs) {
+  auto wgrad = [&](const WgradJob& j, cudaStream_t ss) -> int {
     GemmParams p = base;
     MAP2(p.sl[0].a, j.a, N, j.M, 64, 64);
     p.nslices = 1;
@@ -579,14 +575,58 @@ int moe_lora_grouped_mlp_bwd(const moe_dims* dims, const moe_bf16* dYp, const mo
     MAP2(p.wb_lo, j.b + Nr, N, r, 64, 64);
     p.M = j.M; p.N = r; p.n_ntiles = (j.M + 127) / 128;
     p.fout = j.out; p.fstride = static_cast<int64_t>(j.M) * r; p.transpose_out = j.transpose;
-    if ((rc = run_gemm({128, true, true, Epi::kWgrad}, p, R, st->num_sms, s, j.name))) return rc;
+    return run_gemm({128, true, true, Epi::kWgrad}, p, R, st->num_sms, ss, j.name);
+  };
+  std::lock_guard<std::mutex> aux_lock(st->aux_mu);
+  cudaStream_t aux = nullptr;
+  if ((rc = aux_stream(st, &aux))) return rc;
+
+  {  // u = dYp B_dn -> pairs us = s*u, uw = s*w*u, xw = w * (s xa_dn)
+    GemmParams p = base;
+    SLICE(p, 0, dYp, N, d, MAP3(p.sl[0].b, B_dn, G, d, r, 64, 64), d);
+    p.nslices = 1; p.N = r; p.n_ntiles = (r + 63) / 64; p.ld0 = r; p.pair = Nr;
+    p.out0 = w.us; p.out1 = w.uw; p.out2 = w.xw; p.aux0 = xa_dn;
+    if ((rc = run_gemm({64, true, false, Epi::kLoRA}, p, R, st->num_sms, s, "u"))) return rc;
   }
-  cudaError_t e;
+  if ((rc = stream_dep(st->ev[0], s, aux))) return rc;
+  if ((rc = wgrad(jobs[0], aux))) return rc;  // dB_dn
+  if ((rc = wgrad(jobs[1], aux))) return rc;  // dA_dn
+  {  // g = dYp W_dn + us A_dn ; SwiGLU backward from fp32 h -> dh pair ; dw partials
+    GemmParams p = base;
+    SLICE(p, 0, dYp, N, d, MAP3(p.sl[0].b, W_dn, G, d, f, 64, 64), d);
+    SLICE(p, 1, w.us, N, r, MAP3(p.sl[1].b, A_dn, G, r, f, 64, 64), r);
+    SLICE(p, 2, w.us + Nr, N, r, MAP3(p.sl[2].b, A_dn, G, r, f, 64, 64), r);
+    p.nslices = 3; p.N = f; p.n_ntiles = ntiles_f;
+    p.fin = h; p.out0 = w.dh; p.ld0 = 2 * f; p.pair = N2f; p.fout = w.dwp; p.fstride = N;
+    if ((rc = run_gemm({256, true, false, Epi::kDgradDn}, p, R, st->num_sms, s, "dgrad_dn")))
+      return rc;
+  }
+  if ((rc = stream_dep(st->ev[1], s, aux))) return rc;
   {
-    ProbeScope probe("dw_reduce", s);
-    e = launch_sum_parts(w.dwp, nparts, N, N, dw_rows, s);
+    ProbeScope probe("dw_reduce", aux);
+    const cudaError_t e = launch_sum_parts(w.dwp, nparts, N, N, dw_rows, aux);
+    if (e != cudaSuccess) return cuda_fail(e, "dw reduce");
   }
-  if (e != cudaSuccess) return cuda_fail(e, "dw reduce");
+  if ((rc = wgrad(jobs[2], aux))) return rc;  // dB_gu
+  {  // v = dh B_gu (dh = hi + lo) -> vs pair = s*v
+    GemmParams p = base;
+    SLICE(p, 0, w.dh, N, 2 * f, MAP3(p.sl[0].b, B_gu, G, 2 * f, r, 64, 64), 2 * f);
+    SLICE(p, 1, w.dh + N2f, N, 2 * f, MAP3(p.sl[1].b, B_gu, G, 2 * f, r, 64, 64), 2 * f);
+    p.nslices = 2; p.N = r; p.n_ntiles = (r + 63) / 64; p.ld0 = r; p.pair = Nr; p.out0 = w.vs;
+    if ((rc = run_gemm({64, true, false, Epi::kLoRA}, p, R, st->num_sms, s, "v"))) return rc;
+  }
+  if ((rc = stream_dep(st->ev[2], s, aux))) return rc;
+  if ((rc = wgrad(jobs[3], aux))) return rc;  // dA_gu
+  {  // dXp = dh W_gu + vs A_gu   (high halves: dX is an output, not a row reduction)
+    GemmParams p = base;
+    SLICE(p, 0, w.dh, N, 2 * f, MAP3(p.sl[0].b, W_gu, G, 2 * f, d, 64, 64), 2 * f);
+    SLICE(p, 1, w.vs, N, r, MAP3(p.sl[1].b, A_gu, G, r, d, 64, 64), r);
+    p.nslices = 2; p.N = d; p.n_ntiles = (d + 255) / 256; p.out0 = dXp; p.ld0 = d;
+    if ((rc = run_gemm({256, true, false, Epi::kStore}, p, R, st->num_sms, s, "dgrad_gu")))
+      return rc;
+  }
+  // join: everything on the second stream completes before later work on s
+  if ((rc = stream_dep(st->ev[3], aux, s))) return rc;
   return ok();
 }
 

@@ -346,13 +346,9 @@ __device__ __forceinline__ void epi_dgrad_dn(const GemmParams& p, const TileInfo
                   p.ld0 * 4, 2, 2, clamp_bytes(static_cast<int64_t>(f - j0) * 4, 64), nrows};
   };
   const int jbase = ti.nt * BN + hf * (BN / 2);
-  uint4 pre[8];
-  stg_fetch(pre, lane, h_planes(jbase));
-  stg_commit(stg, lane, pre);
-  __syncwarp();
   float dot = 0.f;
-#pragma unroll 1
-  for (int sub = 0; sub < kSubs; ++sub) {
+  // one 16-column chunk: h from the staging tile, g from TMEM, dh pair out
+  auto process = [&](int sub) {
     const int j0 = jbase + sub * 16;
     float gt[16], up[16], gr[16];
 #pragma unroll
@@ -364,7 +360,6 @@ __device__ __forceinline__ void epi_dgrad_dn(const GemmParams& p, const TileInfo
       up[4 * c] = __uint_as_float(y.x); up[4 * c + 1] = __uint_as_float(y.y);
       up[4 * c + 2] = __uint_as_float(y.z); up[4 * c + 3] = __uint_as_float(y.w);
     }
-    if (sub + 1 < kSubs) stg_fetch(pre, lane, h_planes(j0 + 16));  // next chunk in flight
     tmem_ld16(tq + hf * (BN / 2) + sub * 16, gr);
     float dg[16], du[16];
 #pragma unroll
@@ -391,17 +386,33 @@ __device__ __forceinline__ void epi_dgrad_dn(const GemmParams& p, const TileInfo
     sts128(stg_at(stg, lane, 6), b0);
     sts128(stg_at(stg, lane, 7), b1);
     __syncwarp();
-    {
-      Planes pl{reinterpret_cast<char*>(db + j0), reinterpret_cast<char*>(db + p.pair + j0),
-                reinterpret_cast<char*>(db + f + j0),
-                reinterpret_cast<char*>(db + p.pair + f + j0), p.ld0 * 2, 1, 4,
-                clamp_bytes(static_cast<int64_t>(f - j0) * 2, 32), nrows};
-      stg_flush(stg, lane, pl);
-    }
+    Planes pl{reinterpret_cast<char*>(db + j0), reinterpret_cast<char*>(db + p.pair + j0),
+              reinterpret_cast<char*>(db + f + j0),
+              reinterpret_cast<char*>(db + p.pair + f + j0), p.ld0 * 2, 1, 4,
+              clamp_bytes(static_cast<int64_t>(f - j0) * 2, 32), nrows};
+    stg_flush(stg, lane, pl);
     __syncwarp();
+  };
+  // h chunks are fetched two ahead (two register buffers in flight)
+  uint4 pa[8], pb[8];
+  stg_fetch(pa, lane, h_planes(jbase));
+  stg_commit(stg, lane, pa);
+  __syncwarp();
+  if (kSubs > 1) stg_fetch(pa, lane, h_planes(jbase + 16));
+  if (kSubs > 2) stg_fetch(pb, lane, h_planes(jbase + 32));
+#pragma unroll 1
+  for (int sub = 0; sub < kSubs; sub += 2) {
+    process(sub);
     if (sub + 1 < kSubs) {
-      stg_commit(stg, lane, pre);
+      stg_commit(stg, lane, pa);
       __syncwarp();
+      if (sub + 3 < kSubs) stg_fetch(pa, lane, h_planes(jbase + (sub + 3) * 16));
+      process(sub + 1);
+    }
+    if (sub + 2 < kSubs) {
+      stg_commit(stg, lane, pb);
+      __syncwarp();
+      if (sub + 4 < kSubs) stg_fetch(pb, lane, h_planes(jbase + (sub + 4) * 16));
     }
   }
   if (lane < nrows)

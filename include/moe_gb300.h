@@ -232,7 +232,12 @@ MOE_API size_t moe_mlp_bwd_workspace_size(const moe_dims* dims);
  *   dB_gu[g] = s sum_p dh^T xa             [G,2f,r] fp32
  *   dA_gu[g] = s sum_p v^T Xp              [G,r,d] fp32
  * Gradients are overwritten (not accumulated); groups with no rows get zeros.
- * ws: >= moe_mlp_bwd_workspace_size bytes of device scratch, 16-byte aligned. */
+ * ws: >= moe_mlp_bwd_workspace_size bytes of device scratch, 16-byte aligned.
+ * The four weight-gradient GEMMs run on a second stream that the library
+ * creates once per device (no device memory); it forks from `stream` after
+ * their inputs exist and joins back before the call returns, so all results
+ * are ordered on `stream` as if everything ran there.  Calls from several host
+ * threads serialise their enqueueing on that stream. */
 MOE_API int moe_lora_grouped_mlp_bwd(const moe_dims* dims, const moe_bf16* dYp, const moe_bf16* Xp,
                              const int32_t* counts, const int32_t* offsets,
                              const int32_t* tile_off, const int32_t* sorted_src,
