@@ -482,7 +482,7 @@ int moe_lora_grouped_mlp_fwd(const moe_dims* dims, const moe_bf16* Xp, const int
     SLICE(p, 1, xa_gu, N, r, MAP3(p.sl[1].b, B_gu, G, 2 * f, r, 128, 64), r);
     SLICE(p, 2, xa_gu + Nr, N, r, MAP3(p.sl[2].b, B_gu, G, 2 * f, r, 128, 64), r);
     p.nslices = 3; p.N = f; p.n_ntiles = (f + 127) / 128; p.b_split = f;
-    p.fout = h; p.ld0 = 2 * f; p.out0 = act; p.pair = Nf;
+    p.fout = h; p.ldf = 32 * ((f + 15) / 16); p.ld0 = 2 * f; p.out0 = act; p.pair = Nf;
     if ((rc = run_gemm({256, false, false, Epi::kSwiGLU}, p, R, st->num_sms, s, "gate_up")))
       return rc;
   }
@@ -597,7 +597,8 @@ int moe_lora_grouped_mlp_bwd(const moe_dims* dims, const moe_bf16* dYp, const mo
     SLICE(p, 1, w.us, N, r, MAP3(p.sl[1].b, A_dn, G, r, f, 64, 64), r);
     SLICE(p, 2, w.us + Nr, N, r, MAP3(p.sl[2].b, A_dn, G, r, f, 64, 64), r);
     p.nslices = 3; p.N = f; p.n_ntiles = ntiles_f;
-    p.fin = h; p.out0 = w.dh; p.ld0 = 2 * f; p.pair = N2f; p.fout = w.dwp; p.fstride = N;
+    p.fin = h; p.ldf = 32 * ((f + 15) / 16);
+    p.out0 = w.dh; p.ld0 = 2 * f; p.pair = N2f; p.fout = w.dwp; p.fstride = N;
     if ((rc = run_gemm({256, true, false, Epi::kDgradDn}, p, R, st->num_sms, s, "dgrad_dn")))
       return rc;
   }

@@ -270,9 +270,11 @@ __device__ __forceinline__ void epi_swiglu(const GemmParams& p, const TileInfo& 
     }
     __syncwarp();
     {
-      float* hb = p.fout + row0 * p.ld0;
-      Planes pl{reinterpret_cast<char*>(hb + j0), reinterpret_cast<char*>(hb + f + j0), nullptr,
-                nullptr, p.ld0 * 4, 2, 2, clamp_bytes(static_cast<int64_t>(f - j0) * 4, 64), nrows};
+      // h row layout: features in chunks of 16, [gate 16 | up 16] per chunk,
+      // so one chunk is one 128-byte line
+      float* hb = p.fout + row0 * p.ldf;
+      Planes pl{reinterpret_cast<char*>(hb + 2 * j0), nullptr, nullptr, nullptr, p.ldf * 4, 3,
+                1, j0 < f ? 128 : 0, nrows};
       stg_flush(stg, lane, pl);
     }
     __syncwarp();
@@ -337,13 +339,12 @@ __device__ __forceinline__ void epi_dgrad_dn(const GemmParams& p, const TileInfo
   // this warp: columns hf*BN/2 + [0, BN/2) in chunks of 16
   const int f = p.N;
   const float w = lane < nrows ? row_weight(p, row0 + lane) : 0.f;
-  const float* hb = p.fin + row0 * p.ld0;     // h [rows, 2f] fp32
+  const float* hb = p.fin + row0 * p.ldf;     // h rows: [gate 16 | up 16] per chunk, fp32
   uint16_t* db = p.out0 + row0 * p.ld0;       // dh pair [rows, 2f]
   constexpr int kSubs = (BN / 2) / 16;
   auto h_planes = [&](int j0) {
-    return Planes{reinterpret_cast<char*>(const_cast<float*>(hb + j0)),
-                  reinterpret_cast<char*>(const_cast<float*>(hb + f + j0)), nullptr, nullptr,
-                  p.ld0 * 4, 2, 2, clamp_bytes(static_cast<int64_t>(f - j0) * 4, 64), nrows};
+    return Planes{reinterpret_cast<char*>(const_cast<float*>(hb + 2 * j0)), nullptr, nullptr,
+                  nullptr, p.ldf * 4, 3, 1, j0 < f ? 128 : 0, nrows};
   };
   const int jbase = ti.nt * BN + hf * (BN / 2);
   float dot = 0.f;
@@ -364,6 +365,7 @@ __device__ __forceinline__ void epi_dgrad_dn(const GemmParams& p, const TileInfo
     float dg[16], du[16];
 #pragma unroll
     for (int i = 0; i < 16; ++i) {
+      if (j0 + i >= f) gt[i] = up[i] = 0.f;  // columns past f of a partial chunk
       const float sg = sigmoidf_(gt[i]);
       const float sl = gt[i] * sg;
       dot = fmaf(sl * up[i], gr[i], dot);

@@ -98,6 +98,7 @@ struct GemmParams {
   float* fout;        // fp32 output: h (SwiGLU), dw partials (dgrad), weight grad (wgrad)
   const float* fin;   // fp32 input: h (dgrad)
   int64_t ld0;        // leading dimension (elements) of out*/aux0 rows
+  int64_t ldf;        // leading dimension (floats) of the fp32 h buffer (fout / fin)
   int64_t pair;       // element offset from the hi to the lo half of a pair buffer
   int64_t fstride;    // stride between dw partial slices, or group stride of fout
   int transpose_out;  // wgrad: write fout[g][n][m] instead of fout[g][m][n]

@@ -47,7 +47,7 @@ class MoELoRALayer:
         self.Xp = torch.empty(P, d, **bf)
         self.Yp = torch.empty(P, d, **bf)
         # saved intermediates: h in fp32; act / xa_gu / xa_dn as hi+lo bf16 pairs
-        self.h = torch.empty(P, 2 * f, **f32)
+        self.h = torch.empty(P, 32 * ((f + 15) // 16), **f32)  # [gate 16 | up 16] chunks
         self.act = torch.empty(2, P, f, **bf)
         self.xa_gu = torch.empty(2, P, r, **bf)
         self.xa_dn = torch.empty(2, P, r, **bf)
@@ -105,3 +105,12 @@ class MoELoRALayer:
         """One forward + backward pass of the layer (the hot path)."""
         self.forward(X, ids, topk_w, stream)
         return self.backward(dY, stream)
+
+    def h_gate_up(self):
+        """The saved pre-activations as a plain [N, 2f] (gate | up) fp32 tensor
+        (un-interleaves the 16-feature chunks of the stored layout)."""
+        n, f = self.N, self.f
+        hc = self.h.view(n, -1, 2, 16)
+        gate = hc[:, :, 0, :].reshape(n, -1)[:, :f]
+        up = hc[:, :, 1, :].reshape(n, -1)[:, :f]
+        return torch.cat([gate, up], dim=1)

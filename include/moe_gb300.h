@@ -190,7 +190,8 @@ MOE_API int moe_unpermute_combine(const moe_bf16* rows, const int32_t* dest_pos,
 
 /* Precision of saved intermediates.  Every value that later feeds a sum over
  * the rows of an expert (the LoRA weight gradients and the routing-weight
- * gradient) keeps ~16 significant bits: h is stored in fp32, and the other
+ * gradient) keeps ~16 significant bits: h is stored in fp32 (interleaved in
+ * 16-feature chunks so that each chunk is one 128-byte line), and the other
  * such intermediates as "pair" buffers [2, P, cols] of bf16 with
  * value = pair[0] + pair[1] (pair[0] = bf16(v), pair[1] = bf16(v - pair[0])).
  * The tensor cores consume a pair as two bf16 operands (extra K steps).
@@ -201,7 +202,9 @@ MOE_API int moe_unpermute_combine(const moe_bf16* rows, const int32_t* dest_pos,
  * row's routing weight), topk weights [T,k] fp32, the six weight tensors.  Outputs:
  *   Yp    [P,d]    bf16  w-scaled expert outputs (feed moe_unpermute_combine
  *                        with weights = NULL)
- *   h     [P,2f]   fp32  saved gate|up pre-activations
+ *   h     [P,hs]   fp32  saved gate and up pre-activations, hs = 32*ceil(f/16):
+ *                        features in chunks of 16, row layout
+ *                        [gate c*16..c*16+15 | up c*16..c*16+15] for chunk c
  *   act   [2,P,f]  bf16 pair  saved silu(gate) * up
  *   xa_gu [2,P,r]  bf16 pair  saved s * Xp A_gu^T
  *   xa_dn [2,P,r]  bf16 pair  saved s * act A_dn^T

@@ -77,7 +77,8 @@ def test_layer_full_parity(name):
     wfull = np.concatenate([w_np, np.ones((cfg.T, 1))], 1) if cfg.shared else w_np
     groups, N = group_rows(ids_np, cfg)
     # forward intermediates, group by group, in the permuted layout
-    bufs = {n: to64(getattr(layer, n)) for n in ("Xp", "xa_gu", "h", "act", "xa_dn", "Yp")}
+    bufs = {n: to64(getattr(layer, n)) for n in ("Xp", "xa_gu", "act", "xa_dn", "Yp")}
+    bufs["h"] = to64(layer.h_gate_up())
     for n in ("xa_gu", "act", "xa_dn"):  # hi + lo pairs carry ~16 significant bits
         bufs[n] = bufs[n][0] + bufs[n][1]
     for gi, tok, flat, prow in groups:
