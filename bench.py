@@ -361,7 +361,7 @@ def routing_sweep(torch, L, synth, dev, peaks, points=((1 << 20, 128, 8), (1 << 
 
 def run_ours(args):
     import torch
-    from expert_routing_grouped_moe_gb300 import (LAUNCHES_BWD, LAUNCHES_FWD, MoELoRALayer,
+    from expert_routing_grouped_moe_gb300 import (MoELoRALayer,
                                                   _lib as L, build, synth)
 
     dist, rank, world, local = dist_setup(torch)
@@ -511,7 +511,7 @@ def run_ours(args):
         "cpu_baseline": cpu,
         "e2e": {"value": world * cfg.T / (e2e_ms / 1e3), "unit": "tokens/s",
                 "ms_per_step": e2e_ms, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
-        "gpu_launches": args.steps * (LAUNCHES_FWD + LAUNCHES_BWD),
+        "gpu_launches": args.steps * layer.launches_per_step(),
         "clocks": clocks,
     }
     if dist is not None:

@@ -79,9 +79,9 @@ def load(path: str = LIB_PATH):
             "moe_permute": (ctypes.c_int, [_P, _I, _I, _I, _P, _P, _P]),
             "moe_unpermute_combine": (ctypes.c_int, [_P, _P, _I, _I, _I, _I, _P, _P, _P, _P,
                                                      _P]),
-            "moe_lora_grouped_mlp_fwd": (ctypes.c_int, [ctypes.POINTER(MoeDims)] + [_P] * 18),
+            "moe_lora_grouped_mlp_fwd": (ctypes.c_int, [ctypes.POINTER(MoeDims)] + [_P] * 19),
             "moe_mlp_bwd_workspace_size": (_SZ, [ctypes.POINTER(MoeDims)]),
-            "moe_lora_grouped_mlp_bwd": (ctypes.c_int, [ctypes.POINTER(MoeDims)] + [_P] * 24
+            "moe_lora_grouped_mlp_bwd": (ctypes.c_int, [ctypes.POINTER(MoeDims)] + [_P] * 26
                                          + [_SZ, _P]),
             "moe_status": (ctypes.c_int, [_P]),
             "moe_last_error": (ctypes.c_char_p, []),
@@ -190,11 +190,13 @@ def moe_unpermute_combine(rows, dest_pos, k, shared_expert, out, weights=None, r
         _bf(out, "out"), _stream(stream)), "moe_unpermute_combine")
 
 
-def moe_lora_grouped_mlp_fwd(dims: MoeDims, Xp, counts, offsets, tile_off, sorted_src, topk_w,
+def moe_lora_grouped_mlp_fwd(dims: MoeDims, Xp, X, counts, offsets, tile_off, sorted_src, topk_w,
                              W_gu, A_gu, B_gu, W_dn, A_dn, B_dn, Yp, h, act, xa_gu, xa_dn,
                              stream=None):
+    """Pass the permuted rows Xp, or Xp=None and the token rows X (gathered)."""
     _check(load().moe_lora_grouped_mlp_fwd(
-        ctypes.byref(dims), _bf(Xp, "Xp"), _i32(counts, "counts"), _i32(offsets, "offsets"),
+        ctypes.byref(dims), _bf(Xp, "Xp"), _bf(X, "X"), _i32(counts, "counts"),
+        _i32(offsets, "offsets"),
         _i32(tile_off, "tile_off"), _i32(sorted_src, "sorted_src"), _f32(topk_w, "topk_w"),
         _bf(W_gu, "W_gu"), _bf(A_gu, "A_gu"), _bf(B_gu, "B_gu"), _bf(W_dn, "W_dn"),
         _bf(A_dn, "A_dn"), _bf(B_dn, "B_dn"), _bf(Yp, "Yp"), _f32(h, "h"), _bf(act, "act"),
@@ -205,11 +207,14 @@ def moe_mlp_bwd_workspace_size(dims: MoeDims) -> int:
     return int(load().moe_mlp_bwd_workspace_size(ctypes.byref(dims)))
 
 
-def moe_lora_grouped_mlp_bwd(dims: MoeDims, dYp, Xp, counts, offsets, tile_off, sorted_src,
-                             topk_w, W_gu, A_gu, B_gu, W_dn, A_dn, B_dn, h, act, xa_gu, xa_dn,
-                             dXp, dw_rows, dA_gu, dB_gu, dA_dn, dB_dn, ws, stream=None):
+def moe_lora_grouped_mlp_bwd(dims: MoeDims, dYp, dY, Xp, X, counts, offsets, tile_off,
+                             sorted_src, topk_w, W_gu, A_gu, B_gu, W_dn, A_dn, B_dn, h, act,
+                             xa_gu, xa_dn, dXp, dw_rows, dA_gu, dB_gu, dA_dn, dB_dn, ws,
+                             stream=None):
+    """Pass permuted rows (dYp, Xp) or None and the token rows (dY, X)."""
     _check(load().moe_lora_grouped_mlp_bwd(
-        ctypes.byref(dims), _bf(dYp, "dYp"), _bf(Xp, "Xp"), _i32(counts, "counts"),
+        ctypes.byref(dims), _bf(dYp, "dYp"), _bf(dY, "dY"), _bf(Xp, "Xp"), _bf(X, "X"),
+        _i32(counts, "counts"),
         _i32(offsets, "offsets"), _i32(tile_off, "tile_off"), _i32(sorted_src, "sorted_src"),
         _f32(topk_w, "topk_w"), _bf(W_gu, "W_gu"), _bf(A_gu, "A_gu"), _bf(B_gu, "B_gu"),
         _bf(W_dn, "W_dn"), _bf(A_dn, "A_dn"), _bf(B_dn, "B_dn"), _f32(h, "h"), _bf(act, "act"),

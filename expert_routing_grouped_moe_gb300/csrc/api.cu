@@ -303,6 +303,23 @@ int run_gemm(const GemmShape& sh, GemmParams& p, int64_t row_tiles, int num_sms,
       return fail(MOE_ERR_CUDA, "tensor map encode failed (%s)", #ptr);            \
   } while (0)
 
+// Slice i's A operand: the permuted rows `perm` [N, cols] (TMA), or
+// (perm == NULL) token rows `tok` [T, cols] gathered by sorted_src (cp.async).
+#define SLICE_ROWS(p, i, perm, tok, cols, bexpr, kext)                                 \
+  do {                                                                               \
+    if ((perm) != nullptr) {                                                         \
+      MAP2((p).sl[i].a, (perm), N, (cols), 128, 64);                                 \
+    } else {                                                                         \
+      (p).sl[i].gather = 1;                                                          \
+      (p).sl[i].gsrc = (tok);                                                        \
+      (p).sl[i].gld = (cols);                                                        \
+      (p).sl[i].gcols = (cols);                                                      \
+      (p).gather_any = 1;                                                            \
+    }                                                                                \
+    bexpr;                                                                           \
+    (p).sl[i].K = (kext);                                                            \
+  } while (0)
+
 #define SLICE(p, i, amap_ptr, amap_rows, amap_cols, bexpr, kext)                  \
   do {                                                                           \
     MAP2((p).sl[i].a, (amap_ptr), (amap_rows), (amap_cols), 128, 64);            \
@@ -442,7 +459,8 @@ int moe_unpermute_combine(const moe_bf16* rows, const int32_t* dest_pos, int32_t
   return ok();
 }
 
-int moe_lora_grouped_mlp_fwd(const moe_dims* dims, const moe_bf16* Xp, const int32_t* counts,
+int moe_lora_grouped_mlp_fwd(const moe_dims* dims, const moe_bf16* Xp, const moe_bf16* X,
+                             const int32_t* counts,
                              const int32_t* offsets, const int32_t* tile_off,
                              const int32_t* sorted_src, const float* topk_w,
                              const moe_bf16* W_gu, const moe_bf16* A_gu, const moe_bf16* B_gu,
@@ -452,7 +470,10 @@ int moe_lora_grouped_mlp_fwd(const moe_dims* dims, const moe_bf16* Xp, const int
   (void)counts;
   int rc = check_dims(dims);
   if (rc) return rc;
-  MOE_CHECK_PTR(Xp);
+  if ((Xp == nullptr) == (X == nullptr))
+    return fail(MOE_ERR_INVALID_ARG, "pass exactly one of Xp (permuted rows) and X (token rows)");
+  if (Xp) MOE_CHECK_PTR(Xp);
+  if (X) MOE_CHECK_PTR(X);
   MOE_CHECK_PTR(W_gu); MOE_CHECK_PTR(A_gu); MOE_CHECK_PTR(B_gu);
   MOE_CHECK_PTR(W_dn); MOE_CHECK_PTR(A_dn); MOE_CHECK_PTR(B_dn);
   MOE_CHECK_PTR(Yp); MOE_CHECK_PTR(h); MOE_CHECK_PTR(act); MOE_CHECK_PTR(xa_gu);
@@ -472,13 +493,13 @@ int moe_lora_grouped_mlp_fwd(const moe_dims* dims, const moe_bf16* Xp, const int
   const int64_t Nf = N * f, Nr = N * r;
   {  // xa_gu pair = s * Xp A_gu^T
     GemmParams p = base;
-    SLICE(p, 0, Xp, N, d, MAP3(p.sl[0].b, A_gu, G, r, d, 64, 64), d);
+    SLICE_ROWS(p, 0, Xp, X, d, MAP3(p.sl[0].b, A_gu, G, r, d, 64, 64), d);
     p.nslices = 1; p.N = r; p.n_ntiles = (r + 63) / 64; p.out0 = xa_gu; p.ld0 = r; p.pair = Nr;
     if ((rc = run_gemm({64, false, false, Epi::kLoRA}, p, R, st->num_sms, s, "xa_gu"))) return rc;
   }
   {  // h = Xp W_gu^T + (s xa) B_gu^T (fp32) ; act pair = silu(gate) * up
     GemmParams p = base;
-    SLICE(p, 0, Xp, N, d, MAP3(p.sl[0].b, W_gu, G, 2 * f, d, 128, 64), d);
+    SLICE_ROWS(p, 0, Xp, X, d, MAP3(p.sl[0].b, W_gu, G, 2 * f, d, 128, 64), d);
     SLICE(p, 1, xa_gu, N, r, MAP3(p.sl[1].b, B_gu, G, 2 * f, r, 128, 64), r);
     SLICE(p, 2, xa_gu + Nr, N, r, MAP3(p.sl[2].b, B_gu, G, 2 * f, r, 128, 64), r);
     p.nslices = 3; p.N = f; p.n_ntiles = (f + 127) / 128; p.b_split = f;
@@ -509,7 +530,8 @@ size_t moe_mlp_bwd_workspace_size(const moe_dims* dims) {
   return bwd_layout(dims, nullptr).bytes;
 }
 
-int moe_lora_grouped_mlp_bwd(const moe_dims* dims, const moe_bf16* dYp, const moe_bf16* Xp,
+int moe_lora_grouped_mlp_bwd(const moe_dims* dims, const moe_bf16* dYp, const moe_bf16* dY,
+                             const moe_bf16* Xp, const moe_bf16* X,
                              const int32_t* counts, const int32_t* offsets,
                              const int32_t* tile_off, const int32_t* sorted_src,
                              const float* topk_w, const moe_bf16* W_gu, const moe_bf16* A_gu,
@@ -521,7 +543,14 @@ int moe_lora_grouped_mlp_bwd(const moe_dims* dims, const moe_bf16* dYp, const mo
   (void)counts;
   int rc = check_dims(dims);
   if (rc) return rc;
-  MOE_CHECK_PTR(dYp); MOE_CHECK_PTR(Xp);
+  if ((dYp == nullptr) == (dY == nullptr))
+    return fail(MOE_ERR_INVALID_ARG, "pass exactly one of dYp (permuted rows) and dY (token rows)");
+  if ((Xp == nullptr) == (X == nullptr))
+    return fail(MOE_ERR_INVALID_ARG, "pass exactly one of Xp (permuted rows) and X (token rows)");
+  if (dYp) MOE_CHECK_PTR(dYp);
+  if (dY) MOE_CHECK_PTR(dY);
+  if (Xp) MOE_CHECK_PTR(Xp);
+  if (X) MOE_CHECK_PTR(X);
   MOE_CHECK_PTR(W_gu); MOE_CHECK_PTR(A_gu); MOE_CHECK_PTR(B_gu);
   MOE_CHECK_PTR(W_dn); MOE_CHECK_PTR(A_dn); MOE_CHECK_PTR(B_dn);
   MOE_CHECK_PTR(h); MOE_CHECK_PTR(act); MOE_CHECK_PTR(xa_gu); MOE_CHECK_PTR(xa_dn);
@@ -550,6 +579,7 @@ int moe_lora_grouped_mlp_bwd(const moe_dims* dims, const moe_bf16* dYp, const mo
   // second stream, each as soon as its inputs exist, beside the dgrad chain.
   struct WgradJob {
     const moe_bf16* a;
+    const moe_bf16* a_tok;  // token rows to gather when a == NULL
     int a_pair;  // 1: a is a hi/lo pair buffer
     int M;
     const uint16_t* b;  // hi/lo pair buffer [2, N, r]
@@ -558,14 +588,22 @@ int moe_lora_grouped_mlp_bwd(const moe_dims* dims, const moe_bf16* dYp, const mo
     const char* name;
   };
   const WgradJob jobs[4] = {
-      {dYp, 0, d, w.xw, dB_dn, 0, "dB_dn"},
-      {act, 1, f, w.uw, dA_dn, 1, "dA_dn"},
-      {w.dh, 1, 2 * f, xa_gu, dB_gu, 0, "dB_gu"},
-      {Xp, 0, d, w.vs, dA_gu, 1, "dA_gu"},
+      {dYp, dY, 0, d, w.xw, dB_dn, 0, "dB_dn"},
+      {act, nullptr, 1, f, w.uw, dA_dn, 1, "dA_dn"},
+      {w.dh, nullptr, 1, 2 * f, xa_gu, dB_gu, 0, "dB_gu"},
+      {Xp, X, 0, d, w.vs, dA_gu, 1, "dA_gu"},
   };
   auto wgrad = [&](const WgradJob& j, cudaStream_t ss) -> int {
     GemmParams p = base;
-    MAP2(p.sl[0].a, j.a, N, j.M, 64, 64);
+    if (j.a != nullptr) {
+      MAP2(p.sl[0].a, j.a, N, j.M, 64, 64);
+    } else {
+      p.sl[0].gather = 1;
+      p.sl[0].gsrc = j.a_tok;
+      p.sl[0].gld = j.M;
+      p.sl[0].gcols = j.M;
+      p.gather_any = 1;
+    }
     p.nslices = 1;
     if (j.a_pair) {
       MAP2(p.sl[1].a, j.a + N * static_cast<int64_t>(j.M), N, j.M, 64, 64);
@@ -583,7 +621,7 @@ int moe_lora_grouped_mlp_bwd(const moe_dims* dims, const moe_bf16* dYp, const mo
 
   {  // u = dYp B_dn -> pairs us = s*u, uw = s*w*u, xw = w * (s xa_dn)
     GemmParams p = base;
-    SLICE(p, 0, dYp, N, d, MAP3(p.sl[0].b, B_dn, G, d, r, 64, 64), d);
+    SLICE_ROWS(p, 0, dYp, dY, d, MAP3(p.sl[0].b, B_dn, G, d, r, 64, 64), d);
     p.nslices = 1; p.N = r; p.n_ntiles = (r + 63) / 64; p.ld0 = r; p.pair = Nr;
     p.out0 = w.us; p.out1 = w.uw; p.out2 = w.xw; p.aux0 = xa_dn;
     if ((rc = run_gemm({64, true, false, Epi::kLoRA}, p, R, st->num_sms, s, "u"))) return rc;
@@ -593,7 +631,7 @@ int moe_lora_grouped_mlp_bwd(const moe_dims* dims, const moe_bf16* dYp, const mo
   if ((rc = wgrad(jobs[1], aux))) return rc;  // dA_dn
   {  // g = dYp W_dn + us A_dn ; SwiGLU backward from fp32 h -> dh pair ; dw partials
     GemmParams p = base;
-    SLICE(p, 0, dYp, N, d, MAP3(p.sl[0].b, W_dn, G, d, f, 64, 64), d);
+    SLICE_ROWS(p, 0, dYp, dY, d, MAP3(p.sl[0].b, W_dn, G, d, f, 64, 64), d);
     SLICE(p, 1, w.us, N, r, MAP3(p.sl[1].b, A_dn, G, r, f, 64, 64), r);
     SLICE(p, 2, w.us + Nr, N, r, MAP3(p.sl[2].b, A_dn, G, r, f, 64, 64), r);
     p.nslices = 3; p.N = f; p.n_ntiles = ntiles_f;

@@ -527,7 +527,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < S; ++i) {
-      mbar_init(full_bar + i, 1);
+      mbar_init(full_bar + i, p.gather_any ? 1 + 32 : 1);  // + one arrival per producer lane
       mbar_init(empty_bar + i, 1);
     }
     for (int i = 0; i < 2; ++i) {
@@ -559,52 +559,122 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
   const int num_tiles =
       WGRAD ? p.G * p.n_ntiles : min(__ldg(p.tile_off + p.G) * p.n_ntiles, p.max_tiles);
 
-  if (warp == 0 && lane == 0) {
+  if (warp == 0) {
     // ------------------------------------------------------------ producer
+    // Lane 0 waits for free stages and issues the TMA tile copies.  A gathered
+    // A operand (token rows picked by sorted_src) is copied by all 32 lanes
+    // with 16-byte cp.async into the 128B-swizzled layout TMA would produce.
+    // When any slice gathers, every lane arrives on each stage's full barrier
+    // (which then expects 1 + 32 arrivals) once its copies so far have
+    // completed; the MMA issuer fences them for the async proxy.
     int stage = 0;
     uint32_t phase = 0;
     int armed[S];
 #pragma unroll
     for (int i = 0; i < S; ++i) armed[i] = -1;
     bool ok = true;
+    const bool lanes_arrive = p.gather_any != 0;
+    // Token rows of the permuted rows first + lane + 32*i (i < n): y[i].  Rows
+    // past the group's `valid` rows repeat its first row (never stored).
+    auto lane_rows = [&](int first, int valid, int n, int (&y)[4]) {
+      const int r0 = __ldg(p.sorted_src + first) / p.K;
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int r = lane + 32 * i;
+        y[i] = (i < n && r < valid) ? __ldg(p.sorted_src + first + r) / p.K : r0;
+      }
+    };
+    int y[4] = {0, 0, 0, 0};
     for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
       const TileInfo ti = tile_info<WGRAD>(p, t);
+      if (!WGRAD && p.gather_any) lane_rows(ti.row0, ti.nvalid, 4, y);
       for (int kb = 0; kb < ti.nk; ++kb) {
-        if (!mbar_wait(empty_bar + stage, phase ^ 1u, abort_flag, kWaitTimeoutNs)) {
-          ok = false;
-          break;
+        int s = 0, kc = 0, kext = 0, row = 0;
+        if (!WGRAD) {
+          rows_kblock(p, kb, s, kc, kext);
+        } else {
+          s = kb / ti.nkb;
+          const int b = kb - s * ti.nkb;
+          row = ti.row0 + b * BK;
+          if (p.sl[s].gather) lane_rows(row, ti.nvalid - b * BK, 2, y);
         }
+        const bool gat = p.sl[s].gather != 0;
+        int w_ok = 1;
         uint64_t* fb = full_bar + stage;
         uint8_t* sa = ring + stage * C::kStageBytes;
         uint8_t* sb = sa + kAStageBytes;
-        mbar_expect_tx(fb, C::kStageBytes);
-        armed[stage] = static_cast<int>(phase);
-        if (!WGRAD) {
-          int s, kc, kext;
-          rows_kblock(p, kb, s, kc, kext);
-          const CUtensorMap* ma = &p.sl[s].a;
-          const CUtensorMap* mb = &p.sl[s].b;
-          tma_load_2d(sa, ma, fb, kc, ti.row0);
-          if (!B_MN) {
-            if (p.b_split) {
-              const int n0 = ti.nt * (BN / 2);
-              tma_load_3d(sb, mb, fb, kc, n0, ti.g);
-              tma_load_3d(sb + (BN / 2) * 128, mb, fb, kc, n0 + p.b_split, ti.g);
-            } else {
-              tma_load_3d(sb, mb, fb, kc, ti.nt * BN, ti.g);
-            }
-          } else {
+        if (lane == 0) {
+          w_ok = mbar_wait(empty_bar + stage, phase ^ 1u, abort_flag, kWaitTimeoutNs);
+          if (w_ok) {
+            mbar_expect_tx(fb, gat ? C::kBStageBytes : C::kStageBytes);
+            armed[stage] = static_cast<int>(phase);
+            if (!WGRAD) {
+              const CUtensorMap* mb = &p.sl[s].b;
+              if (!gat) tma_load_2d(sa, &p.sl[s].a, fb, kc, ti.row0);
+              if (!B_MN) {
+                if (p.b_split) {
+                  const int n0 = ti.nt * (BN / 2);
+                  tma_load_3d(sb, mb, fb, kc, n0, ti.g);
+                  tma_load_3d(sb + (BN / 2) * 128, mb, fb, kc, n0 + p.b_split, ti.g);
+                } else {
+                  tma_load_3d(sb, mb, fb, kc, ti.nt * BN, ti.g);
+                }
+              } else {
 #pragma unroll
-            for (int c = 0; c < BN / 64; ++c)
-              tma_load_3d(sb + c * kChunkBytes, mb, fb, ti.nt * BN + c * 64, kc, ti.g);
+                for (int c = 0; c < BN / 64; ++c)
+                  tma_load_3d(sb + c * kChunkBytes, mb, fb, ti.nt * BN + c * 64, kc, ti.g);
+              }
+            } else {
+              if (!gat) {
+                tma_load_2d(sa, &p.sl[s].a, fb, ti.mt * BM, row);
+                tma_load_2d(sa + kChunkBytes, &p.sl[s].a, fb, ti.mt * BM + 64, row);
+              }
+              tma_load_2d(sb, &p.wb_hi, fb, 0, row);
+              tma_load_2d(sb + kChunkBytes, &p.wb_lo, fb, 0, row);
+            }
           }
-        } else {
-          const int s = kb / ti.nkb;
-          const int row = ti.row0 + (kb - s * ti.nkb) * BK;
-          tma_load_2d(sa, &p.sl[s].a, fb, ti.mt * BM, row);
-          tma_load_2d(sa + kChunkBytes, &p.sl[s].a, fb, ti.mt * BM + 64, row);
-          tma_load_2d(sb, &p.wb_hi, fb, 0, row);
-          tma_load_2d(sb + kChunkBytes, &p.wb_lo, fb, 0, row);
+        }
+        w_ok = __shfl_sync(0xffffffffu, w_ok, 0);  // the stage is free and armed
+        if (!w_ok) {
+          ok = false;
+          break;
+        }
+        if (lanes_arrive) {
+          if (gat) {
+            const GemmSlice& sl = p.sl[s];
+            const uint32_t sa_u = smem_u32(sa);
+            // Each copy instruction moves whole 128-byte row segments: eight
+            // lanes per segment (lane & 7 = its 16-byte piece), so global reads
+            // are coalesced and the swizzled shared-memory writes conflict-free.
+            const int c = lane & 7;
+            if (!WGRAD) {
+              // 128 rows x 64 columns: rows 4*it + lane/8, it < 32
+              const bool in = kc + c * 8 < sl.gcols;
+#pragma unroll
+              for (int it = 0; it < 32; ++it) {
+                const int r = 4 * it + (lane >> 3);
+                const int tok = __shfl_sync(0xffffffffu, y[it >> 3], r & 31);
+                const uint16_t* src = sl.gsrc + static_cast<int64_t>(tok) * sl.gld + kc + c * 8;
+                cp_async16(sa_u + r * 128 + (((c ^ r) & 7) << 4), in ? src : sl.gsrc,
+                           in ? 16u : 0u);
+              }
+            } else {
+              // 64 K rows x two 64-column chunks: 16 lanes per row (256 bytes),
+              // rows 2*it + lane/16, it < 32
+              const int ch = (lane >> 3) & 1;
+              const int col = ti.mt * BM + ch * 64 + c * 8;
+              const bool in = col < sl.gcols;
+#pragma unroll
+              for (int it = 0; it < 32; ++it) {
+                const int r = 2 * it + (lane >> 4);
+                const int tok = __shfl_sync(0xffffffffu, y[it >> 4], r & 31);
+                const uint16_t* src = sl.gsrc + static_cast<int64_t>(tok) * sl.gld + col;
+                cp_async16(sa_u + ch * kChunkBytes + r * 128 + (((c ^ r) & 7) << 4),
+                           in ? src : sl.gsrc, in ? 16u : 0u);
+              }
+            }
+          }
+          cp_async_mbar_arrive_noinc(fb);
         }
         if (++stage == S) {
           stage = 0;
@@ -612,7 +682,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
         }
       }
     }
-    if (!ok) {
+    if (lanes_arrive) cp_async_wait<0>();  // no copy outlives the producer
+    if (!ok && lane == 0) {
       // drain copies still in flight into this CTA's shared memory
       for (int i = 0; i < S; ++i)
         if (armed[i] >= 0) {
@@ -671,6 +742,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
         }
         if (lane == 0) {
           tc_fence_after();
+          if (p.gather_any) fence_proxy_async_smem();  // LSU-copied A rows -> async proxy
           int nk16 = 4;
           if (!WGRAD) {
             int s, kc, kext;

@@ -75,12 +75,17 @@ struct GemmSlice {
   CUtensorMap a;
   CUtensorMap b;
   int K;
+  int gather;                // 1: A rows are token rows gathered by sorted_src[p] / K
+  const uint16_t* gsrc;      // gathered A: token-row matrix [T, gcols] bf16
+  int64_t gld;               //             its leading dimension (elements)
+  int gcols;                 //             its columns (K for rows mode, M for wgrad)
 };
 
 struct GemmParams {
   GemmSlice sl[kMaxSlices];  // rows mode: A/B per slice; wgrad: A sources (hi, lo)
   CUtensorMap wb_hi, wb_lo;  // wgrad: B operand hi / lo (columns [0,64) / [64,128))
   int nslices;
+  int gather_any;     // some slice gathers its A rows
   int N;              // valid output columns (rows mode) / LoRA rank r (wgrad)
   int M;              // wgrad: rows of the weight gradient (d, f or 2f)
   int n_ntiles;       // N tiles per M tile (rows mode) / M tiles per group (wgrad)

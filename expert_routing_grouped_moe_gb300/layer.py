@@ -2,10 +2,14 @@
 
 ``MoELoRALayer`` is a convenience wrapper over the library's calls for one
 layer shape: it allocates every buffer once (torch device memory), then
-``forward`` runs route -> permute -> grouped split-LoRA SwiGLU MLP ->
-combine and ``backward`` runs the dY permute -> grouped backward -> combine
-of dX and of the routing-weight gradient.  All arithmetic happens in the CUDA
-library; this module only sequences calls and owns memory.
+``forward`` runs route -> grouped split-LoRA SwiGLU MLP -> combine and
+``backward`` runs the grouped backward -> combine of dX and of the
+routing-weight gradient.  With ``gather=False`` (default) the token rows are
+first permuted into Xp / dYp by moe_permute and the GEMMs read them with TMA;
+with ``gather=True`` the GEMMs copy token rows straight from X and dY
+(sorted_src picks them), which saves the two [N, d] permuted buffers but is
+slower on GB300.  All arithmetic happens in the CUDA library; this module
+only sequences calls and owns memory.
 """
 from __future__ import annotations
 
@@ -13,17 +17,18 @@ import torch
 
 from . import _lib as L
 
-# Kernel launches issued by one forward / one backward (every call below
-# launches a fixed number of kernels: route 3, permute 1, forward GEMMs 4,
-# combine 1; backward: permute 1, GEMMs 4 + weight-gradient GEMMs 4,
-# partial-sum 1, combine 1).
+# Kernel launches issued by one forward / one backward in the default
+# (permuted) mode: route 3, permute 1, forward GEMMs 4, combine 1; backward:
+# permute 1, GEMMs 4 + weight-gradient GEMMs 4, partial-sum 1, combine 1.
+# The gather mode issues no permute.
 LAUNCHES_FWD = 9
 LAUNCHES_BWD = 11
 
 
 class MoELoRALayer:
     def __init__(self, T, d, f, E, k, r, alpha, weights: dict, shared_expert=False,
-                 device="cuda"):
+                 device="cuda", gather=False):
+        self.gather = bool(gather)
         self.dims = L.make_dims(T, d, f, E, k, r, alpha / r, shared_expert)
         self.T, self.d, self.f, self.E, self.k, self.r = T, d, f, E, k, r
         self.shared = bool(shared_expert)
@@ -44,7 +49,7 @@ class MoELoRALayer:
         self.dest_pos = torch.zeros(self.N, **i32)
         self.route_ws = torch.empty(max(16, L.moe_route_workspace_size(T, self.K, G)),
                                     dtype=torch.uint8, device=dev)
-        self.Xp = torch.empty(P, d, **bf)
+        self.Xp = None if self.gather else torch.empty(P, d, **bf)
         self.Yp = torch.empty(P, d, **bf)
         # saved intermediates: h in fp32; act / xa_gu / xa_dn as hi+lo bf16 pairs
         self.h = torch.empty(P, 32 * ((f + 15) // 16), **f32)  # [gate 16 | up 16] chunks
@@ -52,7 +57,7 @@ class MoELoRALayer:
         self.xa_gu = torch.empty(2, P, r, **bf)
         self.xa_dn = torch.empty(2, P, r, **bf)
         self.Y = torch.empty(T, d, **bf)
-        self.dYp = torch.empty(P, d, **bf)
+        self.dYp = None if self.gather else torch.empty(P, d, **bf)
         self.dXp = torch.empty(P, d, **bf)
         self.dw_rows = torch.empty(P, **f32)
         self.dX = torch.empty(T, d, **bf)
@@ -66,6 +71,10 @@ class MoELoRALayer:
         self._ids = None
         self._topk_w = None
 
+    def launches_per_step(self):
+        """Kernel launches of one forward + backward in this layer's mode."""
+        return LAUNCHES_FWD + LAUNCHES_BWD - (2 if self.gather else 0)
+
     # ------------------------------------------------------------------ steps
     def route(self, ids, stream=None):
         L.moe_route(ids, self.E, self.shared, self.counts, self.offsets, self.tile_off,
@@ -73,11 +82,13 @@ class MoELoRALayer:
 
     def forward(self, X, ids, topk_w, stream=None):
         """Y [T,d] bf16 for token rows X [T,d], top-k ids [T,k], weights [T,k]."""
-        self._ids, self._topk_w = ids, topk_w
+        self._ids, self._topk_w, self._X = ids, topk_w, X
         self.route(ids, stream)
-        L.moe_permute(X, self.K, self.dest_pos, self.Xp, stream)
+        if not self.gather:
+            L.moe_permute(X, self.K, self.dest_pos, self.Xp, stream)
         w = self.w
-        L.moe_lora_grouped_mlp_fwd(self.dims, self.Xp, self.counts, self.offsets, self.tile_off,
+        L.moe_lora_grouped_mlp_fwd(self.dims, self.Xp, None if self.Xp is not None else X,
+                                   self.counts, self.offsets, self.tile_off,
                                    self.sorted_src, topk_w, w["W_gu"], w["A_gu"], w["B_gu"],
                                    w["W_dn"], w["A_dn"], w["B_dn"], self.Yp, self.h, self.act,
                                    self.xa_gu, self.xa_dn, stream)
@@ -89,9 +100,12 @@ class MoELoRALayer:
         """dX [T,d] bf16, dw [T,k] fp32 and the four fp32 LoRA gradients."""
         if self._ids is None:
             raise RuntimeError("backward before forward")
-        L.moe_permute(dY, self.K, self.dest_pos, self.dYp, stream)
+        if not self.gather:
+            L.moe_permute(dY, self.K, self.dest_pos, self.dYp, stream)
         w, g = self.w, self.grads
-        L.moe_lora_grouped_mlp_bwd(self.dims, self.dYp, self.Xp, self.counts, self.offsets,
+        L.moe_lora_grouped_mlp_bwd(self.dims, self.dYp, None if self.dYp is not None else dY,
+                                   self.Xp, None if self.Xp is not None else self._X,
+                                   self.counts, self.offsets,
                                    self.tile_off, self.sorted_src, self._topk_w, w["W_gu"],
                                    w["A_gu"], w["B_gu"], w["W_dn"], w["A_dn"], w["B_dn"], self.h,
                                    self.act, self.xa_gu, self.xa_dn, self.dXp, self.dw_rows,

@@ -197,7 +197,13 @@ MOE_API int moe_unpermute_combine(const moe_bf16* rows, const int32_t* dest_pos,
  * The tensor cores consume a pair as two bf16 operands (extra K steps).
  * Here P = N = T * K (permuted rows). */
 
-/* Forward.  Inputs: Xp (moe_permute of X), the routing outputs (counts is
+/* Forward.  Row input: either Xp = moe_permute(X) [P,d], or X itself [T,d]
+ * with Xp = NULL, in which case the GEMMs gather each permuted row's token row
+ * straight from X while loading it (16-byte cp.async copies picked by
+ * sorted_src; no permuted copy is made).  The permuted input is the faster
+ * of the two on GB300 (its tiles load with TMA); the gathered one needs no
+ * [P,d] buffer.
+ * Other inputs: the routing outputs (counts is
  * not read; offsets and tile_off define the tiles, sorted_src locates each
  * row's routing weight), topk weights [T,k] fp32, the six weight tensors.  Outputs:
  *   Yp    [P,d]    bf16  w-scaled expert outputs (feed moe_unpermute_combine
@@ -210,7 +216,7 @@ MOE_API int moe_unpermute_combine(const moe_bf16* rows, const int32_t* dest_pos,
  *   xa_dn [2,P,r]  bf16 pair  saved s * act A_dn^T
  * The down projection consumes act's high half (Yp is a bf16 output). */
 MOE_API int moe_lora_grouped_mlp_fwd(const moe_dims* dims, const moe_bf16* Xp,
-                             const int32_t* counts, const int32_t* offsets,
+                             const moe_bf16* X, const int32_t* counts, const int32_t* offsets,
                              const int32_t* tile_off, const int32_t* sorted_src,
                              const float* topk_w,
                              const moe_bf16* W_gu, const moe_bf16* A_gu, const moe_bf16* B_gu,
@@ -221,9 +227,10 @@ MOE_API int moe_lora_grouped_mlp_fwd(const moe_dims* dims, const moe_bf16* Xp,
 /* Bytes of scratch moe_lora_grouped_mlp_bwd needs. */
 MOE_API size_t moe_mlp_bwd_workspace_size(const moe_dims* dims);
 
-/* Backward for frozen W (and frozen router).  dYp = moe_permute of the
- * upstream gradient dY (unscaled); Xp, h, act, xa_gu, xa_dn as saved by the
- * forward.  With dO = w_p dYp:
+/* Backward for frozen W (and frozen router).  Row inputs as in the forward:
+ * dYp = moe_permute of the upstream gradient dY (unscaled) or dY itself [T,d]
+ * with dYp = NULL (gathered), and Xp or X likewise; h, act, xa_gu, xa_dn as
+ * saved by the forward.  With dO = w_p dYp:
  *   dw_rows[p] = <dYp_p, o_p> = <act_p, g_p>  [P] fp32, the gradient of the
  *                routing weight of row p (moe_unpermute_combine gathers it
  *                to [T,k] through row_scalars / slot_out)
@@ -241,7 +248,8 @@ MOE_API size_t moe_mlp_bwd_workspace_size(const moe_dims* dims);
  * their inputs exist and joins back before the call returns, so all results
  * are ordered on `stream` as if everything ran there.  Calls from several host
  * threads serialise their enqueueing on that stream. */
-MOE_API int moe_lora_grouped_mlp_bwd(const moe_dims* dims, const moe_bf16* dYp, const moe_bf16* Xp,
+MOE_API int moe_lora_grouped_mlp_bwd(const moe_dims* dims, const moe_bf16* dYp,
+                             const moe_bf16* dY, const moe_bf16* Xp, const moe_bf16* X,
                              const int32_t* counts, const int32_t* offsets,
                              const int32_t* tile_off, const int32_t* sorted_src,
                              const float* topk_w,

@@ -40,9 +40,9 @@ def make_inputs(cfg, seed, ids=None, w=None):
     return wts, act, ids_np, w_np
 
 
-def run(cfg, wts, act, ids_np, w_np):
+def run(cfg, wts, act, ids_np, w_np, gather=False):
     layer = MoELoRALayer(cfg.T, cfg.d, cfg.f, cfg.E, cfg.k, cfg.r, cfg.alpha, wts,
-                         shared_expert=cfg.shared, device=DEV)
+                         shared_expert=cfg.shared, device=DEV, gather=gather)
     ids = torch.from_numpy(np.ascontiguousarray(ids_np, dtype=np.int32)).to(DEV)
     w = torch.from_numpy(np.ascontiguousarray(w_np, dtype=np.float32)).to(DEV)
     Y = layer.forward(act["X"], ids, w).clone()
@@ -66,18 +66,21 @@ def group_rows(ids_np, cfg):
     return out, T * K
 
 
+@pytest.mark.parametrize("gather", [True, False])
 @pytest.mark.parametrize("name", list(SMALL))
-def test_layer_full_parity(name):
+def test_layer_full_parity(name, gather):
+    """gather=True: GEMMs gather token rows from X / dY; False: permuted copies."""
     cfg = SMALL[name]
     wts, act, ids_np, w_np = make_inputs(cfg, seed=7)
-    layer, Y, g = run(cfg, wts, act, ids_np, w_np)
+    layer, Y, g = run(cfg, wts, act, ids_np, w_np, gather=gather)
     P = oracle_params(wts, cfg)
     X, dY = to64(act["X"]), to64(act["dY"])
     s = cfg.scale
     wfull = np.concatenate([w_np, np.ones((cfg.T, 1))], 1) if cfg.shared else w_np
     groups, N = group_rows(ids_np, cfg)
     # forward intermediates, group by group, in the permuted layout
-    bufs = {n: to64(getattr(layer, n)) for n in ("Xp", "xa_gu", "act", "xa_dn", "Yp")}
+    names = ("xa_gu", "act", "xa_dn", "Yp") + (() if gather else ("Xp",))
+    bufs = {n: to64(getattr(layer, n)) for n in names}
     bufs["h"] = to64(layer.h_gate_up())
     for n in ("xa_gu", "act", "xa_dn"):  # hi + lo pairs carry ~16 significant bits
         bufs[n] = bufs[n][0] + bufs[n][1]
@@ -86,7 +89,8 @@ def test_layer_full_parity(name):
             continue
         fw = oracle.expert_forward(X[tok], P, gi)
         wt = wfull.reshape(-1)[flat]
-        np.testing.assert_array_equal(bufs["Xp"][prow], X[tok])
+        if not gather:
+            np.testing.assert_array_equal(bufs["Xp"][prow], X[tok])
         # fp32 accumulation of exact bf16 products: far inside the bf16 bounds
         tight = dict(rel_fro=1e-4, elem=1e-4)
         assert_close_bf16(bufs["xa_gu"][prow], s * fw["xa"], "xa_gu g%d" % gi, **tight)
@@ -126,14 +130,15 @@ EDGE = {
 }
 
 
+@pytest.mark.parametrize("gather", [False, True])
 @pytest.mark.parametrize("name", list(EDGE))
-def test_layer_edge_cases(name):
+def test_layer_edge_cases(name, gather):
     cfg, mk = EDGE[name]
     rng = np.random.default_rng(5)
     ids_np = mk(cfg.T, cfg.E, cfg.k, rng).astype(np.int32)
     w_np = synth.combine_weights(cfg.T, cfg.k, seed=9).numpy()
     wts, act, ids_np, w_np = make_inputs(cfg, seed=13, ids=ids_np, w=w_np)
-    layer, Y, g = run(cfg, wts, act, ids_np, w_np)
+    layer, Y, g = run(cfg, wts, act, ids_np, w_np, gather=gather)
     P = oracle_params(wts, cfg)
     X, dY = to64(act["X"]), to64(act["dY"])
     assert_close_bf16(to64(Y), oracle.layer_forward(X, ids_np, w_np, P), "Y")
@@ -146,11 +151,12 @@ def test_layer_edge_cases(name):
         assert np.all(g[n].cpu().numpy()[empty] == 0), n
 
 
-@pytest.mark.parametrize("name", ["qwen3_30b_a3b", "gpt_oss_20b", "skewed_shared"])
-def test_layer_full_size_sampled(name):
+@pytest.mark.parametrize("name,gather", [("qwen3_30b_a3b", False), ("qwen3_30b_a3b", True),
+                                         ("gpt_oss_20b", False), ("skewed_shared", False)])
+def test_layer_full_size_sampled(name, gather):
     cfg = synth.CONFIGS[name]
     wts, act, ids_np, w_np = make_inputs(cfg, seed=1)
-    layer, Y, g = run(cfg, wts, act, ids_np, w_np)
+    layer, Y, g = run(cfg, wts, act, ids_np, w_np, gather=gather)
     rng = np.random.default_rng(3)
     toks = sorted(rng.choice(cfg.T, size=4, replace=False).tolist() + [0, cfg.T - 1])
     counts = np.bincount(ids_np.reshape(-1), minlength=cfg.E)

@@ -65,20 +65,25 @@ def test_fwd_argument_errors_before_launch(lib):
     P = ctypes.c_void_p
     fake = P(1 << 20)  # never dereferenced: checks fail first
     d = _dims(k=9)
-    rc = lib.moe_lora_grouped_mlp_fwd(ctypes.byref(d), *([fake] * 17), None)
+    rc = lib.moe_lora_grouped_mlp_fwd(ctypes.byref(d), None, *([fake] * 17), None)
     assert rc == _lib.MOE_ERR_INVALID_ARG
     assert b"k=9" in lib.moe_last_error()
     d = _dims()
-    args = [fake] * 17
-    args[0] = None  # Xp
-    rc = lib.moe_lora_grouped_mlp_fwd(ctypes.byref(d), *args, None)
-    assert rc == _lib.MOE_ERR_INVALID_ARG
-    assert b"Xp" in lib.moe_last_error()
-    args = [fake] * 17
-    args[12] = P((1 << 20) + 4)  # Yp misaligned
+    # exactly one of Xp (permuted rows) and X (token rows)
+    for xp, x in ((None, None), (fake, fake)):
+        rc = lib.moe_lora_grouped_mlp_fwd(ctypes.byref(d), xp, x, *([fake] * 16), None)
+        assert rc == _lib.MOE_ERR_INVALID_ARG
+        assert b"exactly one of Xp" in lib.moe_last_error()
+    args = [None] + [fake] * 17
+    args[14] = P((1 << 20) + 4)  # Yp misaligned
     rc = lib.moe_lora_grouped_mlp_fwd(ctypes.byref(d), *args, None)
     assert rc == _lib.MOE_ERR_INVALID_ARG
     assert b"aligned" in lib.moe_last_error()
+    args = [None] + [fake] * 17
+    args[7] = None  # W_gu
+    rc = lib.moe_lora_grouped_mlp_fwd(ctypes.byref(d), *args, None)
+    assert rc == _lib.MOE_ERR_INVALID_ARG
+    assert b"W_gu" in lib.moe_last_error()
 
 
 def test_route_argument_errors_before_launch(lib):
