@@ -17,7 +17,7 @@
 //                  match (warp multisplit); position = offsets[g] + earlier
 //                  CTAs (scanned histogram) + earlier warps + rank.  The chunk
 //                  is sorted in shared memory first, so sorted_src leaves the
-//                  CTA as contiguous per-expert runs.
+//                  CTA as one contiguous run per expert, written by one warp.
 //
 // The walk order (CTA, then warp, then iteration, then lane) is ascending flat
 // index, so equal ids keep ascending flat index: the sort is stable and the
@@ -39,21 +39,26 @@ __device__ __forceinline__ unsigned lanemask_lt() {
   return m;
 }
 
-// Lanes of the warp holding the same value v (0 <= v < 2^nbits): one ballot
-// per bit, keeping the lanes that agree on every bit (warp multisplit).
-__device__ __forceinline__ unsigned warp_match(unsigned v, int nbits) {
+// Lanes of the warp holding the same value v (0 <= v < 2^NB): one ballot per
+// bit, keeping the lanes that agree on every bit (warp multisplit).  Bits
+// above the values' width are zero in every lane and cost one no-op ballot.
+template <int NB>
+__device__ __forceinline__ unsigned warp_match(unsigned v) {
   unsigned m = kFull;
-  for (int b = 0; b < nbits; ++b) {
+#pragma unroll
+  for (int b = 0; b < NB; ++b) {
     const unsigned bit = (v >> b) & 1u;
     const unsigned bal = __ballot_sync(kFull, bit);
-    m &= bit ? bal : ~bal;
+    m &= ~(bal ^ (0u - bit));  // lanes whose bit b equals this lane's
   }
   return m;
 }
 
-__device__ __forceinline__ int bits_for(int n) {  // bits to encode 0..n-1
-  return 32 - __clz(n > 1 ? n - 1 : 1);
-}
+// Bits of the group ids the scatter kernel matches on (groups 0..G-1).
+inline int match_bits(int G) { return G <= 64 ? 6 : G <= 128 ? 7 : G <= 256 ? 8 : 11; }
+
+// Expert id as loaded -> routed group (>= 0), -2 for an id outside [0,E).
+__device__ __forceinline__ int classify(int e, int E) { return (e >= 0 && e < E) ? e : -2; }
 
 // Exclusive block-wide prefix sum of one int per thread; *total gets the sum.
 __device__ int block_excl_scan(int v, int* total) {
@@ -102,23 +107,54 @@ __device__ __forceinline__ int flat_id(const int32_t* __restrict__ ids, int i, i
   return (e >= 0 && e < E) ? e : -2;
 }
 
+// Expert ids of this lane's PER assignments of its warp's run [base, base +
+// 32*PER): ev[it] is flat index base + it*32 + lane (-1 past N, -2 bad id).
+// Without a shared expert and with 16-byte aligned ids the lane loads them as
+// int4 vectors, all in flight at once: ids of flat index base + (v*32 +
+// lane)*4 + c, so ev[] is then in a different order (the counts do not care).
+template <int PER, bool SHARED>
+__device__ __forceinline__ void load_ids_any_order(const int32_t* __restrict__ ids, int base,
+                                                   int lane, int N, int k, int K, int E,
+                                                   bool vec, int (&ev)[PER]) {
+  if (!SHARED && vec) {
+#pragma unroll
+    for (int v = 0; v < PER / 4; ++v) {
+      const int i0 = base + (v * 32 + lane) * 4;
+      if (i0 + 3 < N) {
+        const int4 q = __ldg(reinterpret_cast<const int4*>(ids + i0));
+        ev[4 * v + 0] = classify(q.x, E);
+        ev[4 * v + 1] = classify(q.y, E);
+        ev[4 * v + 2] = classify(q.z, E);
+        ev[4 * v + 3] = classify(q.w, E);
+      } else {
+#pragma unroll
+        for (int c = 0; c < 4; ++c)
+          ev[4 * v + c] = i0 + c < N ? classify(__ldg(ids + i0 + c), E) : -1;
+      }
+    }
+  } else {
+#pragma unroll
+    for (int it = 0; it < PER; ++it) ev[it] = flat_id<SHARED>(ids, base + it * 32 + lane, N, k, K, E);
+  }
+}
+
 template <int PER, bool SHARED>
 __global__ void __launch_bounds__(kRouteThreads) route_hist_kernel(
-    const int32_t* __restrict__ ids, int N, int k, int K, int E, int G, int C,
+    const int32_t* __restrict__ ids, int N, int k, int K, int E, int G, int C, int vec,
     int32_t* __restrict__ hist, int* __restrict__ status) {
   extern __shared__ int cnt[];  // [kRouteWarps][G]
   for (int x = threadIdx.x; x < kRouteWarps * G; x += blockDim.x) cnt[x] = 0;
-  __syncthreads();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int base = blockIdx.x * (kRouteThreads * PER) + warp * (32 * PER);
+  int ev[PER];
+  load_ids_any_order<PER, SHARED>(ids, base, lane, N, k, K, E, vec != 0, ev);
+  __syncthreads();
   int* my = cnt + warp * G;
   bool bad = false;
-#pragma unroll 4
+#pragma unroll
   for (int it = 0; it < PER; ++it) {
-    const int i = base + it * 32 + lane;
-    const int e = flat_id<SHARED>(ids, i, N, k, K, E);
-    bad |= (e == -2);
-    if (e >= 0) atomicAdd(my + e, 1);
+    bad |= (ev[it] == -2);
+    if (ev[it] >= 0) atomicAdd(my + ev[it], 1);
   }
   if (bad) atomicCAS(status, 0, kErrBadIds);
   __syncthreads();
@@ -150,12 +186,12 @@ __global__ void __launch_bounds__(1024) route_scan_kernel(int32_t* __restrict__ 
 
 // Shared memory of the scatter kernel, in ints.
 __host__ __device__ constexpr int scatter_smem_ints(int G, int chunk) {
-  return (G + 1) /*off*/ + kRouteWarps * G /*cnt*/ + (G + 1) /*lbase*/ + G /*gbase*/ +
-         2 * chunk /*flat index, global position*/;
+  return (G + 1) /*off*/ + kRouteWarps * G /*cnt*/ + (G + 1) /*lbase*/ + G /*delta*/ +
+         chunk /*flat index at each chunk-local sorted position*/;
 }
 
-template <int PER, bool SHARED>
-__global__ void __launch_bounds__(kRouteThreads) route_scatter_kernel(
+template <int PER, bool SHARED, int NB>
+__global__ void __launch_bounds__(kRouteThreads, 4) route_scatter_kernel(
     const int32_t* __restrict__ ids, int N, int k, int K, int E, int G, int C,
     const int32_t* __restrict__ hist, const int32_t* __restrict__ counts,
     int32_t* __restrict__ offsets, int32_t* __restrict__ tile_off,
@@ -165,10 +201,15 @@ __global__ void __launch_bounds__(kRouteThreads) route_scatter_kernel(
   int* off = sm;                      // [G+1] global offsets
   int* cnt = off + (G + 1);           // [8][G] per-warp counts -> per-warp local starts
   int* lbase = cnt + kRouteWarps * G;  // [G+1] start of group g inside this CTA's chunk
-  int* gbase = lbase + (G + 1);       // [G]   global start of this CTA's run of group g
-  int* stage = gbase + G;             // [CH]  flat index at each chunk-local sorted position
-  int* stage_dst = stage + CH;        // [CH]  its global sorted position
+  int* delta = lbase + (G + 1);       // [G]   global position - chunk-local position, group g
+  int* stage = delta + G;             // [CH]  flat index at each chunk-local sorted position
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  // this warp's ids, in walk order (all loads in flight before the scans)
+  const int base = blockIdx.x * CH + warp * (32 * PER);
+  int ev[PER];
+#pragma unroll
+  for (int it = 0; it < PER; ++it) ev[it] = flat_id<SHARED>(ids, base + it * 32 + lane, N, k, K, E);
 
   // offsets (and tile offsets) = exclusive scans of counts, by warp 0
   if (warp == 0) {
@@ -213,15 +254,14 @@ __global__ void __launch_bounds__(kRouteThreads) route_scatter_kernel(
   __syncthreads();
 
   // pass 1: per-warp counts of this warp's contiguous run of assignments
-  const int base = blockIdx.x * CH + warp * (32 * PER);
   int* my = cnt + warp * G;
-  int ev[PER];
+  bool valid = true;
 #pragma unroll
   for (int it = 0; it < PER; ++it) {
-    const int i = base + it * 32 + lane;
-    ev[it] = flat_id<SHARED>(ids, i, N, k, K, E);
+    valid &= ev[it] >= 0;
     if (ev[it] >= 0) atomicAdd(my + ev[it], 1);
   }
+  const bool all_valid = __all_sync(kFull, valid);
   __syncthreads();
 
   // chunk-local group starts (scan over g), per-warp starts, global run starts
@@ -236,7 +276,7 @@ __global__ void __launch_bounds__(kRouteThreads) route_scatter_kernel(
     int run = block_excl_scan(s, &total);
     for (int g = lo; g < hi; ++g) {
       lbase[g] = run;
-      gbase[g] = off[g] + __ldg(hist + static_cast<int64_t>(g) * C + blockIdx.x);
+      delta[g] = off[g] + __ldg(hist + static_cast<int64_t>(g) * C + blockIdx.x) - run;
 #pragma unroll
       for (int w = 0; w < kRouteWarps; ++w) {
         const int c = cnt[w * G + g];
@@ -250,32 +290,50 @@ __global__ void __launch_bounds__(kRouteThreads) route_scatter_kernel(
 
   // pass 2: stable chunk-local position; dest_pos straight to global memory
   const unsigned lt = lanemask_lt();
-  const int nbits = bits_for(G);
+  int32_t* dp = dest_pos + base + lane;  // dest_pos of element it: dp[it * 32]
+  if (all_valid) {
+    // every element of this warp's run exists and has a valid id
 #pragma unroll
-  for (int it = 0; it < PER; ++it) {
-    const int i = base + it * 32 + lane;
-    const int e = ev[it];
-    // lanes holding the same valid id (invalid lanes match nothing)
-    const unsigned m = __ballot_sync(kFull, e >= 0) &
-                       warp_match(static_cast<unsigned>(e >= 0 ? e : 0), nbits);
-    if (e >= 0) {
+    for (int it = 0; it < PER; ++it) {
+      const int e = ev[it];
+      const unsigned m = warp_match<NB>(static_cast<unsigned>(e));
       const int lp = my[e] + __popc(m & lt);
-      const int dst = gbase[e] + (lp - lbase[e]);
-      stage[lp] = i;
-      stage_dst[lp] = dst;
-      dest_pos[i] = dst;
-    } else if (i < N) {
-      dest_pos[i] = -1;
+      stage[lp] = base + it * 32 + lane;
+      dp[it * 32] = delta[e] + lp;
+      __syncwarp();
+      if ((m >> lane) == 1u) my[e] = lp + 1;  // the last matching lane
+      __syncwarp();
     }
-    __syncwarp();
-    if (e >= 0 && lane == __ffs(m) - 1) my[e] += __popc(m);
-    __syncwarp();
+  } else {
+#pragma unroll
+    for (int it = 0; it < PER; ++it) {
+      const int i = base + it * 32 + lane;
+      const int e = ev[it];
+      // lanes holding the same valid id (invalid lanes match nothing)
+      const unsigned m = __ballot_sync(kFull, e >= 0) &
+                         warp_match<NB>(static_cast<unsigned>(e >= 0 ? e : 0));
+      int lp = 0;
+      if (e >= 0) {
+        lp = my[e] + __popc(m & lt);
+        stage[lp] = i;
+        dp[it * 32] = delta[e] + lp;
+      } else if (i < N) {
+        dp[it * 32] = -1;
+      }
+      __syncwarp();
+      if (e >= 0 && (m >> lane) == 1u) my[e] = lp + 1;
+      __syncwarp();
+    }
   }
   __syncthreads();
 
-  // sorted_src as contiguous per-group runs (consecutive threads, consecutive addresses)
-  const int n_local = lbase[G];
-  for (int lp = threadIdx.x; lp < n_local; lp += blockDim.x) sorted_src[stage_dst[lp]] = stage[lp];
+  // sorted_src: group g's run of this chunk is contiguous both in the stage
+  // and in global memory; one warp copies it
+  for (int g = warp; g < G; g += kRouteWarps) {
+    const int lo = lbase[g], n = lbase[g + 1] - lo;
+    int32_t* dst = sorted_src + (delta[g] + lo);
+    for (int x = lane; x < n; x += 32) dst[x] = stage[lo + x];
+  }
   // sorted positions past the valid total (only when some ids were bad)
   for (int p = off[G] + blockIdx.x * blockDim.x + threadIdx.x; p < N;
        p += gridDim.x * blockDim.x)
@@ -354,23 +412,45 @@ cudaError_t launch_router_topk(const float* logits, int T, int E, int k, int32_t
   return cudaGetLastError();
 }
 
-template <int PER, bool SHARED>
+template <int PER, bool SHARED, int NB>
 cudaError_t launch_route_per(const int32_t* ids, int N, int k, int K, int E, int G, int C,
                              int32_t* counts, int32_t* offsets, int32_t* tile_off,
                              int32_t* sorted_src, int32_t* dest_pos, int32_t* hist, int* status,
                              cudaStream_t s) {
   const size_t sm_hist = static_cast<size_t>(kRouteWarps) * G * sizeof(int);
   const size_t sm_scat = static_cast<size_t>(scatter_smem_ints(G, kRouteThreads * PER)) * 4;
-  cudaError_t e = cudaFuncSetAttribute(route_scatter_kernel<PER, SHARED>,
+  cudaError_t e = cudaFuncSetAttribute(route_scatter_kernel<PER, SHARED, NB>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(sm_scat));
   if (e != cudaSuccess) return e;
-  route_hist_kernel<PER, SHARED><<<C, kRouteThreads, sm_hist, s>>>(ids, N, k, K, E, G, C, hist,
-                                                                   status);
+  const int vec = (reinterpret_cast<uintptr_t>(ids) & 15u) == 0 ? 1 : 0;
+  route_hist_kernel<PER, SHARED><<<C, kRouteThreads, sm_hist, s>>>(ids, N, k, K, E, G, C, vec,
+                                                                   hist, status);
   route_scan_kernel<<<G, 1024, 0, s>>>(hist, C, counts);
-  route_scatter_kernel<PER, SHARED><<<C, kRouteThreads, sm_scat, s>>>(
+  route_scatter_kernel<PER, SHARED, NB><<<C, kRouteThreads, sm_scat, s>>>(
       ids, N, k, K, E, G, C, hist, counts, offsets, tile_off, sorted_src, dest_pos);
   return cudaGetLastError();
+}
+
+template <int PER, bool SHARED>
+cudaError_t launch_route_nb(const int32_t* ids, int N, int k, int K, int E, int G, int C,
+                            int32_t* counts, int32_t* offsets, int32_t* tile_off,
+                            int32_t* sorted_src, int32_t* dest_pos, int32_t* hist, int* status,
+                            cudaStream_t s) {
+  switch (match_bits(G)) {
+    case 6:
+      return launch_route_per<PER, SHARED, 6>(ids, N, k, K, E, G, C, counts, offsets, tile_off,
+                                              sorted_src, dest_pos, hist, status, s);
+    case 7:
+      return launch_route_per<PER, SHARED, 7>(ids, N, k, K, E, G, C, counts, offsets, tile_off,
+                                              sorted_src, dest_pos, hist, status, s);
+    case 8:
+      return launch_route_per<PER, SHARED, 8>(ids, N, k, K, E, G, C, counts, offsets, tile_off,
+                                              sorted_src, dest_pos, hist, status, s);
+    default:
+      return launch_route_per<PER, SHARED, 11>(ids, N, k, K, E, G, C, counts, offsets,
+                                               tile_off, sorted_src, dest_pos, hist, status, s);
+  }
 }
 
 cudaError_t launch_route(const int32_t* ids, int T, int k, int E, int shared, int32_t* counts,
@@ -381,17 +461,17 @@ cudaError_t launch_route(const int32_t* ids, int T, int k, int E, int shared, in
   const int C = route_ctas(N > 0 ? N : 1);
 #define MOE_ROUTE_CASE(P)                                                                  \
   case P:                                                                                  \
-    return shared ? launch_route_per<P, true>(ids, N, k, K, E, G, C, counts, offsets,     \
+    return shared ? launch_route_nb<P, true>(ids, N, k, K, E, G, C, counts, offsets,     \
                                               tile_off, sorted_src, dest_pos, hist, status, s) \
-                  : launch_route_per<P, false>(ids, N, k, K, E, G, C, counts, offsets,    \
+                  : launch_route_nb<P, false>(ids, N, k, K, E, G, C, counts, offsets,    \
                                                tile_off, sorted_src, dest_pos, hist, status, s);
   switch (route_per_lane(N)) {
     MOE_ROUTE_CASE(16)
     MOE_ROUTE_CASE(8)
     default:
-      return shared ? launch_route_per<4, true>(ids, N, k, K, E, G, C, counts, offsets, tile_off,
+      return shared ? launch_route_nb<4, true>(ids, N, k, K, E, G, C, counts, offsets, tile_off,
                                                 sorted_src, dest_pos, hist, status, s)
-                    : launch_route_per<4, false>(ids, N, k, K, E, G, C, counts, offsets,
+                    : launch_route_nb<4, false>(ids, N, k, K, E, G, C, counts, offsets,
                                                  tile_off, sorted_src, dest_pos, hist, status, s);
   }
 #undef MOE_ROUTE_CASE

@@ -24,8 +24,21 @@ def test_layer_counts_qwen3_shape():
     F_lora = 2 * N * (2048 * 64 + 64 * 1536 + 768 * 64 + 64 * 2048)
     assert c["flops"] == 2 * F_base + 3 * F_lora
     assert abs(c["flops"] / 1e9 - 699.1) < 1.0   # ~699 GFLOP per fwd+bwd step
-    assert c["kernels"]["gate_up"] == ("tensor", 2 * N * 2048 * 1536 + 2 * N * 64 * 1536)
-    assert c["kernels"]["route"][0] == "hbm"
+    fl, nb = c["kernels"]["gate_up"]
+    assert fl == 2 * N * 2048 * 1536 + 2 * N * 64 * 1536
+    # W_gu (128 experts x 1536 x 2048 bf16) alone is 805 MB of the gate_up bytes
+    assert nb > 128 * 1536 * 2048 * 2
+    assert c["kernels"]["route"][0] == 0 and c["kernels"]["route"][1] > 0
+
+
+def test_kernel_roofline_picks_the_longer_bound():
+    peaks = {"bf16_tflops_sustained": 1000.0, "hbm_gbs": 5000.0}
+    # 1 TFLOP and 1 GB: tensor time 1 ms > HBM time 0.2 ms -> tensor-bound
+    r = bench.kernel_roofline("k", 1e12, 1e9, 2e-3, peaks)
+    assert r["bound"] == "tensor" and abs(r["frac"] - 0.5) < 1e-12
+    # 1 GFLOP and 10 GB: HBM time 2 ms -> HBM-bound, achieved 10 GB / 4 ms
+    r = bench.kernel_roofline("k", 1e9, 1e10, 4e-3, peaks)
+    assert r["bound"] == "hbm" and r["unit"] == "GB/s" and abs(r["achieved"] - 2500.0) < 1e-9
 
 
 def test_layer_counts_shared_rows():
