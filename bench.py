@@ -431,13 +431,6 @@ def run_ours(args):
 
     counts = layer_counts(cfg)
     names = L.kernel_names()
-    probe_steps = min(args.steps, args.probe_steps)
-    probes = {}
-    for n in names:
-        if n in ("router_topk",):
-            continue
-        per = counts["launches"].get(n, 1)
-        probes[n] = L.KernelProbe(n, per * probe_steps)
 
     sampler = ClockSampler(gpu_uuid(torch, dev))
     sampler.start()
@@ -458,6 +451,20 @@ def run_ours(args):
     if L.moe_status() != L.MOE_OK:
         raise SystemExit("device status error in the timed region")
 
+    # per-kernel device times: a separate pass of the same step loop right
+    # after the timed region (the probe's events between launches would stop
+    # each kernel from overlapping its set-up with the previous one, so the
+    # timed steps above carry no probes)
+    probe_steps = min(args.steps, args.probe_steps)
+    probes = {}
+    for n in names:
+        if n in ("router_topk",):
+            continue
+        per = counts["launches"].get(n, 1)
+        probes[n] = L.KernelProbe(n, per * probe_steps)
+    for _ in range(probe_steps):
+        layer.step(X, ids, topw, dY)
+    torch.cuda.synchronize()
     kstats = {}
     for n, pr in probes.items():
         ts = pr.times_ms()

@@ -46,6 +46,9 @@ constexpr uint32_t kAStageBytes = BM * BK * 2;  // 16 KB
 constexpr uint32_t kChunkBytes = 64 * 128;      // one [64][64] bf16 swizzle block
 constexpr uint32_t kStgBytes = 32 * 128;        // staging tile per epilogue warp
 constexpr uint32_t kRingBytes = 192 * 1024;
+// Groups whose tile offsets are kept in shared memory (G + 1 <= kTileTabInts);
+// beyond that the tile scheduler searches tile_off in global memory.
+constexpr int kTileTabInts = 448;
 
 template <int BN>
 struct Cfg {
@@ -55,17 +58,19 @@ struct Cfg {
   static constexpr uint32_t kTmemCols = 2 * BN;              // power of two >= 32
   static constexpr size_t kSmemBytes = 1024 /*alignment slack*/ +
                                        static_cast<size_t>(kStages) * kStageBytes +
-                                       kEpiWarps * kStgBytes + 256 /*barriers*/;
+                                       kEpiWarps * kStgBytes + 256 /*barriers*/ +
+                                       kTileTabInts * 4 /*tile_off copy*/;
 };
 
 // Group owning permuted M tile mt: the largest g with tile_off[g] <= mt
-// (non-empty because mt < tile_off[G]).
-__device__ __forceinline__ int group_of_tile(const int32_t* __restrict__ tile_off, int G,
-                                             int mt) {
+// (non-empty because mt < tile_off[G]).  `tab` is the CTA's shared-memory
+// copy of tile_off, or nullptr (search global memory).
+__device__ __forceinline__ int group_of_tile(const int32_t* __restrict__ tile_off,
+                                             const int* tab, int G, int mt) {
   int lo = 0, hi = G - 1;
   while (lo < hi) {
     const int mid = (lo + hi + 1) >> 1;
-    if (__ldg(tile_off + mid) <= mt) lo = mid;
+    if ((tab ? tab[mid] : __ldg(tile_off + mid)) <= mt) lo = mid;
     else hi = mid - 1;
   }
   return lo;
@@ -111,7 +116,9 @@ __device__ __forceinline__ uint4 f4_as_u4(float a, float b, float c, float d) {
                     __float_as_uint(d));
 }
 
-__device__ __forceinline__ float sigmoidf_(float z) { return 1.f / (1.f + __expf(-z)); }
+// Logistic function with the fast reciprocal (relative error ~2^-22, far
+// below the 16 significant bits the saved values keep).
+__device__ __forceinline__ float sigmoidf_(float z) { return __fdividef(1.f, 1.f + __expf(-z)); }
 
 // ------------------------------------------------------------ staging tile
 // A warp's staging tile is 32 rows x 128 bytes (8 chunks of 16 B) with the
@@ -199,20 +206,26 @@ struct TileInfo {
   int nkb;     // wgrad: 64-row K blocks per slice
 };
 
-template <bool WGRAD>
-__device__ __forceinline__ TileInfo tile_info(const GemmParams& p, int t) {
+// ROWS = false skips the row range (row0, nvalid) of a rows-mode tile, which
+// the MMA issuer does not need.
+template <bool WGRAD, bool ROWS = true>
+__device__ __forceinline__ TileInfo tile_info(const GemmParams& p, int t, const int* tab) {
   TileInfo ti;
   if (!WGRAD) {
     ti.mt = t / p.n_ntiles;
     ti.nt = t - ti.mt * p.n_ntiles;
-    ti.g = group_of_tile(p.tile_off, p.G, ti.mt);
+    ti.g = group_of_tile(p.tile_off, tab, p.G, ti.mt);
     ti.nk = 0;
     for (int s = 0; s < p.nslices; ++s) ti.nk += (p.sl[s].K + BK - 1) / BK;
-    const int local = ti.mt - __ldg(p.tile_off + ti.g);
-    const int off = __ldg(p.offsets + ti.g);
-    const int cnt = __ldg(p.offsets + ti.g + 1) - off;
-    ti.row0 = off + local * BM;
-    ti.nvalid = min(BM, cnt - local * BM);
+    ti.row0 = 0;
+    ti.nvalid = 0;
+    if (ROWS) {
+      const int local = ti.mt - (tab ? tab[ti.g] : __ldg(p.tile_off + ti.g));
+      const int off = __ldg(p.offsets + ti.g);
+      const int cnt = __ldg(p.offsets + ti.g + 1) - off;
+      ti.row0 = off + local * BM;
+      ti.nvalid = min(BM, cnt - local * BM);
+    }
     ti.nkb = 0;
   } else {
     ti.g = t / p.n_ntiles;
@@ -521,6 +534,9 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
   uint64_t* drain_bar = tempty_bar + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain_bar + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  int* tile_tab = reinterpret_cast<int*>(reinterpret_cast<uint8_t*>(full_bar) + 256);
+  const int* tab = (!WGRAD && p.G + 1 <= kTileTabInts) ? tile_tab : nullptr;
+
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -552,6 +568,11 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
     tmem_alloc(tmem_slot, C::kTmemCols);
     tmem_relinquish();
   }
+  // everything above overlaps the previous kernel; from here on its outputs
+  // (routing tables, permuted rows, intermediates) are read
+  pdl_wait();
+  if (tab != nullptr)
+    for (int i = threadIdx.x; i <= p.G; i += blockDim.x) tile_tab[i] = __ldg(p.tile_off + i);
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
@@ -586,7 +607,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
     };
     int y[4] = {0, 0, 0, 0};
     for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
-      const TileInfo ti = tile_info<WGRAD>(p, t);
+      const TileInfo ti = tile_info<WGRAD>(p, t, tab);
       if (!WGRAD && p.gather_any) lane_rows(ti.row0, ti.nvalid, 4, y);
       for (int kb = 0; kb < ti.nk; ++kb) {
         int s = 0, kc = 0, kext = 0, row = 0;
@@ -702,7 +723,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
     int local = 0;
     bool ok = true;
     for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x, ++local) {
-      const TileInfo ti = tile_info<WGRAD>(p, t);
+      const TileInfo ti = tile_info<WGRAD, WGRAD>(p, t, tab);
       const int buf = local & 1;
       const uint32_t use = static_cast<uint32_t>(local >> 1);
       int w_ok = 1;
@@ -785,7 +806,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
     const uint32_t stg = smem_u32(stage_tiles + ew * kStgBytes);
     int local = 0;
     for (int t = blockIdx.x; t < num_tiles; t += gridDim.x, ++local) {
-      const TileInfo ti = tile_info<WGRAD>(p, t);
+      const TileInfo ti = tile_info<WGRAD>(p, t, tab);
       const int buf = local & 1;
       const uint32_t use = static_cast<uint32_t>(local >> 1);
       if (!mbar_wait(tfull_bar + buf, use & 1u, abort_flag, kWaitTimeoutNs)) break;
@@ -833,8 +854,7 @@ cudaError_t launch_one(const GemmParams& p, int num_sms, cudaStream_t s) {
   if (e != cudaSuccess) return e;
   const int tiles = WGRAD ? p.G * p.n_ntiles : p.max_tiles;
   const int grid = tiles < num_sms ? (tiles > 0 ? tiles : 1) : num_sms;
-  kern<<<grid, kThreads, C::kSmemBytes, s>>>(p);
-  return cudaGetLastError();
+  return launch_pdl(kern, dim3(grid), dim3(kThreads), C::kSmemBytes, s, p);
 }
 
 }  // namespace

@@ -9,6 +9,25 @@
 
 namespace moe {
 
+// Launches a kernel with programmatic stream serialization: it may begin
+// (and run up to its griddepcontrol.wait) while the previous kernel of the
+// stream finishes, which hides launch latency and its own set-up.
+template <typename... Params, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(Params...), dim3 grid, dim3 block, size_t smem,
+                       cudaStream_t s, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, static_cast<Args&&>(args)...);
+}
+
 constexpr int kTileM = 128;            // rows per M tile (= permuted layout granularity)
 constexpr int kMaxExperts = 1024;      // routed experts supported
 constexpr uint64_t kWaitTimeoutNs = 4000000000ull;  // pipeline waits give up after 4 s

@@ -19,6 +19,15 @@ __device__ __forceinline__ uint64_t globaltimer_ns() {
   return t;
 }
 
+// ------------------------------------------------- programmatic dependent launch
+// A kernel launched with programmatic stream serialization may start while
+// the previous kernel of its stream is finishing.  pdl_wait() blocks until
+// that kernel has completed and its memory is visible; everything before it
+// must not read what earlier kernels write.  A no-op for a normal launch.
+// (No kernel here signals its dependents early: waiting CTAs of the next
+// kernel would then hold SMs that the second stream's kernels can use.)
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 // ---------------------------------------------------------------- mbarrier
 __device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
   asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count)

@@ -27,6 +27,7 @@
 #include <cstdint>
 
 #include "internal.h"
+#include "ptx.cuh"
 
 namespace moe {
 namespace {
@@ -146,6 +147,7 @@ __global__ void __launch_bounds__(kRouteThreads) route_hist_kernel(
   for (int x = threadIdx.x; x < kRouteWarps * G; x += blockDim.x) cnt[x] = 0;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int base = blockIdx.x * (kRouteThreads * PER) + warp * (32 * PER);
+  pdl_wait();
   int ev[PER];
   load_ids_any_order<PER, SHARED>(ids, base, lane, N, k, K, E, vec != 0, ev);
   __syncthreads();
@@ -168,6 +170,7 @@ __global__ void __launch_bounds__(kRouteThreads) route_hist_kernel(
 
 __global__ void __launch_bounds__(1024) route_scan_kernel(int32_t* __restrict__ hist, int C,
                                                          int32_t* __restrict__ counts) {
+  pdl_wait();
   int32_t* h = hist + static_cast<int64_t>(blockIdx.x) * C;
   const int per = (C + blockDim.x - 1) / blockDim.x;
   const int lo = min(C, static_cast<int>(threadIdx.x) * per);
@@ -204,6 +207,7 @@ __global__ void __launch_bounds__(kRouteThreads, 4) route_scatter_kernel(
   int* delta = lbase + (G + 1);       // [G]   global position - chunk-local position, group g
   int* stage = delta + G;             // [CH]  flat index at each chunk-local sorted position
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  pdl_wait();
 
   // this warp's ids, in walk order (all loads in flight before the scans)
   const int base = blockIdx.x * CH + warp * (32 * PER);
@@ -346,6 +350,7 @@ template <int NC>
 __global__ void __launch_bounds__(256) router_topk_kernel(const float* __restrict__ logits, int T,
                                                          int E, int k, int32_t* __restrict__ ids,
                                                          float* __restrict__ w) {
+  pdl_wait();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int t = blockIdx.x * 8 + warp;
   if (t >= T) return;
@@ -403,13 +408,13 @@ cudaError_t launch_router_topk(const float* logits, int T, int E, int k, int32_t
   if (T == 0) return cudaSuccess;
   const dim3 grid((T + 7) / 8), block(256);
   const int nc = (E + 31) / 32;
-  if (nc <= 1) router_topk_kernel<1><<<grid, block, 0, s>>>(logits, T, E, k, ids, w);
-  else if (nc <= 2) router_topk_kernel<2><<<grid, block, 0, s>>>(logits, T, E, k, ids, w);
-  else if (nc <= 4) router_topk_kernel<4><<<grid, block, 0, s>>>(logits, T, E, k, ids, w);
-  else if (nc <= 8) router_topk_kernel<8><<<grid, block, 0, s>>>(logits, T, E, k, ids, w);
-  else if (nc <= 16) router_topk_kernel<16><<<grid, block, 0, s>>>(logits, T, E, k, ids, w);
-  else router_topk_kernel<32><<<grid, block, 0, s>>>(logits, T, E, k, ids, w);
-  return cudaGetLastError();
+  if (nc <= 1) return launch_pdl(router_topk_kernel<1>, grid, block, 0, s, logits, T, E, k, ids, w);
+  if (nc <= 2) return launch_pdl(router_topk_kernel<2>, grid, block, 0, s, logits, T, E, k, ids, w);
+  if (nc <= 4) return launch_pdl(router_topk_kernel<4>, grid, block, 0, s, logits, T, E, k, ids, w);
+  if (nc <= 8) return launch_pdl(router_topk_kernel<8>, grid, block, 0, s, logits, T, E, k, ids, w);
+  if (nc <= 16)
+    return launch_pdl(router_topk_kernel<16>, grid, block, 0, s, logits, T, E, k, ids, w);
+  return launch_pdl(router_topk_kernel<32>, grid, block, 0, s, logits, T, E, k, ids, w);
 }
 
 template <int PER, bool SHARED, int NB>
@@ -424,12 +429,15 @@ cudaError_t launch_route_per(const int32_t* ids, int N, int k, int K, int E, int
                                        static_cast<int>(sm_scat));
   if (e != cudaSuccess) return e;
   const int vec = (reinterpret_cast<uintptr_t>(ids) & 15u) == 0 ? 1 : 0;
-  route_hist_kernel<PER, SHARED><<<C, kRouteThreads, sm_hist, s>>>(ids, N, k, K, E, G, C, vec,
-                                                                   hist, status);
-  route_scan_kernel<<<G, 1024, 0, s>>>(hist, C, counts);
-  route_scatter_kernel<PER, SHARED, NB><<<C, kRouteThreads, sm_scat, s>>>(
-      ids, N, k, K, E, G, C, hist, counts, offsets, tile_off, sorted_src, dest_pos);
-  return cudaGetLastError();
+  e = launch_pdl(route_hist_kernel<PER, SHARED>, dim3(C), dim3(kRouteThreads), sm_hist, s, ids,
+                 N, k, K, E, G, C, vec, hist, status);
+  if (e == cudaSuccess)
+    e = launch_pdl(route_scan_kernel, dim3(G), dim3(1024), 0, s, hist, C, counts);
+  if (e == cudaSuccess)
+    e = launch_pdl(route_scatter_kernel<PER, SHARED, NB>, dim3(C), dim3(kRouteThreads), sm_scat,
+                   s, ids, N, k, K, E, G, C, static_cast<const int32_t*>(hist),
+                   static_cast<const int32_t*>(counts), offsets, tile_off, sorted_src, dest_pos);
+  return e;
 }
 
 template <int PER, bool SHARED>

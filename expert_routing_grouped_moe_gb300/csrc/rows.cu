@@ -14,6 +14,7 @@
 #include <cstdint>
 
 #include "internal.h"
+#include "ptx.cuh"
 
 namespace moe {
 namespace {
@@ -26,6 +27,7 @@ __global__ void __launch_bounds__(256) permute_kernel(const uint4* __restrict__ 
                                                      int d8, int K,
                                                      const int32_t* __restrict__ dest_pos,
                                                      uint4* __restrict__ dst) {
+  pdl_wait();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int t = blockIdx.x * 8 + warp;
   if (t >= T) return;
@@ -74,6 +76,7 @@ __global__ void __launch_bounds__(256) combine_kernel(
     float* __restrict__ slot_out, uint4* __restrict__ out) {
   __shared__ int s_row[8][kMaxSlots];
   __shared__ float s_c[8][kMaxSlots];
+  pdl_wait();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int t = blockIdx.x * 8 + warp;
   if (t >= T) return;
@@ -113,6 +116,7 @@ __global__ void __launch_bounds__(256) combine_kernel(
 
 __global__ void sum_parts_kernel(const float* __restrict__ parts, int nparts, int64_t stride,
                                  int64_t n, float* __restrict__ out) {
+  pdl_wait();
   for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < n;
        i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
     float s = 0.f;
@@ -126,27 +130,26 @@ __global__ void sum_parts_kernel(const float* __restrict__ parts, int nparts, in
 cudaError_t launch_permute(const uint16_t* src, int T, int d, int K, const int32_t* dest_pos,
                            uint16_t* dst, cudaStream_t s) {
   if (T == 0) return cudaSuccess;
-  permute_kernel<<<(T + 7) / 8, 256, 0, s>>>(reinterpret_cast<const uint4*>(src), T, d / 8, K,
-                                             dest_pos, reinterpret_cast<uint4*>(dst));
-  return cudaGetLastError();
+  return launch_pdl(permute_kernel, dim3((T + 7) / 8), dim3(256), 0, s,
+                    reinterpret_cast<const uint4*>(src), T, d / 8, K, dest_pos,
+                    reinterpret_cast<uint4*>(dst));
 }
 
 cudaError_t launch_combine(const uint16_t* rows, const int32_t* dest_pos, int T, int d, int k,
                            int shared, const float* weights, const float* row_scalars,
                            float* slot_out, uint16_t* out, cudaStream_t s) {
   if (T == 0) return cudaSuccess;
-  combine_kernel<<<(T + 7) / 8, 256, 0, s>>>(reinterpret_cast<const uint4*>(rows), dest_pos, T,
-                                             d / 8, k, shared, weights, row_scalars, slot_out,
-                                             reinterpret_cast<uint4*>(out));
-  return cudaGetLastError();
+  return launch_pdl(combine_kernel, dim3((T + 7) / 8), dim3(256), 0, s,
+                    reinterpret_cast<const uint4*>(rows), dest_pos, T, d / 8, k, shared, weights,
+                    row_scalars, slot_out, reinterpret_cast<uint4*>(out));
 }
 
 cudaError_t launch_sum_parts(const float* parts, int nparts, int64_t stride, int64_t n,
                              float* out, cudaStream_t s) {
   if (n == 0) return cudaSuccess;
   const int blocks = static_cast<int>(std::min<int64_t>((n + 255) / 256, 4096));
-  sum_parts_kernel<<<blocks, 256, 0, s>>>(parts, nparts, stride, n, out);
-  return cudaGetLastError();
+  return launch_pdl(sum_parts_kernel, dim3(blocks), dim3(256), 0, s, parts, nparts, stride, n,
+                    out);
 }
 
 }  // namespace moe
