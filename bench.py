@@ -35,7 +35,10 @@ PEAKS_FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # DRAM traffic per launch of the dominant kernel from one ncu capture
 # (dram__bytes_read.sum + dram__bytes_write.sum), keyed by kernel and workload;
 # None until captured for the current kernel version.
-NCU_TRAFFIC_BYTES = {}
+# dram__bytes_read.sum + dram__bytes_write.sum of one launch of the dominant
+# kernel, read from one ncu --set full capture of the current kernel
+# (kernel, workload)
+NCU_TRAFFIC_BYTES = {("gate_up", "qwen3_30b_a3b"): 1033093000 + 274513408}
 
 
 def parse_args(argv=None):
@@ -51,6 +54,8 @@ def parse_args(argv=None):
     ap.add_argument("--cpu-budget-s", type=float, default=20.0)
     ap.add_argument("--probe-steps", type=int, default=100)
     ap.add_argument("--no-route-sweep", action="store_true")
+    ap.add_argument("--route-only", action="store_true",
+                    help="time only moe_route on the routing sweep points")
     return ap.parse_args(argv)
 
 
@@ -350,14 +355,16 @@ def run_e2e(torch, layer, X, dY, ids, topw, cfg, steps, main):
 
 
 def routing_sweep(torch, L, synth, dev, peaks, points=((1 << 20, 128, 8), (1 << 18, 64, 4)),
-                  d=2048, reps=5):
+                  d=2048, reps=5, route_only=False):
     """Route, permute and combine throughput (algorithmic GB/s) on the routing
-    workload's large points: T tokens, E experts, top-k, bf16 rows of d."""
+    workload's large points: T tokens, E experts, top-k, bf16 rows of d.
+    Each call is timed on its own with CUDA events, after a write of 256 MB
+    (twice L2) that evicts its inputs from L2.  route_only: routing alone,
+    with only the id and routing-table buffers allocated."""
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
     out = []
     for T, E, k in points:
         ids = synth.topk_ids(T, E, k, "uniform", seed=7, device=dev)
-        w = synth.combine_weights(T, k, seed=7, device=dev)
-        X = synth.hidden_rows(T, d, seed=7, device=dev)
         N = T * k
         counts = torch.empty(E, dtype=torch.int32, device=dev)
         offsets = torch.empty(E + 1, dtype=torch.int32, device=dev)
@@ -365,36 +372,57 @@ def routing_sweep(torch, L, synth, dev, peaks, points=((1 << 20, 128, 8), (1 << 
         src = torch.empty(N, dtype=torch.int32, device=dev)
         dst = torch.empty(N, dtype=torch.int32, device=dev)
         ws = torch.empty(L.moe_route_workspace_size(T, k, E), dtype=torch.uint8, device=dev)
-        Xp = torch.empty(N, d, dtype=torch.bfloat16, device=dev)
-        Y = torch.empty(T, d, dtype=torch.bfloat16, device=dev)
         calls = {
             "route": (lambda: L.moe_route(ids, E, False, counts, offsets, tile_off, src, dst, ws),
                       4 * T * k + 8 * N + 12 * E),
-            "permute": (lambda: L.moe_permute(X, k, dst, Xp),
-                        2 * T * d + 2 * N * d + 4 * N),
-            "combine": (lambda: L.moe_unpermute_combine(Xp, dst, k, False, Y, weights=w),
-                        2 * N * d + 2 * T * d + 8 * N + 4 * T * k),
         }
+        if not route_only:
+            w = synth.combine_weights(T, k, seed=7, device=dev)
+            X = synth.hidden_rows(T, d, seed=7, device=dev)
+            Xp = torch.empty(N, d, dtype=torch.bfloat16, device=dev)
+            Y = torch.empty(T, d, dtype=torch.bfloat16, device=dev)
+            calls["permute"] = (lambda: L.moe_permute(X, k, dst, Xp),
+                                2 * T * d + 2 * N * d + 4 * N)
+            calls["combine"] = (lambda: L.moe_unpermute_combine(Xp, dst, k, False, Y, weights=w),
+                                2 * N * d + 2 * T * d + 8 * N + 4 * T * k)
         res = {"T": T, "E": E, "k": k, "d": d}
         for name, (fn, nbytes) in calls.items():
             fn()
             torch.cuda.synchronize()
-            e0 = torch.cuda.Event(enable_timing=True)
-            e1 = torch.cuda.Event(enable_timing=True)
-            e0.record()
+            total = 0.0
             for _ in range(reps):
+                flush.fill_(1)
+                e0 = torch.cuda.Event(enable_timing=True)
+                e1 = torch.cuda.Event(enable_timing=True)
+                e0.record()
                 fn()
-            e1.record()
-            torch.cuda.synchronize()
-            ms = e0.elapsed_time(e1) / reps
+                e1.record()
+                torch.cuda.synchronize()
+                total += e0.elapsed_time(e1)
+            ms = total / reps
             gbs = nbytes / (ms / 1e3) / 1e9
             res[name] = {"ms": ms, "gbs": gbs, "frac_of_hbm": gbs / peaks["hbm_gbs"]}
         out.append(res)
-        del Xp, Y, X
+        calls.clear()
+        X = Xp = Y = w = None  # noqa: F841  (free this point's rows before the next)
         torch.cuda.empty_cache()
     if L.moe_status() != L.MOE_OK:
         raise SystemExit("device status error in the routing sweep")
     return out
+
+
+def run_route_only(args):
+    """Routing alone on the sweep's large points (the command the routing
+    profiles are taken with): small allocations, one JSON line."""
+    import torch
+    from expert_routing_grouped_moe_gb300 import _lib as L, build, synth
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    build.build()
+    L.load()
+    res = routing_sweep(torch, L, synth, dev, peaks=load_peaks()[0], reps=args.steps,
+                        route_only=True)
+    return {"metric": "routing GB/s (route only)", "unit": "GB/s", "routing_sweep": res}
 
 
 # ---------------------------------------------------------------- our arm
@@ -612,7 +640,10 @@ def run_reference(args):
 
 def main(argv=None):
     args = parse_args(argv)
-    out = run_reference(args) if args.impl == "reference" else run_ours(args)
+    if args.route_only:
+        out = run_route_only(args)
+    else:
+        out = run_reference(args) if args.impl == "reference" else run_ours(args)
     if out is not None:
         print(json.dumps(out), flush=True)
 
