@@ -239,7 +239,7 @@ bool make_map_3d(CUtensorMap* m, const void* base, uint64_t G, uint64_t rows, ui
 namespace {
 
 struct BwdWs {
-  uint16_t *us, *uw, *xw, *vs, *dh;  // hi/lo pair buffers
+  uint16_t *us, *vs, *dh;  // hi/lo pair buffers
   float* dwp;
   size_t bytes;
 };
@@ -258,8 +258,6 @@ BwdWs bwd_layout(const moe_dims* dm, void* base) {
   uint8_t* b = static_cast<uint8_t*>(base);
   size_t o = 0;
   w.us = reinterpret_cast<uint16_t*>(b + o); o += nr;
-  w.uw = reinterpret_cast<uint16_t*>(b + o); o += nr;
-  w.xw = reinterpret_cast<uint16_t*>(b + o); o += nr;
   w.vs = reinterpret_cast<uint16_t*>(b + o); o += nr;
   w.dh = reinterpret_cast<uint16_t*>(b + o); o += ndh;
   w.dwp = reinterpret_cast<float*>(b + o); o += ndw;
@@ -497,7 +495,7 @@ int moe_lora_grouped_mlp_fwd(const moe_dims* dims, const moe_bf16* Xp, const moe
     p.nslices = 1; p.N = r; p.n_ntiles = (r + 63) / 64; p.out0 = xa_gu; p.ld0 = r; p.pair = Nr;
     if ((rc = run_gemm({64, false, false, Epi::kLoRA}, p, R, st->num_sms, s, "xa_gu"))) return rc;
   }
-  {  // h = Xp W_gu^T + (s xa) B_gu^T (fp32) ; act pair = silu(gate) * up
+  {  // h = Xp W_gu^T + (s xa) B_gu^T (fp32) ; act pair = w * silu(gate) * up
     GemmParams p = base;
     SLICE_ROWS(p, 0, Xp, X, d, MAP3(p.sl[0].b, W_gu, G, 2 * f, d, 128, 64), d);
     SLICE(p, 1, xa_gu, N, r, MAP3(p.sl[1].b, B_gu, G, 2 * f, r, 128, 64), r);
@@ -507,19 +505,19 @@ int moe_lora_grouped_mlp_fwd(const moe_dims* dims, const moe_bf16* Xp, const moe
     if ((rc = run_gemm({256, false, false, Epi::kSwiGLU}, p, R, st->num_sms, s, "gate_up")))
       return rc;
   }
-  {  // xa_dn pair = s * act A_dn^T   (act = hi + lo)
+  {  // xa_dn pair = s * act A_dn^T   (act = hi + lo, already scaled by w)
     GemmParams p = base;
     SLICE(p, 0, act, N, f, MAP3(p.sl[0].b, A_dn, G, r, f, 64, 64), f);
     SLICE(p, 1, act + Nf, N, f, MAP3(p.sl[1].b, A_dn, G, r, f, 64, 64), f);
     p.nslices = 2; p.N = r; p.n_ntiles = (r + 63) / 64; p.out0 = xa_dn; p.ld0 = r; p.pair = Nr;
     if ((rc = run_gemm({64, false, false, Epi::kLoRA}, p, R, st->num_sms, s, "xa_dn"))) return rc;
   }
-  {  // Yp = w * (act W_dn^T + (s xa_dn) B_dn^T)
+  {  // Yp = act W_dn^T + xa_dn B_dn^T = w * (o)   (act and xa_dn carry w)
     GemmParams p = base;
     SLICE(p, 0, act, N, f, MAP3(p.sl[0].b, W_dn, G, d, f, 256, 64), f);
     SLICE(p, 1, xa_dn, N, r, MAP3(p.sl[1].b, B_dn, G, d, r, 256, 64), r);
     p.nslices = 2; p.N = d; p.n_ntiles = (d + 255) / 256; p.out0 = Yp; p.ld0 = d;
-    if ((rc = run_gemm({256, false, false, Epi::kScaleW}, p, R, st->num_sms, s, "down")))
+    if ((rc = run_gemm({256, false, false, Epi::kStore}, p, R, st->num_sms, s, "down")))
       return rc;
   }
   return ok();
@@ -588,8 +586,8 @@ int moe_lora_grouped_mlp_bwd(const moe_dims* dims, const moe_bf16* dYp, const mo
     const char* name;
   };
   const WgradJob jobs[4] = {
-      {dYp, dY, 0, d, w.xw, dB_dn, 0, "dB_dn"},
-      {act, nullptr, 1, f, w.uw, dA_dn, 1, "dA_dn"},
+      {dYp, dY, 0, d, xa_dn, dB_dn, 0, "dB_dn"},
+      {act, nullptr, 1, f, w.us, dA_dn, 1, "dA_dn"},
       {w.dh, nullptr, 1, 2 * f, xa_gu, dB_gu, 0, "dB_gu"},
       {Xp, X, 0, d, w.vs, dA_gu, 1, "dA_gu"},
   };
@@ -619,11 +617,11 @@ int moe_lora_grouped_mlp_bwd(const moe_dims* dims, const moe_bf16* dYp, const mo
   cudaStream_t aux = nullptr;
   if ((rc = aux_stream(st, &aux))) return rc;
 
-  {  // u = dYp B_dn -> pairs us = s*u, uw = s*w*u, xw = w * (s xa_dn)
+  {  // u = dYp B_dn -> pair us = s*u
     GemmParams p = base;
     SLICE_ROWS(p, 0, dYp, dY, d, MAP3(p.sl[0].b, B_dn, G, d, r, 64, 64), d);
     p.nslices = 1; p.N = r; p.n_ntiles = (r + 63) / 64; p.ld0 = r; p.pair = Nr;
-    p.out0 = w.us; p.out1 = w.uw; p.out2 = w.xw; p.aux0 = xa_dn;
+    p.out0 = w.us;
     if ((rc = run_gemm({64, true, false, Epi::kLoRA}, p, R, st->num_sms, s, "u"))) return rc;
   }
   if ((rc = stream_dep(st->ev[0], s, aux))) return rc;

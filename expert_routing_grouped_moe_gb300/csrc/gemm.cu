@@ -263,8 +263,10 @@ __device__ __forceinline__ void epi_swiglu(const GemmParams& p, const TileInfo& 
                                            int hf, int64_t row0, int nrows, int lane,
                                            uint32_t stg) {
   // accumulator columns [0, BN/2) = gate, [BN/2, BN) = up of the same features;
-  // this warp: features hf*BN/4 + [0, BN/4)
+  // this warp: features hf*BN/4 + [0, BN/4).  The saved activation is scaled
+  // by the row's routing weight: act' = w * silu(gate) * up.
   const int f = p.N;
+  const float w = lane < nrows ? row_weight(p, row0 + lane) : 0.f;
 #pragma unroll 1
   for (int sub = 0; sub < BN / 4; sub += 16) {
     const int cg = hf * (BN / 4) + sub;
@@ -272,7 +274,7 @@ __device__ __forceinline__ void epi_swiglu(const GemmParams& p, const TileInfo& 
     tmem_ld16(tq + cg, g);
     tmem_ld16(tq + BN / 2 + cg, u);
 #pragma unroll
-    for (int i = 0; i < 16; ++i) a[i] = g[i] * sigmoidf_(g[i]) * u[i];
+    for (int i = 0; i < 16; ++i) a[i] = w * (g[i] * sigmoidf_(g[i]) * u[i]);
     const int j0 = ti.nt * (BN / 2) + cg;
     // h (fp32): [gate 16 | up 16]
 #pragma unroll
@@ -311,11 +313,10 @@ __device__ __forceinline__ void epi_swiglu(const GemmParams& p, const TileInfo& 
   }
 }
 
-template <int BN, bool SCALE>
+template <int BN>
 __device__ __forceinline__ void epi_store(const GemmParams& p, const TileInfo& ti, uint32_t tq,
                                           int hf, int64_t row0, int nrows, int lane,
                                           uint32_t stg) {
-  const float w = SCALE ? (lane < nrows ? row_weight(p, row0 + lane) : 0.f) : 1.f;
 #pragma unroll 1
   for (int c0 = hf * (BN / 2); c0 < (hf + 1) * (BN / 2); c0 += 64) {
 #pragma unroll
@@ -325,8 +326,8 @@ __device__ __forceinline__ void epi_store(const GemmParams& p, const TileInfo& t
       float a[8], b[8];
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
-        a[i] = w * v[i];
-        b[i] = w * v[8 + i];
+        a[i] = v[i];
+        b[i] = v[8 + i];
       }
       sts128(stg_at(stg, lane, 2 * q4),
              make_uint4(pack_bf16x2(a[0], a[1]), pack_bf16x2(a[2], a[3]),
@@ -437,10 +438,9 @@ __device__ __forceinline__ void epi_dgrad_dn(const GemmParams& p, const TileInfo
 template <int BN>
 __device__ __forceinline__ void epi_lora(const GemmParams& p, const TileInfo& ti, uint32_t tq,
                                          int hf, int64_t row0, int nrows, int lane) {
+  // out0 = s * acc as a hi/lo pair
   const int64_t row = row0 + lane;
   const bool valid = lane < nrows;
-  const bool need_w = p.out1 != nullptr || p.out2 != nullptr;
-  const float w = (need_w && valid) ? row_weight(p, row) : 0.f;
   const float s = p.scale;
 #pragma unroll 1
   for (int c0 = hf * (BN / 2); c0 < (hf + 1) * (BN / 2); c0 += 16) {
@@ -450,24 +450,10 @@ __device__ __forceinline__ void epi_lora(const GemmParams& p, const TileInfo& ti
     for (int h8 = 0; h8 < 2; ++h8) {
       const int j = ti.nt * BN + c0 + h8 * 8;
       if (valid && j < p.N) {
-        const int64_t o = row * p.ld0 + j;
         float ov[8];
 #pragma unroll
         for (int i = 0; i < 8; ++i) ov[i] = s * v16[h8 * 8 + i];
-        store8_pair(p.out0 + o, p.pair, ov);
-        if (p.out1 != nullptr) {
-#pragma unroll
-          for (int i = 0; i < 8; ++i) ov[i] *= w;
-          store8_pair(p.out1 + o, p.pair, ov);
-        }
-        if (p.out2 != nullptr) {
-          float ah[8], al[8];
-          load8(p.aux0 + o, ah);
-          load8(p.aux0 + p.pair + o, al);
-#pragma unroll
-          for (int i = 0; i < 8; ++i) ah[i] = w * (ah[i] + al[i]);
-          store8_pair(p.out2 + o, p.pair, ah);
-        }
+        store8_pair(p.out0 + row * p.ld0 + j, p.pair, ov);
       }
     }
   }
@@ -821,10 +807,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
         epi_wgrad(p, ti, tq, hf, q, lane, stg);
       } else if constexpr (EPI == static_cast<int>(Epi::kSwiGLU)) {
         epi_swiglu<BN>(p, ti, tq, hf, row0, nrows, lane, stg);
-      } else if constexpr (EPI == static_cast<int>(Epi::kScaleW)) {
-        epi_store<BN, true>(p, ti, tq, hf, row0, nrows, lane, stg);
       } else if constexpr (EPI == static_cast<int>(Epi::kStore)) {
-        epi_store<BN, false>(p, ti, tq, hf, row0, nrows, lane, stg);
+        epi_store<BN>(p, ti, tq, hf, row0, nrows, lane, stg);
       } else if constexpr (EPI == static_cast<int>(Epi::kLoRA)) {
         epi_lora<BN>(p, ti, tq, hf, row0, nrows, lane);
       } else if constexpr (EPI == static_cast<int>(Epi::kDgradDn)) {
@@ -861,7 +845,6 @@ cudaError_t launch_one(const GemmParams& p, int num_sms, cudaStream_t s) {
 
 cudaError_t launch_gemm(const GemmShape& sh, const GemmParams& p, int num_sms, cudaStream_t s) {
   constexpr int kSw = static_cast<int>(Epi::kSwiGLU);
-  constexpr int kSc = static_cast<int>(Epi::kScaleW);
   constexpr int kSt = static_cast<int>(Epi::kStore);
   constexpr int kLo = static_cast<int>(Epi::kLoRA);
   constexpr int kDd = static_cast<int>(Epi::kDgradDn);
@@ -874,7 +857,7 @@ cudaError_t launch_gemm(const GemmShape& sh, const GemmParams& p, int num_sms, c
   }
   if (sh.BN == 256 && !sh.b_mn) {
     if (e == kSw) return launch_one<256, false, false, kSw>(p, num_sms, s);
-    if (e == kSc) return launch_one<256, false, false, kSc>(p, num_sms, s);
+    if (e == kSt) return launch_one<256, false, false, kSt>(p, num_sms, s);
   }
   if (sh.BN == 256 && sh.b_mn) {
     if (e == kDd) return launch_one<256, true, false, kDd>(p, num_sms, s);

@@ -76,10 +76,9 @@ cudaError_t launch_sum_parts(const float* parts, int nparts, int64_t stride, int
 // values hi + lo (hi = bf16(v), lo = bf16(v - hi)), ~16 significant bits; a
 // pair buffer holds hi at [0, P*cols) and lo at [P*cols, 2*P*cols).
 enum class Epi : int {
-  kSwiGLU = 0,   // h = acc (fp32, gate|up halves), act = silu(gate)*up as a hi/lo pair
-  kScaleW = 1,   // out0 = bf16(w_row * acc)
+  kSwiGLU = 0,   // h = acc (fp32, gate|up halves), act' = w*silu(gate)*up as a hi/lo pair
   kStore = 2,    // out0 = bf16(acc)
-  kLoRA = 3,     // pairs: out0 = s*acc; out1 = s*w*acc; out2 = w*(aux0 hi + lo)
+  kLoRA = 3,     // out0 = s*acc as a hi/lo pair
   kDgradDn = 4,  // SwiGLU backward from fp32 h (fin): dh pair (out0), dw partial (fout)
   kWgrad = 5,    // fp32 per-group weight gradient: acc[:, n] + acc[:, 64 + n]
 };
@@ -116,12 +115,9 @@ struct GemmParams {
   const int32_t* sorted_src;
   const float* topk_w;
   uint16_t* out0;
-  uint16_t* out1;
-  uint16_t* out2;
-  const uint16_t* aux0;
   float* fout;        // fp32 output: h (SwiGLU), dw partials (dgrad), weight grad (wgrad)
   const float* fin;   // fp32 input: h (dgrad)
-  int64_t ld0;        // leading dimension (elements) of out*/aux0 rows
+  int64_t ld0;        // leading dimension (elements) of out0 rows
   int64_t ldf;        // leading dimension (floats) of the fp32 h buffer (fout / fin)
   int64_t pair;       // element offset from the hi to the lo half of a pair buffer
   int64_t fstride;    // stride between dw partial slices, or group stride of fout

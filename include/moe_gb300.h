@@ -211,10 +211,12 @@ MOE_API int moe_unpermute_combine(const moe_bf16* rows, const int32_t* dest_pos,
  *   h     [P,hs]   fp32  saved gate and up pre-activations, hs = 32*ceil(f/16):
  *                        features in chunks of 16, row layout
  *                        [gate c*16..c*16+15 | up c*16..c*16+15] for chunk c
- *   act   [2,P,f]  bf16 pair  saved silu(gate) * up
+ *   act   [2,P,f]  bf16 pair  saved w_p * silu(gate) * up (scaled by the row's
+ *                              routing weight w_p; 1 for shared-expert rows)
  *   xa_gu [2,P,r]  bf16 pair  saved s * Xp A_gu^T
- *   xa_dn [2,P,r]  bf16 pair  saved s * act A_dn^T
- * The down projection consumes act's high half (Yp is a bf16 output). */
+ *   xa_dn [2,P,r]  bf16 pair  saved s * act A_dn^T (so also scaled by w_p)
+ * The down projection consumes the high halves: Yp = act W_dn^T + xa_dn B_dn^T
+ * is w_p * o without a separate scaling step (Yp is a bf16 output). */
 MOE_API int moe_lora_grouped_mlp_fwd(const moe_dims* dims, const moe_bf16* Xp,
                              const moe_bf16* X, const int32_t* counts, const int32_t* offsets,
                              const int32_t* tile_off, const int32_t* sorted_src,
@@ -237,8 +239,9 @@ MOE_API size_t moe_mlp_bwd_workspace_size(const moe_dims* dims);
  *   g = dYp W_dn + s u A_dn with u = dYp B_dn;  dact = w_p g
  *   dh = [dact*up*silu'(gate) | dact*silu(gate)];  v = dh B_gu
  *   dXp = dh W_gu + s v A_gu              [P,d] bf16 (combine -> dX)
- *   dB_dn[g] = s sum_p dO^T xa_dn          [G,d,r] fp32
- *   dA_dn[g] = s sum_p (dO B_dn)^T act     [G,r,f] fp32
+ *   dB_dn[g] = s sum_p dO^T (act_p A_dn^T) = sum_p dYp^T xa_dn   [G,d,r] fp32
+ *   dA_dn[g] = s sum_p (dO B_dn)^T act_p = sum_p (s u)^T act       [G,r,f] fp32
+ *              (act_p unscaled; the saved act and xa_dn already carry w_p)
  *   dB_gu[g] = s sum_p dh^T xa             [G,2f,r] fp32
  *   dA_gu[g] = s sum_p v^T Xp              [G,r,d] fp32
  * Gradients are overwritten (not accumulated); groups with no rows get zeros.

@@ -95,8 +95,10 @@ def test_layer_full_parity(name, gather):
         tight = dict(rel_fro=1e-4, elem=1e-4)
         assert_close_bf16(bufs["xa_gu"][prow], s * fw["xa"], "xa_gu g%d" % gi, **tight)
         assert_close_bf16(bufs["h"][prow], fw["h"], "h g%d" % gi, **tight)
-        assert_close_bf16(bufs["act"][prow], fw["act"], "act g%d" % gi, **tight)
-        assert_close_bf16(bufs["xa_dn"][prow], s * fw["xa_dn"], "xa_dn g%d" % gi, **tight)
+        # the saved act and xa_dn carry the routing weight of their row
+        assert_close_bf16(bufs["act"][prow], wt[:, None] * fw["act"], "act g%d" % gi, **tight)
+        assert_close_bf16(bufs["xa_dn"][prow], s * wt[:, None] * fw["xa_dn"], "xa_dn g%d" % gi,
+                          **tight)
         assert_close_bf16(bufs["Yp"][prow], wt[:, None] * fw["o"], "Yp g%d" % gi)
     for n, b in bufs.items():  # one permuted row per routed (token, slot)
         assert b.shape[0] == N, n
