@@ -19,6 +19,10 @@ intermediate is rounded.  Sources, cited by page and section:
 [S]  same docs, section "Implementation details / MoE LoRA changes the
      picture" -- the split-LoRA equations Y = X A (s x r), Z = Y B (s x n)
      next to X W, per routed token-expert pair.
+[I]  same docs, introduction -- the MoE kernels serve full fine-tuning as
+     well as LoRA (the section "Faster LoRA MoE training" likewise advises
+     bf16 for LoRA or full fine-tuning): the full gradients of the expert
+     weights are the plain chain rule through the same forward.
 
 Readings where the pages are silent (each listed in the design notes):
 * LoRA orientation is PEFT's: A [r, in], B [out, r], delta = s * B @ A with
@@ -197,11 +201,13 @@ def layer_forward(X, ids, w, P: OracleParams):
     return Y
 
 
-def layer_backward(X, ids, w, dY, P: OracleParams):
+def layer_backward(X, ids, w, dY, P: OracleParams, full: bool = False):
     """Gradients of L = sum(Y * dY) for frozen W and router.
 
     Returns dX [T,d], dw [T,k] (gradient w.r.t. the routing weights),
-    dA_gu, dB_gu, dA_dn, dB_dn (shapes of the adapters, every group).
+    dA_gu, dB_gu, dA_dn, dB_dn (shapes of the adapters, every group), and with
+    full=True the full fine-tuning gradients of the expert weights too ([I]):
+      dW_dn = dO^T act  [G,d,f];  dW_gu = dh^T x  [G,2f,d].
     Chain rule through the definitions of ``expert_forward``:
       dO = w dY_t;  dw = <dY_t, o>
       dB_dn = s dO^T xa_dn;  u = dO B_dn;  dA_dn = s u^T act
@@ -217,7 +223,8 @@ def layer_backward(X, ids, w, dY, P: OracleParams):
     f = P.f
     dX = np.zeros_like(X)
     dw = np.zeros(T * k)
-    grads = {n: np.zeros_like(getattr(P, n)) for n in ("A_gu", "B_gu", "A_dn", "B_dn")}
+    names = ("A_gu", "B_gu", "A_dn", "B_dn") + (("W_gu", "W_dn") if full else ())
+    grads = {n: np.zeros_like(getattr(P, n)) for n in names}
     for g, flat, tok, wt in _assignments(ids, w, P):
         if tok.size == 0:
             continue
@@ -236,11 +243,13 @@ def layer_backward(X, ids, w, dY, P: OracleParams):
         grads["B_gu"][g] = P.s * dh.T @ fw["xa"]
         v = dh @ P.B_gu[g]
         grads["A_gu"][g] = P.s * v.T @ x
+        if full:
+            grads["W_dn"][g] = dO.T @ fw["act"]
+            grads["W_gu"][g] = dh.T @ x
         dx = dh @ P.W_gu[g] + P.s * (v @ P.A_gu[g])
         np.add.at(dX, tok, dx)
     return {"dX": dX, "dw": dw.reshape(T, k),
-            "dA_gu": grads["A_gu"], "dB_gu": grads["B_gu"],
-            "dA_dn": grads["A_dn"], "dB_dn": grads["B_dn"]}
+            **{"d" + n: grads[n] for n in names}}
 
 
 # ---------------------------------------------------------------------------
@@ -314,9 +323,10 @@ def token_backward_dx(t: int, X, ids, w, dY, P: OracleParams):
     return dx, dw
 
 
-def expert_lora_grads(g: int, X, ids, w, dY, P: OracleParams):
+def expert_lora_grads(g: int, X, ids, w, dY, P: OracleParams, full: bool = False):
     """dA_gu[g], dB_gu[g], dA_dn[g], dB_dn[g] alone: sums over the rows that
-    group g receives (its routed rows, or every token for the shared expert)."""
+    group g receives (its routed rows, or every token for the shared expert);
+    with full=True also dW_gu[g] and dW_dn[g]."""
     X = np.asarray(X, dtype=np.float64)
     dY = np.asarray(dY, dtype=np.float64)
     ids = np.asarray(ids)
@@ -331,6 +341,9 @@ def expert_lora_grads(g: int, X, ids, w, dY, P: OracleParams):
         wt = np.asarray(w, dtype=np.float64)[tt, jj]
     out = {"dA_gu": np.zeros_like(P.A_gu[g]), "dB_gu": np.zeros_like(P.B_gu[g]),
            "dA_dn": np.zeros_like(P.A_dn[g]), "dB_dn": np.zeros_like(P.B_dn[g])}
+    if full:
+        out["dW_gu"] = np.zeros_like(P.W_gu[g])
+        out["dW_dn"] = np.zeros_like(P.W_dn[g])
     if tok.size == 0:
         return out
     x = X[tok]
@@ -344,4 +357,7 @@ def expert_lora_grads(g: int, X, ids, w, dY, P: OracleParams):
     dh = np.concatenate([dact * up * dsilu(gate), dact * silu(gate)], axis=1)
     out["dB_gu"] = P.s * dh.T @ fw["xa"]
     out["dA_gu"] = P.s * (dh @ P.B_gu[g]).T @ x
+    if full:
+        out["dW_dn"] = dO.T @ fw["act"]
+        out["dW_gu"] = dh.T @ x
     return out

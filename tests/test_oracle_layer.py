@@ -171,6 +171,40 @@ def test_gradients_finite_difference(shared, dup):
         check(gname, getattr(P, pname), gr[gname], setter)
 
 
+@pytest.mark.parametrize("shared,dup", [(False, False), (True, True)])
+def test_full_weight_gradients_finite_difference(shared, dup):
+    """dW_gu and dW_dn (full fine-tuning) against central differences of the
+    loss in the expert weights themselves."""
+    P, X, ids, w, dY = _problem(51 + shared, shared=shared, dup=dup)
+    gr = oracle.layer_backward(X, ids, w, dY, P, full=True)
+    rng = np.random.default_rng(7)
+    eps = 1e-5
+    for pname in ("W_gu", "W_dn"):
+        base = getattr(P, pname)
+        for _ in range(3):
+            V = rng.standard_normal(base.shape)
+            Qp, Qm = copy.deepcopy(P), copy.deepcopy(P)
+            setattr(Qp, pname, base + eps * V)
+            setattr(Qm, pname, base - eps * V)
+            fd = (_loss(Qp, X, ids, w, dY) - _loss(Qm, X, ids, w, dY)) / (2 * eps)
+            an = float(np.sum(gr["d" + pname] * V))
+            assert fd == pytest.approx(an, rel=1e-6, abs=1e-8), pname
+
+
+def test_full_and_lora_gradients_are_tied():
+    """W_eff = W + s B A, so dB = s dW A^T and dA = s B^T dW for both
+    projections: the full gradients must reproduce the LoRA gradients that
+    the chain rule computes along a different path (through xa, u, v)."""
+    P, X, ids, w, dY = _problem(61, T=13, E=5, k=3, shared=True)
+    gr = oracle.layer_backward(X, ids, w, dY, P, full=True)
+    for g in range(P.E + 1):
+        for proj in ("gu", "dn"):
+            dW = gr["dW_" + proj][g]
+            A, B = getattr(P, "A_" + proj)[g], getattr(P, "B_" + proj)[g]
+            np.testing.assert_allclose(gr["dB_" + proj][g], P.s * dW @ A.T, rtol=1e-10, atol=1e-12)
+            np.testing.assert_allclose(gr["dA_" + proj][g], P.s * B.T @ dW, rtol=1e-10, atol=1e-12)
+
+
 @pytest.mark.parametrize("shared", [False, True])
 def test_sampled_evaluators_agree(shared):
     P, X, ids, w, dY = _problem(31, T=11, E=5, k=2, shared=shared)
@@ -181,10 +215,11 @@ def test_sampled_evaluators_agree(shared):
         dx, dw = oracle.token_backward_dx(t, X, ids, w, dY, P)
         np.testing.assert_allclose(dx, gr["dX"][t], rtol=1e-12, atol=1e-12)
         np.testing.assert_allclose(dw, gr["dw"][t], rtol=1e-12, atol=1e-12)
+    grf = oracle.layer_backward(X, ids, w, dY, P, full=True)
     for g in range(P.E + (1 if shared else 0)):
-        eg = oracle.expert_lora_grads(g, X, ids, w, dY, P)
-        for n in ("dA_gu", "dB_gu", "dA_dn", "dB_dn"):
-            np.testing.assert_allclose(eg[n], gr[n][g], rtol=1e-12, atol=1e-12)
+        eg = oracle.expert_lora_grads(g, X, ids, w, dY, P, full=True)
+        for n in ("dA_gu", "dB_gu", "dA_dn", "dB_dn", "dW_gu", "dW_dn"):
+            np.testing.assert_allclose(eg[n], grf[n][g], rtol=1e-12, atol=1e-12)
 
 
 def test_empty_expert_has_zero_grads():
