@@ -81,7 +81,7 @@ def load(path: str = LIB_PATH):
                                                      _P]),
             "moe_lora_grouped_mlp_fwd": (ctypes.c_int, [ctypes.POINTER(MoeDims)] + [_P] * 19),
             "moe_mlp_bwd_workspace_size": (_SZ, [ctypes.POINTER(MoeDims)]),
-            "moe_lora_grouped_mlp_bwd": (ctypes.c_int, [ctypes.POINTER(MoeDims)] + [_P] * 26
+            "moe_lora_grouped_mlp_bwd": (ctypes.c_int, [ctypes.POINTER(MoeDims)] + [_P] * 28
                                          + [_SZ, _P]),
             "moe_status": (ctypes.c_int, [_P]),
             "moe_last_error": (ctypes.c_char_p, []),
@@ -210,8 +210,9 @@ def moe_mlp_bwd_workspace_size(dims: MoeDims) -> int:
 def moe_lora_grouped_mlp_bwd(dims: MoeDims, dYp, dY, Xp, X, counts, offsets, tile_off,
                              sorted_src, topk_w, W_gu, A_gu, B_gu, W_dn, A_dn, B_dn, h, act,
                              xa_gu, xa_dn, dXp, dw_rows, dA_gu, dB_gu, dA_dn, dB_dn, ws,
-                             stream=None):
-    """Pass permuted rows (dYp, Xp) or None and the token rows (dY, X)."""
+                             stream=None, dW_gu=None, dW_dn=None):
+    """Pass permuted rows (dYp, Xp) or None and the token rows (dY, X).
+    dW_gu [G,2f,d] / dW_dn [G,d,f] fp32: optional full weight gradients."""
     _check(load().moe_lora_grouped_mlp_bwd(
         ctypes.byref(dims), _bf(dYp, "dYp"), _bf(dY, "dY"), _bf(Xp, "Xp"), _bf(X, "X"),
         _i32(counts, "counts"),
@@ -220,6 +221,7 @@ def moe_lora_grouped_mlp_bwd(dims: MoeDims, dYp, dY, Xp, X, counts, offsets, til
         _bf(W_dn, "W_dn"), _bf(A_dn, "A_dn"), _bf(B_dn, "B_dn"), _f32(h, "h"), _bf(act, "act"),
         _bf(xa_gu, "xa_gu"), _bf(xa_dn, "xa_dn"), _bf(dXp, "dXp"), _f32(dw_rows, "dw_rows"),
         _f32(dA_gu, "dA_gu"), _f32(dB_gu, "dB_gu"), _f32(dA_dn, "dA_dn"), _f32(dB_dn, "dB_dn"),
+        _f32(dW_gu, "dW_gu"), _f32(dW_dn, "dW_dn"),
         _ptr(ws, name="ws"), ws.numel() * ws.element_size(), _stream(stream)),
         "moe_lora_grouped_mlp_bwd")
 

@@ -78,7 +78,8 @@ int device_state(DevState** out) {
 // ---- timing probe (tracing): caller-owned CUDA events around kernel launches
 const char* const kKernelNames[] = {
     "route", "permute", "combine", "router_topk", "xa_gu", "gate_up", "xa_dn", "down",
-    "u", "dgrad_dn", "v", "dgrad_gu", "dB_dn", "dA_dn", "dB_gu", "dA_gu", "dw_reduce"};
+    "u", "dgrad_dn", "v", "dgrad_gu", "dB_dn", "dA_dn", "dB_gu", "dA_gu", "dw_reduce",
+    "dW_dn", "dW_gu"};
 constexpr int kNumKernels = sizeof(kKernelNames) / sizeof(kKernelNames[0]);
 
 struct Probe {
@@ -278,6 +279,7 @@ GemmParams base_params(const moe_dims* dm, const int32_t* offsets, const int32_t
   p.sorted_src = sorted_src;
   p.topk_w = topk_w;
   p.status = status;
+  p.n_btiles = 1;
   return p;
 }
 
@@ -537,7 +539,8 @@ int moe_lora_grouped_mlp_bwd(const moe_dims* dims, const moe_bf16* dYp, const mo
                              const moe_bf16* B_dn, const float* h, const moe_bf16* act,
                              const moe_bf16* xa_gu, const moe_bf16* xa_dn, moe_bf16* dXp,
                              float* dw_rows, float* dA_gu, float* dB_gu, float* dA_dn,
-                             float* dB_dn, void* ws, size_t ws_bytes, moe_stream_t stream) {
+                             float* dB_dn, float* dW_gu, float* dW_dn, void* ws,
+                             size_t ws_bytes, moe_stream_t stream) {
   (void)counts;
   int rc = check_dims(dims);
   if (rc) return rc;
@@ -555,6 +558,10 @@ int moe_lora_grouped_mlp_bwd(const moe_dims* dims, const moe_bf16* dYp, const mo
   MOE_CHECK_PTR(dXp); MOE_CHECK_PTR(dw_rows);
   MOE_CHECK_PTR(dA_gu); MOE_CHECK_PTR(dB_gu); MOE_CHECK_PTR(dA_dn); MOE_CHECK_PTR(dB_dn);
   MOE_CHECK_PTR(ws);
+  if (dW_gu) MOE_CHECK_PTR(dW_gu);
+  if (dW_dn) MOE_CHECK_PTR(dW_dn);
+  if ((dW_gu || dW_dn) && (Xp == nullptr || dYp == nullptr))
+    return fail(MOE_ERR_UNSUPPORTED, "full weight gradients need the permuted rows Xp and dYp");
   if (!offsets || !tile_off || !sorted_src || !topk_w)
     return fail(MOE_ERR_INVALID_ARG, "NULL routing pointer");
   const BwdWs w = bwd_layout(dims, ws);
@@ -613,6 +620,21 @@ int moe_lora_grouped_mlp_bwd(const moe_dims* dims, const moe_bf16* dYp, const mo
     p.fout = j.out; p.fstride = static_cast<int64_t>(j.M) * r; p.transpose_out = j.transpose;
     return run_gemm({128, true, true, Epi::kWgrad}, p, R, st->num_sms, ss, j.name);
   };
+  // full fine-tuning: per-group sum over the group's rows of A^T B with A a
+  // hi/lo pair [2, N, M] (two K passes) and B one wide bf16 row matrix [N, Nb];
+  // out [G, M, Nb] fp32, or [G, Nb, M] when transposed
+  auto wgrad_full = [&](const moe_bf16* a_pair, int M, const moe_bf16* bmat, int Nb, float* out,
+                        int transpose, const char* name, cudaStream_t ss) -> int {
+    GemmParams p = base;
+    MAP2(p.sl[0].a, a_pair, N, M, 64, 64);
+    MAP2(p.sl[1].a, a_pair + N * static_cast<int64_t>(M), N, M, 64, 64);
+    p.nslices = 2;
+    MAP2(p.wb_hi, bmat, N, Nb, 64, 64);
+    p.wb_lo = p.wb_hi;
+    p.M = M; p.N = Nb; p.n_ntiles = (M + 127) / 128; p.n_btiles = (Nb + 255) / 256;
+    p.fout = out; p.fstride = static_cast<int64_t>(M) * Nb; p.transpose_out = transpose;
+    return run_gemm({256, true, true, Epi::kWgradFull}, p, R, st->num_sms, ss, name);
+  };
   std::lock_guard<std::mutex> aux_lock(st->aux_mu);
   cudaStream_t aux = nullptr;
   if ((rc = aux_stream(st, &aux))) return rc;
@@ -627,6 +649,8 @@ int moe_lora_grouped_mlp_bwd(const moe_dims* dims, const moe_bf16* dYp, const mo
   if ((rc = stream_dep(st->ev[0], s, aux))) return rc;
   if ((rc = wgrad(jobs[0], aux))) return rc;  // dB_dn
   if ((rc = wgrad(jobs[1], aux))) return rc;  // dA_dn
+  // dW_dn[g] = sum_p dO_p^T act_p = sum_p dYp_p^T act'_p (act' carries w): [f, d] -> [d, f]
+  if (dW_dn && (rc = wgrad_full(act, f, dYp, d, dW_dn, 1, "dW_dn", aux))) return rc;
   {  // g = dYp W_dn + us A_dn ; SwiGLU backward from fp32 h -> dh pair ; dw partials
     GemmParams p = base;
     SLICE_ROWS(p, 0, dYp, dY, d, MAP3(p.sl[0].b, W_dn, G, d, f, 64, 64), d);
@@ -645,6 +669,8 @@ int moe_lora_grouped_mlp_bwd(const moe_dims* dims, const moe_bf16* dYp, const mo
     if (e != cudaSuccess) return cuda_fail(e, "dw reduce");
   }
   if ((rc = wgrad(jobs[2], aux))) return rc;  // dB_gu
+  // dW_gu[g] = sum_p dh_p^T Xp_p: [2f, d]
+  if (dW_gu && (rc = wgrad_full(w.dh, 2 * f, Xp, d, dW_gu, 0, "dW_gu", aux))) return rc;
   {  // v = dh B_gu (dh = hi + lo) -> vs pair = s*v
     GemmParams p = base;
     SLICE(p, 0, w.dh, N, 2 * f, MAP3(p.sl[0].b, B_gu, G, 2 * f, r, 64, 64), 2 * f);

@@ -228,9 +228,12 @@ __device__ __forceinline__ TileInfo tile_info(const GemmParams& p, int t, const 
     }
     ti.nkb = 0;
   } else {
-    ti.g = t / p.n_ntiles;
-    ti.mt = t - ti.g * p.n_ntiles;
-    ti.nt = 0;
+    // tile t = (group * M tiles + mt) * N tiles + nt
+    const int per_g = p.n_ntiles * p.n_btiles;
+    ti.g = t / per_g;
+    const int rem = t - ti.g * per_g;
+    ti.mt = rem / p.n_btiles;
+    ti.nt = rem - ti.mt * p.n_btiles;
     ti.row0 = __ldg(p.offsets + ti.g);
     ti.nvalid = __ldg(p.offsets + ti.g + 1) - ti.row0;
     ti.nkb = (ti.nvalid + BK - 1) / BK;
@@ -503,6 +506,51 @@ __device__ __forceinline__ void epi_wgrad(const GemmParams& p, const TileInfo& t
   }
 }
 
+// Full weight gradient: fout[g] (+ m * N + n, or + n * M + m when
+// transposed) = acc, this warp's rows m0 + [0,32) and columns
+// nt*BN + hf*BN/2 + [0, BN/2).  A group without rows writes zeros.
+template <int BN>
+__device__ __forceinline__ void epi_wgrad_full(const GemmParams& p, const TileInfo& ti,
+                                               uint32_t tq, int hf, int q, int lane,
+                                               uint32_t stg) {
+  const int m0 = ti.mt * BM + q * 32;
+  const int m = m0 + lane;
+  const bool has = ti.nk > 0;
+  float* fo = p.fout + static_cast<int64_t>(ti.g) * p.fstride;
+  const int nbase = ti.nt * BN + hf * (BN / 2);
+#pragma unroll 1
+  for (int c0 = 0; c0 < BN / 2; c0 += 32) {
+    float v[32];
+    if (has) {
+      tmem_ld16(tq + hf * (BN / 2) + c0, *reinterpret_cast<float(*)[16]>(v));
+      tmem_ld16(tq + hf * (BN / 2) + c0 + 16, *reinterpret_cast<float(*)[16]>(v + 16));
+    } else {
+#pragma unroll
+      for (int i = 0; i < 32; ++i) v[i] = 0.f;
+    }
+    const int n0 = nbase + c0;
+    if (p.transpose_out) {
+      // fout[g][n][m]: consecutive lanes write consecutive m (128-byte lines)
+      if (m < p.M) {
+#pragma unroll
+        for (int i = 0; i < 32; ++i)
+          if (n0 + i < p.N) fo[static_cast<int64_t>(n0 + i) * p.M + m] = v[i];
+      }
+    } else {
+      // fout[g][m][n]: stage the warp's 32 rows x 32 columns, store whole lines
+#pragma unroll
+      for (int c = 0; c < 8; ++c)
+        sts128(stg_at(stg, lane, c), f4_as_u4(v[4 * c], v[4 * c + 1], v[4 * c + 2], v[4 * c + 3]));
+      __syncwarp();
+      Planes pl{reinterpret_cast<char*>(fo + static_cast<int64_t>(m0) * p.N + n0), nullptr,
+                nullptr, nullptr, static_cast<int64_t>(p.N) * 4, 3, 1,
+                clamp_bytes(static_cast<int64_t>(p.N - n0) * 4, 128), p.M - m0};
+      stg_flush(stg, lane, pl);
+      __syncwarp();
+    }
+  }
+}
+
 template <int BN, bool B_MN, bool WGRAD, int EPI>
 __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant__ GemmParams p) {
   using C = Cfg<BN>;
@@ -564,7 +612,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
   const uint32_t tmem_base = *tmem_slot;
 
   const int num_tiles =
-      WGRAD ? p.G * p.n_ntiles : min(__ldg(p.tile_off + p.G) * p.n_ntiles, p.max_tiles);
+      WGRAD ? p.G * p.n_ntiles * p.n_btiles
+            : min(__ldg(p.tile_off + p.G) * p.n_ntiles, p.max_tiles);
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
@@ -636,8 +685,15 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
                 tma_load_2d(sa, &p.sl[s].a, fb, ti.mt * BM, row);
                 tma_load_2d(sa + kChunkBytes, &p.sl[s].a, fb, ti.mt * BM + 64, row);
               }
-              tma_load_2d(sb, &p.wb_hi, fb, 0, row);
-              tma_load_2d(sb + kChunkBytes, &p.wb_lo, fb, 0, row);
+              if constexpr (EPI == static_cast<int>(Epi::kWgradFull)) {
+                // B = one wide row matrix: this tile's BN columns as 64-column chunks
+#pragma unroll
+                for (int c = 0; c < BN / 64; ++c)
+                  tma_load_2d(sb + c * kChunkBytes, &p.wb_hi, fb, ti.nt * BN + c * 64, row);
+              } else {
+                tma_load_2d(sb, &p.wb_hi, fb, 0, row);
+                tma_load_2d(sb + kChunkBytes, &p.wb_lo, fb, 0, row);
+              }
             }
           }
         }
@@ -734,11 +790,14 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
           const int tail = ti.nvalid - b * BK;
           if (tail < BK) {
             // rows [tail, 64) of this block belong to the next group (or lie
-            // past the buffer): zero them in the A and B tiles (4 chunks)
-            const int n = (BK - tail) * 32;
+            // past the buffer): zero them in the A tile (2 chunks) and, for
+            // the LoRA gradients, in the B tile too; with zero A rows the
+            // wide B tile's extra rows (finite data) add nothing
+            constexpr int kPieces = EPI == static_cast<int>(Epi::kWgradFull) ? 16 : 32;
+            const int n = (BK - tail) * kPieces;
             for (int i = lane; i < n; i += 32) {
-              const int line = tail + (i >> 5);
-              const int piece = i & 31;
+              const int line = tail + i / kPieces;
+              const int piece = i % kPieces;
               const uint32_t base = (piece >> 4) ? sb : sa;
               sts128(base + ((piece >> 3) & 1) * kChunkBytes + line * 128 + (piece & 7) * 16,
                      make_uint4(0, 0, 0, 0));
@@ -803,7 +862,9 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
       // 128-row tile runs past the group's end and is not stored)
       const int64_t row0 = static_cast<int64_t>(ti.row0) + q * 32;
       const int nrows = WGRAD ? 32 : max(0, min(32, ti.nvalid - q * 32));
-      if constexpr (WGRAD) {
+      if constexpr (EPI == static_cast<int>(Epi::kWgradFull)) {
+        epi_wgrad_full<BN>(p, ti, tq, hf, q, lane, stg);
+      } else if constexpr (WGRAD) {
         epi_wgrad(p, ti, tq, hf, q, lane, stg);
       } else if constexpr (EPI == static_cast<int>(Epi::kSwiGLU)) {
         epi_swiglu<BN>(p, ti, tq, hf, row0, nrows, lane, stg);
@@ -836,7 +897,7 @@ cudaError_t launch_one(const GemmParams& p, int num_sms, cudaStream_t s) {
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            static_cast<int>(C::kSmemBytes));
   if (e != cudaSuccess) return e;
-  const int tiles = WGRAD ? p.G * p.n_ntiles : p.max_tiles;
+  const int tiles = WGRAD ? p.G * p.n_ntiles * p.n_btiles : p.max_tiles;
   const int grid = tiles < num_sms ? (tiles > 0 ? tiles : 1) : num_sms;
   return launch_pdl(kern, dim3(grid), dim3(kThreads), C::kSmemBytes, s, p);
 }
@@ -852,7 +913,10 @@ cudaError_t launch_gemm(const GemmShape& sh, const GemmParams& p, int num_sms, c
   const int e = static_cast<int>(sh.epi);
   if (p.nslices < 1 || p.nslices > kMaxSlices) return cudaErrorInvalidValue;
   if (sh.wgrad) {
+    if (p.n_btiles < 1) return cudaErrorInvalidValue;
     if (sh.BN == 128 && e == kWg) return launch_one<128, true, true, kWg>(p, num_sms, s);
+    if (sh.BN == 256 && e == static_cast<int>(Epi::kWgradFull))
+      return launch_one<256, true, true, static_cast<int>(Epi::kWgradFull)>(p, num_sms, s);
     return cudaErrorInvalidValue;
   }
   if (sh.BN == 256 && !sh.b_mn) {

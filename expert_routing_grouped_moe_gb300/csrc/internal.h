@@ -81,6 +81,7 @@ enum class Epi : int {
   kLoRA = 3,     // out0 = s*acc as a hi/lo pair
   kDgradDn = 4,  // SwiGLU backward from fp32 h (fin): dh pair (out0), dw partial (fout)
   kWgrad = 5,    // fp32 per-group weight gradient: acc[:, n] + acc[:, 64 + n]
+  kWgradFull = 6,  // fp32 per-group full weight gradient: acc (B = one wide matrix)
 };
 
 constexpr int kMaxSlices = 4;
@@ -107,6 +108,7 @@ struct GemmParams {
   int N;              // valid output columns (rows mode) / LoRA rank r (wgrad)
   int M;              // wgrad: rows of the weight gradient (d, f or 2f)
   int n_ntiles;       // N tiles per M tile (rows mode) / M tiles per group (wgrad)
+  int n_btiles;       // wgrad: N tiles over the B matrix's columns (1 for the LoRA gradients)
   int b_split;        // rows offset of the second B half (gate/up pairing), 0 = none
   int G, k, K;        // groups, top-k, slots per token
   float scale;        // LoRA scale s

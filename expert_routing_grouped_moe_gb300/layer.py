@@ -27,8 +27,14 @@ LAUNCHES_BWD = 11
 
 class MoELoRALayer:
     def __init__(self, T, d, f, E, k, r, alpha, weights: dict, shared_expert=False,
-                 device="cuda", gather=False):
+                 device="cuda", gather=False, full_grads=False):
+        """full_grads: the backward also returns dW_gu [G,2f,d] and dW_dn
+        [G,d,f] (fp32 gradients of the expert weights, for full fine-tuning;
+        needs the permuted-row mode)."""
+        if full_grads and gather:
+            raise ValueError("full weight gradients need the permuted-row mode (gather=False)")
         self.gather = bool(gather)
+        self.full_grads = bool(full_grads)
         self.dims = L.make_dims(T, d, f, E, k, r, alpha / r, shared_expert)
         self.T, self.d, self.f, self.E, self.k, self.r = T, d, f, E, k, r
         self.shared = bool(shared_expert)
@@ -66,6 +72,9 @@ class MoELoRALayer:
             "dA_gu": torch.empty(G, r, d, **f32), "dB_gu": torch.empty(G, 2 * f, r, **f32),
             "dA_dn": torch.empty(G, r, f, **f32), "dB_dn": torch.empty(G, d, r, **f32),
         }
+        if self.full_grads:
+            self.grads["dW_gu"] = torch.empty(G, 2 * f, d, **f32)
+            self.grads["dW_dn"] = torch.empty(G, d, f, **f32)
         self.bwd_ws = torch.empty(L.moe_mlp_bwd_workspace_size(self.dims), dtype=torch.uint8,
                                   device=dev)
         self._ids = None
@@ -73,7 +82,8 @@ class MoELoRALayer:
 
     def launches_per_step(self):
         """Kernel launches of one forward + backward in this layer's mode."""
-        return LAUNCHES_FWD + LAUNCHES_BWD - (2 if self.gather else 0)
+        return (LAUNCHES_FWD + LAUNCHES_BWD - (2 if self.gather else 0)
+                + (2 if self.full_grads else 0))
 
     # ------------------------------------------------------------------ steps
     def route(self, ids, stream=None):
@@ -110,7 +120,7 @@ class MoELoRALayer:
                                    w["A_gu"], w["B_gu"], w["W_dn"], w["A_dn"], w["B_dn"], self.h,
                                    self.act, self.xa_gu, self.xa_dn, self.dXp, self.dw_rows,
                                    g["dA_gu"], g["dB_gu"], g["dA_dn"], g["dB_dn"], self.bwd_ws,
-                                   stream)
+                                   stream, dW_gu=g.get("dW_gu"), dW_dn=g.get("dW_dn"))
         L.moe_unpermute_combine(self.dXp, self.dest_pos, self.k, self.shared, self.dX,
                                 row_scalars=self.dw_rows, slot_out=self.dw, stream=stream)
         return {"dX": self.dX, "dw": self.dw, **g}

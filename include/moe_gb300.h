@@ -244,9 +244,16 @@ MOE_API size_t moe_mlp_bwd_workspace_size(const moe_dims* dims);
  *              (act_p unscaled; the saved act and xa_dn already carry w_p)
  *   dB_gu[g] = s sum_p dh^T xa             [G,2f,r] fp32
  *   dA_gu[g] = s sum_p v^T Xp              [G,r,d] fp32
+ * Full fine-tuning (optional; the Faster MoE docs' introduction: the kernels
+ * serve full fine-tuning as well as LoRA): with dW_gu and/or dW_dn non-NULL
+ * the call also writes the gradients of the expert weights themselves,
+ *   dW_dn[g] = sum_p dO^T act_p = sum_p dYp^T act   [G,d,f]  fp32
+ *   dW_gu[g] = sum_p dh^T Xp                        [G,2f,d] fp32
+ * (act and dh as hi/lo pairs, so the sums keep ~16-bit terms).  They need the
+ * permuted rows (Xp and dYp non-NULL), else MOE_ERR_UNSUPPORTED.
  * Gradients are overwritten (not accumulated); groups with no rows get zeros.
  * ws: >= moe_mlp_bwd_workspace_size bytes of device scratch, 16-byte aligned.
- * The four weight-gradient GEMMs run on a second stream that the library
+ * The weight-gradient GEMMs run on a second stream that the library
  * creates once per device (no device memory); it forks from `stream` after
  * their inputs exist and joins back before the call returns, so all results
  * are ordered on `stream` as if everything ran there.  Calls from several host
@@ -262,6 +269,7 @@ MOE_API int moe_lora_grouped_mlp_bwd(const moe_dims* dims, const moe_bf16* dYp,
                              const moe_bf16* xa_gu, const moe_bf16* xa_dn,
                              moe_bf16* dXp, float* dw_rows,
                              float* dA_gu, float* dB_gu, float* dA_dn, float* dB_dn,
+                             float* dW_gu, float* dW_dn,
                              void* ws, size_t ws_bytes, moe_stream_t stream);
 
 /* ------------------------------------------------------------------------ */

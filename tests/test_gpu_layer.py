@@ -40,9 +40,9 @@ def make_inputs(cfg, seed, ids=None, w=None):
     return wts, act, ids_np, w_np
 
 
-def run(cfg, wts, act, ids_np, w_np, gather=False):
+def run(cfg, wts, act, ids_np, w_np, gather=False, full=False):
     layer = MoELoRALayer(cfg.T, cfg.d, cfg.f, cfg.E, cfg.k, cfg.r, cfg.alpha, wts,
-                         shared_expert=cfg.shared, device=DEV, gather=gather)
+                         shared_expert=cfg.shared, device=DEV, gather=gather, full_grads=full)
     ids = torch.from_numpy(np.ascontiguousarray(ids_np, dtype=np.int32)).to(DEV)
     w = torch.from_numpy(np.ascontiguousarray(w_np, dtype=np.float32)).to(DEV)
     Y = layer.forward(act["X"], ids, w).clone()
@@ -109,6 +109,40 @@ def test_layer_full_parity(name, gather):
     assert_close_bf16(g["dw"].cpu().numpy(), gr["dw"], "dw")
     for n in ("dA_gu", "dB_gu", "dA_dn", "dB_dn"):
         assert_close_bf16(g[n].cpu().numpy(), gr[n], n)
+
+
+@pytest.mark.parametrize("name", list(SMALL))
+def test_full_weight_gradients_parity(name):
+    """Full fine-tuning: dW_gu and dW_dn of every group against the oracle,
+    next to unchanged LoRA gradients and dX."""
+    cfg = SMALL[name]
+    wts, act, ids_np, w_np = make_inputs(cfg, seed=17)
+    layer, Y, g = run(cfg, wts, act, ids_np, w_np, full=True)
+    P = oracle_params(wts, cfg)
+    X, dY = to64(act["X"]), to64(act["dY"])
+    gr = oracle.layer_backward(X, ids_np, w_np, dY, P, full=True)
+    for n in ("dW_gu", "dW_dn", "dA_gu", "dB_gu", "dA_dn", "dB_dn"):
+        assert_close_bf16(g[n].cpu().numpy(), gr[n], n)
+    assert_close_bf16(to64(g["dX"]), gr["dX"], "dX")
+    counts = np.bincount(ids_np.reshape(-1), minlength=cfg.E)
+    for e in np.nonzero(counts == 0)[0]:
+        assert np.all(g["dW_gu"][e].cpu().numpy() == 0) and np.all(g["dW_dn"][e].cpu().numpy() == 0)
+
+
+def test_full_weight_gradients_sampled_full_size():
+    """dW_gu / dW_dn at the Qwen3-shaped size: the largest and the smallest
+    expert, against the per-expert oracle."""
+    cfg = synth.CONFIGS["qwen3_30b_a3b"]
+    wts, act, ids_np, w_np = make_inputs(cfg, seed=1)
+    layer, Y, g = run(cfg, wts, act, ids_np, w_np, full=True)
+    counts = np.bincount(ids_np.reshape(-1), minlength=cfg.E)
+    groups = [int(np.argmax(counts)), int(np.argmin(counts))]
+    P = oracle_params(wts, cfg, groups=groups)
+    X, dY = to64(act["X"]), to64(act["dY"])
+    for gi in groups:
+        ref = oracle.expert_lora_grads(gi, X, ids_np, w_np, dY, P, full=True)
+        for n in ("dW_gu", "dW_dn"):
+            assert_close_bf16(g[n][gi].cpu().numpy(), ref[n], "%s[g%d]" % (n, gi))
 
 
 EDGE = {

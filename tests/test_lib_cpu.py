@@ -86,6 +86,19 @@ def test_fwd_argument_errors_before_launch(lib):
     assert b"W_gu" in lib.moe_last_error()
 
 
+def test_bwd_full_gradients_need_permuted_rows(lib):
+    from expert_routing_grouped_moe_gb300 import _lib
+    P = ctypes.c_void_p
+    fake = P(1 << 20)  # never dereferenced: checks fail first
+    d = _dims()
+    # dYp = NULL (gathered dY) with dW_gu requested: dYp, dY, Xp, X, then
+    # counts .. dB_dn (21 pointers), dW_gu, dW_dn, ws
+    args = [None, fake, fake, None] + [fake] * 21 + [fake, None] + [fake]
+    rc = lib.moe_lora_grouped_mlp_bwd(ctypes.byref(d), *args, 1 << 40, None)
+    assert rc == _lib.MOE_ERR_UNSUPPORTED
+    assert b"permuted rows" in lib.moe_last_error()
+
+
 def test_route_argument_errors_before_launch(lib):
     from expert_routing_grouped_moe_gb300 import _lib
     P = ctypes.c_void_p
