@@ -54,6 +54,8 @@ def parse_args(argv=None):
     ap.add_argument("--cpu-budget-s", type=float, default=20.0)
     ap.add_argument("--probe-steps", type=int, default=100)
     ap.add_argument("--no-route-sweep", action="store_true")
+    ap.add_argument("--full-grads", action="store_true",
+                    help="also compute the full weight gradients dW_gu, dW_dn each step")
     ap.add_argument("--route-only", action="store_true",
                     help="time only moe_route on the routing sweep points")
     return ap.parse_args(argv)
@@ -61,11 +63,12 @@ def parse_args(argv=None):
 
 # ---------------------------------------------------------------- work model
 
-def layer_counts(cfg):
+def layer_counts(cfg, full_grads=False):
     """Algorithmic work of one fwd+bwd step (split-LoRA counts; the dense
     merged work is not counted) and, per kernel launch, its FLOPs and the
     bytes it must move at least: each input read once, each output written
-    once, in the stored precisions (bf16 rows, hi/lo bf16 pairs, fp32 h)."""
+    once, in the stored precisions (bf16 rows, hi/lo bf16 pairs, fp32 h).
+    full_grads adds the full weight gradients dW_gu and dW_dn."""
     T, d, f, r, k = cfg.T, cfg.d, cfg.f, cfg.r, cfg.k
     N = cfg.rows                                   # routed rows (+ shared rows)
     G = cfg.groups
@@ -97,14 +100,19 @@ def layer_counts(cfg):
         "combine": (0, 2 * N * d + 2 * T * d + 8 * N + 4 * T * k),
         "dw_reduce": (0, 4 * N * nparts + 4 * N),
     }
-    return {"flops": 2 * F_base + 3 * F_lora, "F_base": F_base, "F_lora": F_lora, "kernels": kern,
-            "launches": {"permute": 2, "combine": 2}}
+    F_full = 0
+    if full_grads:
+        kern["dW_gu"] = (2 * N * 2 * f * d, 2 * pair_f + rows_d + 4 * G * 2 * f * d)
+        kern["dW_dn"] = (2 * N * d * f, pair_f + rows_d + 4 * G * d * f)
+        F_full = 2 * N * 2 * f * d + 2 * N * d * f
+    return {"flops": 2 * F_base + 3 * F_lora + F_full, "F_base": F_base, "F_lora": F_lora,
+            "F_full": F_full, "kernels": kern, "launches": {"permute": 2, "combine": 2}}
 
 
 # Kernels the backward runs on the library's second stream, beside the dgrad
 # chain.  Their event-timed durations include time queued behind the main
 # stream's kernels, so they are not roofline candidates.
-AUX_STREAM_KERNELS = ("dB_dn", "dA_dn", "dw_reduce", "dB_gu", "dA_gu")
+AUX_STREAM_KERNELS = ("dB_dn", "dA_dn", "dw_reduce", "dB_gu", "dA_gu", "dW_dn", "dW_gu")
 
 
 def kernel_roofline(name, flops, nbytes, dur_s, peaks):
@@ -447,7 +455,7 @@ def run_ours(args):
     topw = torch.empty(cfg.T, cfg.k, dtype=torch.float32, device=dev)
     L.moe_router_topk(act["logits"], cfg.k, ids, topw)
     layer = MoELoRALayer(cfg.T, cfg.d, cfg.f, cfg.E, cfg.k, cfg.r, cfg.alpha, weights,
-                         shared_expert=cfg.shared, device=dev)
+                         shared_expert=cfg.shared, device=dev, full_grads=args.full_grads)
     X, dY = act["X"], act["dY"]
     stream = torch.cuda.current_stream()
 
@@ -457,7 +465,7 @@ def run_ours(args):
     if L.moe_status() != L.MOE_OK:
         raise SystemExit("device status error after warm-up")
 
-    counts = layer_counts(cfg)
+    counts = layer_counts(cfg, full_grads=args.full_grads)
     names = L.kernel_names()
 
     sampler = ClockSampler(gpu_uuid(torch, dev))
@@ -565,7 +573,9 @@ def run_ours(args):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_max,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic (seeded; random-init weights of the layer shape)",
-        "config": {"workload": "%s-shaped MoE-LoRA layer fwd+bwd" % cfg.name, "T": cfg.T,
+        "config": {"workload": "%s-shaped MoE-LoRA layer fwd+bwd%s" % (
+                       cfg.name, " with full weight gradients" if args.full_grads else ""),
+                   "T": cfg.T,
                    "d": cfg.d, "f": cfg.f, "E": cfg.E, "k": cfg.k, "r": cfg.r,
                    "alpha": cfg.alpha, "shared_expert": cfg.shared,
                    "global_batch_tokens": world * cfg.T, "parallelism": "replicas x%d" % world,
@@ -614,12 +624,12 @@ def run_reference(args):
     for _ in range(args.warmup):
         sel = rng.choice(cfg.T, size=ntok, replace=False)
         oracle.layer_forward(X[sel], ids[sel], w[sel], P)
-        oracle.layer_backward(X[sel], ids[sel], w[sel], dY[sel], P)
+        oracle.layer_backward(X[sel], ids[sel], w[sel], dY[sel], P, full=args.full_grads)
     t0 = time.perf_counter()
     for _ in range(args.steps):
         sel = rng.choice(cfg.T, size=ntok, replace=False)
         oracle.layer_forward(X[sel], ids[sel], w[sel], P)
-        oracle.layer_backward(X[sel], ids[sel], w[sel], dY[sel], P)
+        oracle.layer_backward(X[sel], ids[sel], w[sel], dY[sel], P, full=args.full_grads)
     dt = time.perf_counter() - t0
     value = args.steps * ntok / dt
     sample = ("each step: oracle fp64 forward+backward of %d random tokens of the %d-token "
@@ -629,7 +639,9 @@ def run_reference(args):
         "n_gpus": int(os.environ.get("WORLD_SIZE", "1")), "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": "%s-shaped MoE-LoRA layer fwd+bwd" % cfg.name, "T": cfg.T,
+        "config": {"workload": "%s-shaped MoE-LoRA layer fwd+bwd%s" % (
+                       cfg.name, " with full weight gradients" if args.full_grads else ""),
+                   "T": cfg.T,
                    "d": cfg.d, "f": cfg.f, "E": cfg.E, "k": cfg.k, "r": cfg.r},
         "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cpu_cores(),
                          "kind": "oracle", "sample": sample},
