@@ -365,10 +365,17 @@ __device__ __forceinline__ void epi_dgrad_dn(const GemmParams& p, const TileInfo
   };
   const int jbase = ti.nt * BN + hf * (BN / 2);
   float dot = 0.f;
+  // g of the next chunk is loaded from TMEM while this chunk is computed
+  uint32_t tr[16];
+  tmem_ld16_issue(tq + hf * (BN / 2), tr);
   // one 16-column chunk: h from the staging tile, g from TMEM, dh pair out
   auto process = [&](int sub) {
     const int j0 = jbase + sub * 16;
     float gt[16], up[16], gr[16];
+    tmem_ld_wait16(tr);
+#pragma unroll
+    for (int i = 0; i < 16; ++i) gr[i] = __uint_as_float(tr[i]);
+    if (sub + 1 < kSubs) tmem_ld16_issue(tq + hf * (BN / 2) + (sub + 1) * 16, tr);
 #pragma unroll
     for (int c = 0; c < 4; ++c) {
       const uint4 x = lds128(stg_at(stg, lane, c));
@@ -378,7 +385,6 @@ __device__ __forceinline__ void epi_dgrad_dn(const GemmParams& p, const TileInfo
       up[4 * c] = __uint_as_float(y.x); up[4 * c + 1] = __uint_as_float(y.y);
       up[4 * c + 2] = __uint_as_float(y.z); up[4 * c + 3] = __uint_as_float(y.w);
     }
-    tmem_ld16(tq + hf * (BN / 2) + sub * 16, gr);
     float dg[16], du[16];
 #pragma unroll
     for (int i = 0; i < 16; ++i) {
