@@ -1,7 +1,6 @@
 // Row permute (gather into expert-grouped sorted order) and combine
-// (gather-reduce back to token order).  Both are pure HBM streams: one warp
-// moves a row as 16-byte vectors, all of a row's loads issued before its
-// stores.
+// (gather-reduce back to token order).  Both are pure HBM streams moving rows
+// as 16-byte vectors, many loads in flight per lane before any store.
 //
 // Permute is step 5 of the routing pass in the Unsloth x NVIDIA article,
 // section "Optimisation 3" (slice the token list by offsets): permuted row p
@@ -19,35 +18,39 @@
 namespace moe {
 namespace {
 
-// One warp per token: the token's row is read once and written to the
-// permuted rows of its K slots, dst[dest_pos[t*K + j]] = src[t].  Reading each
-// source row once keeps the traffic at T*d + N*d elements even when X does not
-// fit in L2.
+// Each warp moves one 512-column block (64 16-byte vectors, two per lane) of
+// one token's row to the permuted rows of its K slots,
+// dst[dest_pos[t*K + j]] = src[t]: the row is read once, and splitting rows
+// into blocks puts all of a lane's loads in flight at once and gives small
+// batches enough warps.
+constexpr int kBlockVecs = 64;  // 16-byte vectors per warp block (512 bf16)
+
 __global__ void __launch_bounds__(256) permute_kernel(const uint4* __restrict__ src, int T,
                                                      int d8, int K,
                                                      const int32_t* __restrict__ dest_pos,
                                                      uint4* __restrict__ dst) {
   pdl_wait();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int t = blockIdx.x * 8 + warp;
-  if (t >= T) return;
+  const int nb = (d8 + kBlockVecs - 1) / kBlockVecs;
+  const int64_t wid = static_cast<int64_t>(blockIdx.x) * 8 + warp;
+  if (wid >= static_cast<int64_t>(T) * nb) return;
+  const int t = static_cast<int>(wid / nb);
+  const int v0 = static_cast<int>(wid - static_cast<int64_t>(t) * nb) * kBlockVecs + lane;
   const uint4* srow = src + static_cast<int64_t>(t) * d8;
-  for (int v0 = 0; v0 < d8; v0 += 256) {
-    uint4 x[8];
+  uint4 x[2];
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      const int v = v0 + i * 32 + lane;
-      x[i] = v < d8 ? __ldg(srow + v) : make_uint4(0, 0, 0, 0);
-    }
-    for (int j = 0; j < K; ++j) {
-      const int p = __ldg(dest_pos + static_cast<int64_t>(t) * K + j);
-      if (p < 0) continue;
-      uint4* drow = dst + static_cast<int64_t>(p) * d8;
+  for (int i = 0; i < 2; ++i) {
+    const int v = v0 + i * 32;
+    x[i] = v < d8 ? __ldg(srow + v) : make_uint4(0, 0, 0, 0);
+  }
+  for (int j = 0; j < K; ++j) {
+    const int p = __ldg(dest_pos + static_cast<int64_t>(t) * K + j);
+    if (p < 0) continue;
+    uint4* drow = dst + static_cast<int64_t>(p) * d8;
 #pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        const int v = v0 + i * 32 + lane;
-        if (v < d8) drow[v] = x[i];
-      }
+    for (int i = 0; i < 2; ++i) {
+      const int v = v0 + i * 32;
+      if (v < d8) drow[v] = x[i];
     }
   }
 }
@@ -70,6 +73,8 @@ __device__ __forceinline__ uint32_t pack2(float lo, float hi) {
 constexpr int kMaxSlots = 33;
 
 // One warp per token, 8 tokens per CTA.  Row of slot j = dest_pos[t*K + j].
+// Two column slots per lane and up to 8 slots' rows per step: 16 loads in
+// flight per lane, summed in fp32 in slot order.
 __global__ void __launch_bounds__(256) combine_kernel(
     const uint4* __restrict__ rows, const int32_t* __restrict__ dest_pos, int T, int d8, int k,
     int shared, const float* __restrict__ weights, const float* __restrict__ row_scalars,
@@ -83,34 +88,48 @@ __global__ void __launch_bounds__(256) combine_kernel(
   const int K = k + shared;
   for (int j = lane; j < K; j += 32) {
     const int dp = __ldg(dest_pos + static_cast<int64_t>(t) * K + j);
-    float c = 0.f;
-    if (dp >= 0)
-      c = (weights != nullptr && j < k) ? __ldg(weights + static_cast<int64_t>(t) * k + j) : 1.f;
+    const float wj =
+        (weights != nullptr && j < k) ? __ldg(weights + static_cast<int64_t>(t) * k + j) : 1.f;
     s_row[warp][j] = dp;
-    s_c[warp][j] = c;
+    s_c[warp][j] = dp >= 0 ? wj : 0.f;
     if (slot_out != nullptr && row_scalars != nullptr && j < k)
       slot_out[static_cast<int64_t>(t) * k + j] = dp >= 0 ? __ldg(row_scalars + dp) : 0.f;
   }
   __syncwarp();
   uint4* orow = out + static_cast<int64_t>(t) * d8;
-  // slot rows in groups of 8: all 8 loads of a group in flight at once
-  for (int v = lane; v < d8; v += 32) {
-    float a[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+  for (int v0 = lane; v0 < d8; v0 += 64) {
+    float a[2][8];
+#pragma unroll
+    for (int i = 0; i < 2; ++i)
+#pragma unroll
+      for (int e = 0; e < 8; ++e) a[i][e] = 0.f;
     for (int j0 = 0; j0 < K; j0 += 8) {
-      uint4 x[8];
+      uint4 x[8][2];
 #pragma unroll
       for (int jj = 0; jj < 8; ++jj) {
         const int j = j0 + jj;
         const int pr = j < K ? s_row[warp][j] : -1;
-        x[jj] = pr >= 0 ? __ldg(rows + static_cast<int64_t>(pr) * d8 + v)
-                        : make_uint4(0, 0, 0, 0);
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+          const int v = v0 + i * 32;
+          x[jj][i] = (pr >= 0 && v < d8) ? __ldg(rows + static_cast<int64_t>(pr) * d8 + v)
+                                         : make_uint4(0, 0, 0, 0);
+        }
       }
 #pragma unroll
       for (int jj = 0; jj < 8; ++jj)
-        if (j0 + jj < K) acc_bf16x8(a, x[jj], s_c[warp][j0 + jj]);
+        if (j0 + jj < K) {
+#pragma unroll
+          for (int i = 0; i < 2; ++i) acc_bf16x8(a[i], x[jj][i], s_c[warp][j0 + jj]);
+        }
     }
-    orow[v] = make_uint4(pack2(a[0], a[1]), pack2(a[2], a[3]), pack2(a[4], a[5]),
-                         pack2(a[6], a[7]));
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+      const int v = v0 + i * 32;
+      if (v < d8)
+        orow[v] = make_uint4(pack2(a[i][0], a[i][1]), pack2(a[i][2], a[i][3]),
+                             pack2(a[i][4], a[i][5]), pack2(a[i][6], a[i][7]));
+    }
   }
 }
 
@@ -130,7 +149,8 @@ __global__ void sum_parts_kernel(const float* __restrict__ parts, int nparts, in
 cudaError_t launch_permute(const uint16_t* src, int T, int d, int K, const int32_t* dest_pos,
                            uint16_t* dst, cudaStream_t s) {
   if (T == 0) return cudaSuccess;
-  return launch_pdl(permute_kernel, dim3((T + 7) / 8), dim3(256), 0, s,
+  const int64_t warps = static_cast<int64_t>(T) * ((d / 8 + kBlockVecs - 1) / kBlockVecs);
+  return launch_pdl(permute_kernel, dim3(static_cast<unsigned>((warps + 7) / 8)), dim3(256), 0, s,
                     reinterpret_cast<const uint4*>(src), T, d / 8, K, dest_pos,
                     reinterpret_cast<uint4*>(dst));
 }
