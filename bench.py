@@ -73,7 +73,7 @@ def layer_counts(cfg, full_grads=False):
     N = cfg.rows                                   # routed rows (+ shared rows)
     G = cfg.groups
     hs = 32 * ((f + 15) // 16)                     # fp32 h row: [gate 16 | up 16] chunks
-    nparts = 2 * ((f + 255) // 256)                # dw partial slices
+    nparts = 2 * ((f + 191) // 192)                # dw partial slices (192-feature tiles)
     F_base = 2 * N * d * 2 * f + 2 * N * f * d     # gate_up + down
     F_lora = 2 * N * (d * r + r * 2 * f + f * r + r * d)
     W_gu, W_dn = 2 * G * 2 * f * d, 2 * G * d * f

@@ -212,7 +212,7 @@ int record_error(int code, const char* msg) {
 }
 
 bool make_map_2d(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols,
-                 uint32_t box_rows, uint32_t box_cols) {
+                 uint32_t box_rows, uint32_t box_cols, bool swizzle128) {
   EncodeTiledFn fn = encode_fn();
   if (fn == nullptr) return false;
   const cuuint64_t dims[2] = {cols, rows};
@@ -220,7 +220,8 @@ bool make_map_2d(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols,
   const cuuint32_t box[2] = {box_cols, box_rows};
   const cuuint32_t es[2] = {1, 1};
   return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box,
-            es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+            swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
@@ -253,7 +254,7 @@ BwdWs bwd_layout(const moe_dims* dm, void* base) {
   const size_t P = static_cast<size_t>(dm->T) * static_cast<size_t>(K);  // routed rows N
   const size_t nr = align_up(2 * P * dm->r * 2);
   const size_t ndh = align_up(2 * P * 2 * static_cast<size_t>(dm->f) * 2);
-  const size_t nparts = static_cast<size_t>(kDwPartsPerTile) * ((dm->f + 255) / 256);
+  const size_t nparts = static_cast<size_t>(kDwPartsPerTile) * ((dm->f + kDgradBN - 1) / kDgradBN);
   const size_t ndw = align_up(nparts * P * 4);
   BwdWs w{};
   uint8_t* b = static_cast<uint8_t*>(base);
@@ -575,7 +576,7 @@ int moe_lora_grouped_mlp_bwd(const moe_dims* dims, const moe_bf16* dYp, const mo
   const int64_t R = max_row_tiles(dims->T, dims->k + dims->shared_expert, G);
   const GemmParams base = base_params(dims, offsets, tile_off, sorted_src, topk_w, st->status);
   cudaStream_t s = stream;
-  const int ntiles_f = (f + 255) / 256;
+  const int ntiles_f = (f + kDgradBN - 1) / kDgradBN;
   const int nparts = kDwPartsPerTile * ntiles_f;
 
   const int64_t Nr = N * r, N2f = N * 2 * f;
@@ -659,7 +660,11 @@ int moe_lora_grouped_mlp_bwd(const moe_dims* dims, const moe_bf16* dYp, const mo
     p.nslices = 3; p.N = f; p.n_ntiles = ntiles_f;
     p.fin = h; p.ldf = 32 * ((f + 15) / 16);
     p.out0 = w.dh; p.ld0 = 2 * f; p.pair = N2f; p.fout = w.dwp; p.fstride = N;
-    if ((rc = run_gemm({256, true, false, Epi::kDgradDn}, p, R, st->num_sms, s, "dgrad_dn")))
+    // dh planes as TMA store targets: 16 features x 32 rows per store
+    p.om_ok = make_map_2d(&p.om_hi, w.dh, N, 2 * f, 32, 16, false) &&
+              make_map_2d(&p.om_lo, w.dh + N2f, N, 2 * f, 32, 16, false);
+    if ((rc = run_gemm({kDgradBN, true, false, Epi::kDgradDn}, p, R, st->num_sms, s,
+                       "dgrad_dn")))
       return rc;
   }
   if ((rc = stream_dep(st->ev[1], s, aux))) return rc;

@@ -44,22 +44,36 @@ constexpr int kEpiWarps = 8;
 constexpr int kThreads = 64 + 32 * kEpiWarps;
 constexpr uint32_t kAStageBytes = BM * BK * 2;  // 16 KB
 constexpr uint32_t kChunkBytes = 64 * 128;      // one [64][64] bf16 swizzle block
-constexpr uint32_t kStgBytes = 32 * 128;        // staging tile per epilogue warp
-constexpr uint32_t kRingBytes = 192 * 1024;
+constexpr uint32_t kStgTileBytes = 32 * 128;    // one staging tile: 32 rows x 128 B
+constexpr uint32_t kRingMax = 192 * 1024;
+constexpr uint32_t kSmemMax = 232448;           // opt-in shared memory per CTA
 // Groups whose tile offsets are kept in shared memory (G + 1 <= kTileTabInts);
 // beyond that the tile scheduler searches tile_off in global memory.
 constexpr int kTileTabInts = 448;
+constexpr uint32_t kFixedSmem = 1024 /*alignment slack*/ + 256 /*barriers*/ +
+                                kTileTabInts * 4 /*tile_off copy*/;
 
-template <int BN>
+__host__ __device__ constexpr uint32_t pow2_at_least(uint32_t v) {
+  uint32_t p = 32;
+  while (p < v) p <<= 1;
+  return p;
+}
+
+template <int BN, int EPI>
 struct Cfg {
   static constexpr uint32_t kBStageBytes = BN * BK * 2;
   static constexpr uint32_t kStageBytes = kAStageBytes + kBStageBytes;
-  static constexpr int kStages = kRingBytes / kStageBytes;  // 4 / 6 / 8 for BN 256 / 128 / 64
-  static constexpr uint32_t kTmemCols = 2 * BN;              // power of two >= 32
-  static constexpr size_t kSmemBytes = 1024 /*alignment slack*/ +
-                                       static_cast<size_t>(kStages) * kStageBytes +
-                                       kEpiWarps * kStgBytes + 256 /*barriers*/ +
-                                       kTileTabInts * 4 /*tile_off copy*/;
+  // staging per epilogue warp: one tile, two for the SwiGLU backward (h in,
+  // dh out through TMA stores)
+  static constexpr uint32_t kStgBytes =
+      (EPI == static_cast<int>(Epi::kDgradDn) ? 2 : 1) * kStgTileBytes;
+  static constexpr uint32_t kRingFit =
+      (kSmemMax - kFixedSmem - kEpiWarps * kStgBytes) / kStageBytes * kStageBytes;
+  // 4 / 4 / 6 / 8 stages for BN 256 / 192 (dgrad) / 128 / 64
+  static constexpr int kStages = (kRingFit < kRingMax ? kRingFit : kRingMax) / kStageBytes;
+  static constexpr uint32_t kTmemCols = pow2_at_least(2 * BN);  // power of two >= 32
+  static constexpr size_t kSmemBytes =
+      kFixedSmem + static_cast<size_t>(kStages) * kStageBytes + kEpiWarps * kStgBytes;
 };
 
 // Group owning permuted M tile mt: the largest g with tile_off[g] <= mt
@@ -228,14 +242,14 @@ __device__ __forceinline__ TileInfo tile_info(const GemmParams& p, int t, const 
     }
     ti.nkb = 0;
   } else {
-    // tile t = (group * M tiles + mt) * N tiles + nt
+    // tile t = (group * M tiles + mt) * N tiles + nt; `tab` holds offsets here
     const int per_g = p.n_ntiles * p.n_btiles;
     ti.g = t / per_g;
     const int rem = t - ti.g * per_g;
     ti.mt = rem / p.n_btiles;
     ti.nt = rem - ti.mt * p.n_btiles;
-    ti.row0 = __ldg(p.offsets + ti.g);
-    ti.nvalid = __ldg(p.offsets + ti.g + 1) - ti.row0;
+    ti.row0 = tab ? tab[ti.g] : __ldg(p.offsets + ti.g);
+    ti.nvalid = (tab ? tab[ti.g + 1] : __ldg(p.offsets + ti.g + 1)) - ti.row0;
     ti.nkb = (ti.nvalid + BK - 1) / BK;
     ti.nk = ti.nkb * p.nslices;
   }
@@ -397,19 +411,48 @@ __device__ __forceinline__ void epi_dgrad_dn(const GemmParams& p, const TileInfo
       du[i] = da * sl;
     }
     __syncwarp();
-    uint4 a0, a1, b0, b1;
+    uint4 a0, a1, b0, b1, c0, c1, e0, e1;
     split8(dg, a0, b0);
     split8(dg + 8, a1, b1);
+    split8(du, c0, e0);
+    split8(du + 8, c1, e1);
+    if (p.om_ok && nrows == 32 && j0 + 16 <= f) {
+      // whole chunk: the four 32-row x 16-feature planes (dgate hi, dup hi,
+      // dgate lo, dup lo) go out as TMA stores from the second staging tile
+      const uint32_t ob = stg + kStgTileBytes;
+      if (lane == 0) bulk_wait_read_all();  // the previous chunk's stores have read ob
+      __syncwarp();
+      const uint32_t rb = ob + lane * 32;
+      sts128(rb, a0);
+      sts128(rb + 16, a1);
+      sts128(rb + 1024, c0);
+      sts128(rb + 1024 + 16, c1);
+      sts128(rb + 2048, b0);
+      sts128(rb + 2048 + 16, b1);
+      sts128(rb + 3072, e0);
+      sts128(rb + 3072 + 16, e1);
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) {
+        const int y = static_cast<int>(row0);
+        tma_store_2d(&p.om_hi, ob, j0, y);
+        tma_store_2d(&p.om_hi, ob + 1024, f + j0, y);
+        tma_store_2d(&p.om_lo, ob + 2048, j0, y);
+        tma_store_2d(&p.om_lo, ob + 3072, f + j0, y);
+        bulk_commit();
+      }
+      return;
+    }
+    // rows past the group's end or columns past f: masked stores through the
+    // staging tile
     sts128(stg_at(stg, lane, 0), a0);
     sts128(stg_at(stg, lane, 1), a1);
     sts128(stg_at(stg, lane, 2), b0);
     sts128(stg_at(stg, lane, 3), b1);
-    split8(du, a0, b0);
-    split8(du + 8, a1, b1);
-    sts128(stg_at(stg, lane, 4), a0);
-    sts128(stg_at(stg, lane, 5), a1);
-    sts128(stg_at(stg, lane, 6), b0);
-    sts128(stg_at(stg, lane, 7), b1);
+    sts128(stg_at(stg, lane, 4), c0);
+    sts128(stg_at(stg, lane, 5), c1);
+    sts128(stg_at(stg, lane, 6), e0);
+    sts128(stg_at(stg, lane, 7), e1);
     __syncwarp();
     Planes pl{reinterpret_cast<char*>(db + j0), reinterpret_cast<char*>(db + p.pair + j0),
               reinterpret_cast<char*>(db + f + j0),
@@ -559,7 +602,7 @@ __device__ __forceinline__ void epi_wgrad_full(const GemmParams& p, const TileIn
 
 template <int BN, bool B_MN, bool WGRAD, int EPI>
 __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant__ GemmParams p) {
-  using C = Cfg<BN>;
+  using C = Cfg<BN, EPI>;
   constexpr int S = C::kStages;
   extern __shared__ uint8_t smem_raw[];
   // 1024-byte aligned stage ring (128B swizzle atoms are 8 rows x 128 B)
@@ -567,15 +610,17 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
   uint8_t* smem = smem_raw + ((1024 - (raw_addr & 1023)) & 1023);
   uint8_t* ring = smem;
   uint8_t* stage_tiles = ring + S * C::kStageBytes;
-  uint64_t* full_bar = reinterpret_cast<uint64_t*>(stage_tiles + kEpiWarps * kStgBytes);
+  uint64_t* full_bar = reinterpret_cast<uint64_t*>(stage_tiles + kEpiWarps * C::kStgBytes);
   uint64_t* empty_bar = full_bar + S;
   uint64_t* tfull_bar = empty_bar + S;
   uint64_t* tempty_bar = tfull_bar + 2;
   uint64_t* drain_bar = tempty_bar + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain_bar + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  // shared-memory copy of the routing table the tile scheduler searches:
+  // tile_off (row tiles) or offsets (weight-gradient tiles)
   int* tile_tab = reinterpret_cast<int*>(reinterpret_cast<uint8_t*>(full_bar) + 256);
-  const int* tab = (!WGRAD && p.G + 1 <= kTileTabInts) ? tile_tab : nullptr;
+  const int* tab = p.G + 1 <= kTileTabInts ? tile_tab : nullptr;
 
 
   const int warp = threadIdx.x >> 5;
@@ -603,6 +648,10 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
       prefetch_tmap(&p.wb_hi);
       prefetch_tmap(&p.wb_lo);
     }
+    if (EPI == static_cast<int>(Epi::kDgradDn) && p.om_ok) {
+      prefetch_tmap(&p.om_hi);
+      prefetch_tmap(&p.om_lo);
+    }
   }
   if (warp == 1) {
     tmem_alloc(tmem_slot, C::kTmemCols);
@@ -611,8 +660,10 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
   // everything above overlaps the previous kernel; from here on its outputs
   // (routing tables, permuted rows, intermediates) are read
   pdl_wait();
-  if (tab != nullptr)
-    for (int i = threadIdx.x; i <= p.G; i += blockDim.x) tile_tab[i] = __ldg(p.tile_off + i);
+  if (tab != nullptr) {
+    const int32_t* src = WGRAD ? p.offsets : p.tile_off;
+    for (int i = threadIdx.x; i <= p.G; i += blockDim.x) tile_tab[i] = __ldg(src + i);
+  }
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
@@ -854,7 +905,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
     const int ew = warp - 2;
     const int q = warp & 3;   // TMEM lane quadrant of this warp
     const int hf = ew >> 2;   // column half owned by this warp
-    const uint32_t stg = smem_u32(stage_tiles + ew * kStgBytes);
+    const uint32_t stg = smem_u32(stage_tiles + ew * C::kStgBytes);
     int local = 0;
     for (int t = blockIdx.x; t < num_tiles; t += gridDim.x, ++local) {
       const TileInfo ti = tile_info<WGRAD>(p, t, tab);
@@ -884,6 +935,12 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
       tc_fence_before();
       mbar_arrive(tempty_bar + buf);
     }
+    // TMA stores issued by this warp complete before the CTA's shared memory
+    // goes away
+    if constexpr (EPI == static_cast<int>(Epi::kDgradDn)) {
+      if (lane == 0) bulk_wait_all();
+      __syncwarp();
+    }
   }
 
   __syncthreads();
@@ -896,7 +953,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
 
 template <int BN, bool B_MN, bool WGRAD, int EPI>
 cudaError_t launch_one(const GemmParams& p, int num_sms, cudaStream_t s) {
-  using C = Cfg<BN>;
+  using C = Cfg<BN, EPI>;
   static_assert(C::kSmemBytes <= 232448, "shared memory budget");
   auto kern = gemm_kernel<BN, B_MN, WGRAD, EPI>;
   cudaError_t e =
@@ -930,9 +987,10 @@ cudaError_t launch_gemm(const GemmShape& sh, const GemmParams& p, int num_sms, c
     if (e == kSt) return launch_one<256, false, false, kSt>(p, num_sms, s);
   }
   if (sh.BN == 256 && sh.b_mn) {
-    if (e == kDd) return launch_one<256, true, false, kDd>(p, num_sms, s);
     if (e == kSt) return launch_one<256, true, false, kSt>(p, num_sms, s);
   }
+  if (sh.BN == kDgradBN && sh.b_mn && e == kDd)
+    return launch_one<kDgradBN, true, false, kDd>(p, num_sms, s);
   if (sh.BN == 64 && e == kLo) {
     if (sh.b_mn) return launch_one<64, true, false, kLo>(p, num_sms, s);
     return launch_one<64, false, false, kLo>(p, num_sms, s);

@@ -88,6 +88,10 @@ constexpr int kMaxSlices = 4;
 // The down-projection dgrad writes one routing-weight-gradient partial per
 // 256-column tile and column half (two epilogue warps share each row).
 constexpr int kDwPartsPerTile = 2;
+// N tile (f features) of the down-projection dgrad with the SwiGLU-backward
+// epilogue: 192 columns leave room in shared memory for a second staging tile
+// per epilogue warp next to a 4-stage ring.
+constexpr int kDgradBN = 192;
 
 // One K-slice of a contraction: D += A_slice * B_slice^T over K columns.
 struct GemmSlice {
@@ -103,6 +107,8 @@ struct GemmSlice {
 struct GemmParams {
   GemmSlice sl[kMaxSlices];  // rows mode: A/B per slice; wgrad: A sources (hi, lo)
   CUtensorMap wb_hi, wb_lo;  // wgrad: B operand hi / lo (columns [0,64) / [64,128))
+  CUtensorMap om_hi, om_lo;  // SwiGLU backward: dh hi / lo planes as TMA store targets
+  int om_ok;                 //   set when om_hi / om_lo are valid
   int nslices;
   int gather_any;     // some slice gathers its A rows
   int N;              // valid output columns (rows mode) / LoRA rank r (wgrad)
@@ -147,9 +153,10 @@ int device_status_word(int** out);
 int record_error(int code, const char* msg);
 
 // ---- tensor maps (api.cu) ----------------------------------------------------
-// 2D bf16 map over [rows, cols] row-major; box (box_cols, box_rows); 128B swizzle.
+// 2D bf16 map over [rows, cols] row-major; box (box_cols, box_rows); 128B
+// swizzle, or none (dense box rows) with swizzle128 = false.
 bool make_map_2d(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols,
-                 uint32_t box_rows, uint32_t box_cols);
+                 uint32_t box_rows, uint32_t box_cols, bool swizzle128 = true);
 // 3D bf16 map over [G, rows, cols]; box (box_cols, box_rows, 1); 128B swizzle.
 bool make_map_3d(CUtensorMap* m, const void* base, uint64_t G, uint64_t rows, uint64_t cols,
                  uint32_t box_rows, uint32_t box_cols);
