@@ -872,14 +872,24 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
             rows_kblock(p, kb, s, kc, kext);
             nk16 = min(4, (kext + 15) / 16);
           }
-          for (int kk = 0; kk < nk16; ++kk) {
-            uint64_t ad, bd;
-            if (!WGRAD) ad = sdesc_sw128(sa + kk * 32, 16, 1024);
-            else ad = sdesc_sw128(sa + kk * 2048, kChunkBytes, 1024);
-            if (!B_MN && !WGRAD) bd = sdesc_sw128(sb + kk * 32, 16, 1024);
-            else bd = sdesc_sw128(sb + kk * 2048, kChunkBytes, 1024);
+          // descriptors of the stage's first K step; each further K step of
+          // 16 moves the start address field (bits 0-13, address >> 4) by
+          // 32 bytes (K-major) or 2048 bytes (MN-major: 16 rows of 128 B)
+          constexpr uint32_t kAStep = (WGRAD ? 2048u : 32u) >> 4;
+          constexpr uint32_t kBStep = ((B_MN || WGRAD) ? 2048u : 32u) >> 4;
+          const uint64_t ad = sdesc_sw128(sa, WGRAD ? kChunkBytes : 16u, 1024);
+          const uint64_t bd = sdesc_sw128(sb, (B_MN || WGRAD) ? kChunkBytes : 16u, 1024);
+          if (nk16 == 4) {
             tc_mma_bf16(d_tmem, ad, bd, idesc, accum);
+            tc_mma_bf16(d_tmem, ad + kAStep, bd + kBStep, idesc, 1u);
+            tc_mma_bf16(d_tmem, ad + 2 * kAStep, bd + 2 * kBStep, idesc, 1u);
+            tc_mma_bf16(d_tmem, ad + 3 * kAStep, bd + 3 * kBStep, idesc, 1u);
             accum = 1;
+          } else {
+            for (int kk = 0; kk < nk16; ++kk) {
+              tc_mma_bf16(d_tmem, ad + kk * kAStep, bd + kk * kBStep, idesc, accum);
+              accum = 1;
+            }
           }
           tc_commit(empty_bar + stage);
         }
