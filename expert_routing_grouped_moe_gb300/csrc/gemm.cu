@@ -256,20 +256,6 @@ __device__ __forceinline__ TileInfo tile_info(const GemmParams& p, int t, const 
   return ti;
 }
 
-// Slice and K offset of k-block kb (rows mode).
-__device__ __forceinline__ void rows_kblock(const GemmParams& p, int kb, int& s, int& kc,
-                                            int& kext) {
-  s = 0;
-  int nk = (p.sl[0].K + BK - 1) / BK;
-  while (kb >= nk && s + 1 < p.nslices) {
-    kb -= nk;
-    ++s;
-    nk = (p.sl[s].K + BK - 1) / BK;
-  }
-  kc = kb * BK;
-  kext = p.sl[s].K - kc;
-}
-
 // ------------------------------------------------------------- epilogues
 // Each epilogue warp owns 32 accumulator rows (TMEM quadrant q) and one half
 // (hf) of the tile's columns.  `tq` is the TMEM address of its rows' column 0,
@@ -701,10 +687,18 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
     for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
       const TileInfo ti = tile_info<WGRAD>(p, t, tab);
       if (!WGRAD && p.gather_any) lane_rows(ti.row0, ti.nvalid, 4, y);
+      int cs = 0, ckc = 0;  // rows mode: slice and K offset of the next K block
       for (int kb = 0; kb < ti.nk; ++kb) {
         int s = 0, kc = 0, kext = 0, row = 0;
         if (!WGRAD) {
-          rows_kblock(p, kb, s, kc, kext);
+          s = cs;
+          kc = ckc;
+          kext = p.sl[s].K - kc;
+          ckc += BK;
+          if (ckc >= p.sl[cs].K) {
+            ++cs;
+            ckc = 0;
+          }
         } else {
           s = kb / ti.nkb;
           const int b = kb - s * ti.nkb;
@@ -832,6 +826,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
       tc_fence_after();
       const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(buf * BN);
       uint32_t accum = 0;
+      int cs = 0, ckc = 0;  // rows mode: slice and K offset of the next K block
       for (int kb = 0; kb < ti.nk; ++kb) {
         int f_ok = 1;
         if (lane == 0) f_ok = mbar_wait(full_bar + stage, phase, abort_flag, kWaitTimeoutNs);
@@ -867,11 +862,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
           tc_fence_after();
           if (p.gather_any) fence_proxy_async_smem();  // LSU-copied A rows -> async proxy
           int nk16 = 4;
-          if (!WGRAD) {
-            int s, kc, kext;
-            rows_kblock(p, kb, s, kc, kext);
-            nk16 = min(4, (kext + 15) / 16);
-          }
+          if (!WGRAD) nk16 = min(4, (p.sl[cs].K - ckc + 15) / 16);
           // descriptors of the stage's first K step; each further K step of
           // 16 moves the start address field (bits 0-13, address >> 4) by
           // 32 bytes (K-major) or 2048 bytes (MN-major: 16 rows of 128 B)
@@ -894,6 +885,13 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
           tc_commit(empty_bar + stage);
         }
         if constexpr (WGRAD) __syncwarp();
+        if (!WGRAD) {
+          ckc += BK;
+          if (ckc >= p.sl[cs].K) {
+            ++cs;
+            ckc = 0;
+          }
+        }
         if (++stage == S) {
           stage = 0;
           phase ^= 1u;
