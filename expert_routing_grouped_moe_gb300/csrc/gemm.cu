@@ -658,19 +658,18 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
       WGRAD ? p.G * p.n_ntiles * p.n_btiles
             : min(__ldg(p.tile_off + p.G) * p.n_ntiles, p.max_tiles);
 
-  if (warp == 0) {
+  if (warp == 0 && (lane == 0 || p.gather_any)) {
     // ------------------------------------------------------------ producer
-    // Lane 0 waits for free stages and issues the TMA tile copies.  A gathered
-    // A operand (token rows picked by sorted_src) is copied by all 32 lanes
-    // with 16-byte cp.async into the 128B-swizzled layout TMA would produce.
-    // When any slice gathers, every lane arrives on each stage's full barrier
-    // (which then expects 1 + 32 arrivals) once its copies so far have
-    // completed; the MMA issuer fences them for the async proxy.
+    // Lane 0 waits for free stages and issues the TMA tile copies (alone
+    // unless rows are gathered).  A gathered A operand (token rows picked by
+    // sorted_src) is copied by all 32 lanes with 16-byte cp.async into the
+    // 128B-swizzled layout TMA would produce.  When any slice gathers, every
+    // lane arrives on each stage's full barrier (which then expects 1 + 32
+    // arrivals) once its copies so far have completed; the MMA issuer fences
+    // them for the async proxy.
     int stage = 0;
     uint32_t phase = 0;
-    int armed[S];
-#pragma unroll
-    for (int i = 0; i < S; ++i) armed[i] = -1;
+    uint32_t armed_bits = 0, armed_phase = 0;  // stages armed, and with which parity
     bool ok = true;
     const bool lanes_arrive = p.gather_any != 0;
     // Token rows of the permuted rows first + lane + 32*i (i < n): y[i].  Rows
@@ -714,7 +713,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
           w_ok = mbar_wait(empty_bar + stage, phase ^ 1u, abort_flag, kWaitTimeoutNs);
           if (w_ok) {
             mbar_expect_tx(fb, gat ? C::kBStageBytes : C::kStageBytes);
-            armed[stage] = static_cast<int>(phase);
+            armed_bits |= 1u << stage;
+            armed_phase = (armed_phase & ~(1u << stage)) | (phase << stage);
             if (!WGRAD) {
               const CUtensorMap* mb = &p.sl[s].b;
               if (!gat) tma_load_2d(sa, &p.sl[s].a, fb, kc, ti.row0);
@@ -748,7 +748,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
             }
           }
         }
-        w_ok = __shfl_sync(0xffffffffu, w_ok, 0);  // the stage is free and armed
+        if (lanes_arrive) w_ok = __shfl_sync(0xffffffffu, w_ok, 0);  // the stage is armed
         if (!w_ok) {
           ok = false;
           break;
@@ -800,9 +800,9 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
     if (!ok && lane == 0) {
       // drain copies still in flight into this CTA's shared memory
       for (int i = 0; i < S; ++i)
-        if (armed[i] >= 0) {
+        if ((armed_bits >> i) & 1u) {
           volatile int never = 0;
-          mbar_wait(full_bar + i, static_cast<uint32_t>(armed[i]), &never, 200000000ull);
+          mbar_wait(full_bar + i, (armed_phase >> i) & 1u, &never, 200000000ull);
         }
     }
   } else if (warp == 1 && (WGRAD || lane == 0)) {
