@@ -234,9 +234,11 @@ __device__ __forceinline__ TileInfo tile_info(const GemmParams& p, int t, const 
     ti.row0 = 0;
     ti.nvalid = 0;
     if (ROWS) {
+      // offsets follow tile_off in the table when both fit
+      const int* otab = (tab && 2 * (p.G + 1) <= kTileTabInts) ? tab + p.G + 1 : nullptr;
       const int local = ti.mt - (tab ? tab[ti.g] : __ldg(p.tile_off + ti.g));
-      const int off = __ldg(p.offsets + ti.g);
-      const int cnt = __ldg(p.offsets + ti.g + 1) - off;
+      const int off = otab ? otab[ti.g] : __ldg(p.offsets + ti.g);
+      const int cnt = (otab ? otab[ti.g + 1] : __ldg(p.offsets + ti.g + 1)) - off;
       ti.row0 = off + local * BM;
       ti.nvalid = min(BM, cnt - local * BM);
     }
@@ -603,8 +605,9 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
   uint64_t* drain_bar = tempty_bar + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain_bar + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
-  // shared-memory copy of the routing table the tile scheduler searches:
-  // tile_off (row tiles) or offsets (weight-gradient tiles)
+  // shared-memory copy of the routing tables the tile scheduler reads:
+  // tile_off then offsets (row tiles; offsets only when both fit), or
+  // offsets (weight-gradient tiles)
   int* tile_tab = reinterpret_cast<int*>(reinterpret_cast<uint8_t*>(full_bar) + 256);
   const int* tab = p.G + 1 <= kTileTabInts ? tile_tab : nullptr;
 
@@ -649,6 +652,9 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
   if (tab != nullptr) {
     const int32_t* src = WGRAD ? p.offsets : p.tile_off;
     for (int i = threadIdx.x; i <= p.G; i += blockDim.x) tile_tab[i] = __ldg(src + i);
+    if (!WGRAD && 2 * (p.G + 1) <= kTileTabInts)
+      for (int i = threadIdx.x; i <= p.G; i += blockDim.x)
+        tile_tab[p.G + 1 + i] = __ldg(p.offsets + i);
   }
   __syncthreads();
   tc_fence_after();
