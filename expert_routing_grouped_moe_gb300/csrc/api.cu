@@ -238,6 +238,32 @@ bool make_map_3d(CUtensorMap* m, const void* base, uint64_t G, uint64_t rows, ui
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+bool make_map_mn4d(CUtensorMap* m, const void* base, uint64_t G, uint64_t rows, uint64_t cols,
+                   uint32_t box_rows, uint32_t chunks) {
+  EncodeTiledFn fn = encode_fn();
+  if (fn == nullptr || cols % 64 != 0) return false;
+  const cuuint64_t dims[4] = {64, rows, cols / 64, G};
+  const cuuint64_t strides[3] = {cols * 2, 128, rows * cols * 2};
+  const cuuint32_t box[4] = {64, box_rows, chunks, 1};
+  const cuuint32_t es[4] = {1, 1, 1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides, box,
+            es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool make_map_split4d(CUtensorMap* m, const void* base, uint64_t G, uint64_t half,
+                      uint64_t cols, uint32_t box_rows, uint32_t box_cols) {
+  EncodeTiledFn fn = encode_fn();
+  if (fn == nullptr) return false;
+  const cuuint64_t dims[4] = {cols, half, 2, G};
+  const cuuint64_t strides[3] = {cols * 2, half * cols * 2, 2 * half * cols * 2};
+  const cuuint32_t box[4] = {box_cols, box_rows, 2, 1};
+  const cuuint32_t es[4] = {1, 1, 1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides, box,
+            es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 namespace {
 
 struct BwdWs {
@@ -505,6 +531,15 @@ int moe_lora_grouped_mlp_fwd(const moe_dims* dims, const moe_bf16* Xp, const moe
     SLICE(p, 2, xa_gu + Nr, N, r, MAP3(p.sl[2].b, B_gu, G, 2 * f, r, 128, 64), r);
     p.nslices = 3; p.N = f; p.n_ntiles = (f + 127) / 128; p.b_split = f;
     p.fout = h; p.ldf = 32 * ((f + 15) / 16); p.ld0 = 2 * f; p.out0 = act; p.pair = Nf;
+    {  // one 4-D box per K block for both halves (the 3-D maps stay as fallback)
+      GemmSlice q[3] = {p.sl[0], p.sl[1], p.sl[2]};
+      if (make_map_split4d(&q[0].b, W_gu, G, f, d, 128, 64) &&
+          make_map_split4d(&q[1].b, B_gu, G, f, r, 128, 64) &&
+          make_map_split4d(&q[2].b, B_gu, G, f, r, 128, 64)) {
+        for (int i = 0; i < 3; ++i) p.sl[i] = q[i];
+        p.b4d = 1;
+      }
+    }
     if ((rc = run_gemm({256, false, false, Epi::kSwiGLU}, p, R, st->num_sms, s, "gate_up")))
       return rc;
   }
@@ -658,6 +693,15 @@ int moe_lora_grouped_mlp_bwd(const moe_dims* dims, const moe_bf16* dYp, const mo
     SLICE(p, 1, w.us, N, r, MAP3(p.sl[1].b, A_dn, G, r, f, 64, 64), r);
     SLICE(p, 2, w.us + Nr, N, r, MAP3(p.sl[2].b, A_dn, G, r, f, 64, 64), r);
     p.nslices = 3; p.N = f; p.n_ntiles = ntiles_f;
+    {  // one 4-D box per K block (the 3-D maps stay as fallback)
+      GemmSlice q[3] = {p.sl[0], p.sl[1], p.sl[2]};
+      if (make_map_mn4d(&q[0].b, W_dn, G, d, f, 64, kDgradBN / 64) &&
+          make_map_mn4d(&q[1].b, A_dn, G, r, f, 64, kDgradBN / 64) &&
+          make_map_mn4d(&q[2].b, A_dn, G, r, f, 64, kDgradBN / 64)) {
+        for (int i = 0; i < 3; ++i) p.sl[i] = q[i];
+        p.b4d = 1;
+      }
+    }
     p.fin = h; p.ldf = 32 * ((f + 15) / 16);
     p.out0 = w.dh; p.ld0 = 2 * f; p.pair = N2f; p.fout = w.dwp; p.fstride = N;
     // dh planes as TMA store targets: 16 features x 32 rows per store
@@ -690,6 +734,14 @@ int moe_lora_grouped_mlp_bwd(const moe_dims* dims, const moe_bf16* dYp, const mo
     SLICE(p, 0, w.dh, N, 2 * f, MAP3(p.sl[0].b, W_gu, G, 2 * f, d, 64, 64), 2 * f);
     SLICE(p, 1, w.vs, N, r, MAP3(p.sl[1].b, A_gu, G, r, d, 64, 64), r);
     p.nslices = 2; p.N = d; p.n_ntiles = (d + 255) / 256; p.out0 = dXp; p.ld0 = d;
+    {  // one 4-D box per K block (the 3-D maps stay as fallback)
+      GemmSlice q[2] = {p.sl[0], p.sl[1]};
+      if (make_map_mn4d(&q[0].b, W_gu, G, 2 * f, d, 64, 4) &&
+          make_map_mn4d(&q[1].b, A_gu, G, r, d, 64, 4)) {
+        for (int i = 0; i < 2; ++i) p.sl[i] = q[i];
+        p.b4d = 1;
+      }
+    }
     if ((rc = run_gemm({256, true, false, Epi::kStore}, p, R, st->num_sms, s, "dgrad_gu")))
       return rc;
   }

@@ -724,7 +724,11 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
             if (!WGRAD) {
               const CUtensorMap* mb = &p.sl[s].b;
               if (!gat) tma_load_2d(sa, &p.sl[s].a, fb, kc, ti.row0);
-              if (!B_MN) {
+              if (p.b4d) {
+                // the whole B tile in one box: gate/up halves or MN chunks
+                if (!B_MN) tma_load_4d(sb, mb, fb, kc, ti.nt * (BN / 2), 0, ti.g);
+                else tma_load_4d(sb, mb, fb, 0, kc, ti.nt * (BN / 64), ti.g);
+              } else if (!B_MN) {
                 if (p.b_split) {
                   const int n0 = ti.nt * (BN / 2);
                   tma_load_3d(sb, mb, fb, kc, n0, ti.g);

@@ -116,6 +116,8 @@ struct GemmParams {
   int n_ntiles;       // N tiles per M tile (rows mode) / M tiles per group (wgrad)
   int n_btiles;       // wgrad: N tiles over the B matrix's columns (1 for the LoRA gradients)
   int b_split;        // rows offset of the second B half (gate/up pairing), 0 = none
+  int b4d;            // every slice's B map is 4-D: one box per K block (MN-major
+                      // 64-column chunks, or the two gate/up halves)
   int G, k, K;        // groups, top-k, slots per token
   float scale;        // LoRA scale s
   const int32_t* tile_off;
@@ -160,5 +162,14 @@ bool make_map_2d(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols,
 // 3D bf16 map over [G, rows, cols]; box (box_cols, box_rows, 1); 128B swizzle.
 bool make_map_3d(CUtensorMap* m, const void* base, uint64_t G, uint64_t rows, uint64_t cols,
                  uint32_t box_rows, uint32_t box_cols);
+// 4D views of [G, rows, cols] for one TMA box per K block (128B swizzle):
+// mn: (64 columns, rows, cols / 64 chunks, G), box (64, box_rows, chunks, 1),
+//     landing as `chunks` consecutive [box_rows][64] blocks; cols % 64 == 0.
+// split: rows = two halves of `half` rows: (cols, half, 2, G), box
+//     (box_cols, box_rows, 2, 1), landing as the two halves' blocks.
+bool make_map_mn4d(CUtensorMap* m, const void* base, uint64_t G, uint64_t rows, uint64_t cols,
+                   uint32_t box_rows, uint32_t chunks);
+bool make_map_split4d(CUtensorMap* m, const void* base, uint64_t G, uint64_t half,
+                      uint64_t cols, uint32_t box_rows, uint32_t box_cols);
 
 }  // namespace moe
