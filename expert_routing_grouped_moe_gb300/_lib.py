@@ -30,7 +30,7 @@ EXPORTED = (
     "moe_permute", "moe_unpermute_combine", "moe_lora_grouped_mlp_fwd",
     "moe_mlp_bwd_workspace_size", "moe_lora_grouped_mlp_bwd", "moe_status",
     "moe_last_error", "moe_abi_version", "moe_kernel_name", "moe_probe_arm", "moe_probe_count",
-    "moe_route_noalloc",
+    "moe_route_noalloc", "moe_selftest_wait_timeout",
 )
 
 
@@ -84,6 +84,7 @@ def load(path: str = LIB_PATH):
             "moe_lora_grouped_mlp_bwd": (ctypes.c_int, [ctypes.POINTER(MoeDims)] + [_P] * 28
                                          + [_SZ, _P]),
             "moe_status": (ctypes.c_int, [_P]),
+            "moe_selftest_wait_timeout": (ctypes.c_int, [ctypes.c_uint32, _P]),
             "moe_last_error": (ctypes.c_char_p, []),
             "moe_abi_version": (ctypes.c_int, []),
             "moe_kernel_name": (ctypes.c_char_p, [_I]),
@@ -229,6 +230,14 @@ def moe_lora_grouped_mlp_bwd(dims: MoeDims, dYp, dY, Xp, X, counts, offsets, til
 def moe_status(stream=None) -> int:
     """Synchronise the stream and return (and clear) the device status word."""
     return int(load().moe_status(_stream(stream)))
+
+
+def moe_selftest_wait_timeout(timeout_us: int, stream=None):
+    """Enqueue the bounded-wait self-test: a GPU thread that waits on an
+    mbarrier nothing arrives on for timeout_us, then records MOE_ERR_TIMEOUT
+    (read it with moe_status)."""
+    _check(load().moe_selftest_wait_timeout(int(timeout_us), _stream(stream)),
+           "moe_selftest_wait_timeout")
 
 
 # ------------------------------------------------------------------ tracing

@@ -412,6 +412,18 @@ int moe_status(moe_stream_t stream) {
   return ok();
 }
 
+int moe_selftest_wait_timeout(uint32_t timeout_us, moe_stream_t stream) {
+  if (timeout_us == 0 || timeout_us > 2000000u)
+    return fail(MOE_ERR_INVALID_ARG, "timeout_us must be in (0, 2000000]");
+  DevState* st = nullptr;
+  int rc = device_state(&st);
+  if (rc) return rc;
+  const cudaError_t e =
+      launch_wait_selftest(st->status, static_cast<uint64_t>(timeout_us) * 1000u, stream);
+  if (e != cudaSuccess) return cuda_fail(e, "wait self-test launch");
+  return ok();
+}
+
 int moe_router_topk(const float* logits, int32_t T, int32_t E, int32_t k, int32_t* ids,
                     float* weights, moe_stream_t stream) {
   if (logits == nullptr || ids == nullptr || weights == nullptr)

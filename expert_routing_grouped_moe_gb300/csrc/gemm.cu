@@ -969,6 +969,20 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
   if (threadIdx.x == 0 && *abort_flag) atomicCAS(p.status, 0, kErrTimeout);
 }
 
+// Self-test of the pipelines' failure path: one thread waits on an mbarrier
+// that nothing ever arrives on, with the same bounded wait the GEMM roles use;
+// when the limit passes it records MOE_ERR_TIMEOUT and returns.
+__global__ void wait_selftest_kernel(int* status, unsigned long long timeout_ns) {
+  __shared__ uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    abort_flag = 0;
+    fence_mbar_init();
+    if (!mbar_wait(&bar, 0, &abort_flag, timeout_ns)) atomicCAS(status, 0, kErrTimeout);
+  }
+}
+
 template <int BN, bool B_MN, bool WGRAD, int EPI>
 cudaError_t launch_one(const GemmParams& p, int num_sms, cudaStream_t s) {
   using C = Cfg<BN, EPI>;
@@ -984,6 +998,11 @@ cudaError_t launch_one(const GemmParams& p, int num_sms, cudaStream_t s) {
 }
 
 }  // namespace
+
+cudaError_t launch_wait_selftest(int* status, uint64_t timeout_ns, cudaStream_t s) {
+  wait_selftest_kernel<<<1, 32, 0, s>>>(status, timeout_ns);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_gemm(const GemmShape& sh, const GemmParams& p, int num_sms, cudaStream_t s) {
   constexpr int kSw = static_cast<int>(Epi::kSwiGLU);

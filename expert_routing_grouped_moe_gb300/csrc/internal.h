@@ -147,6 +147,9 @@ struct GemmShape {
 
 cudaError_t launch_gemm(const GemmShape& shape, const GemmParams& p, int num_sms,
                         cudaStream_t s);
+// One thread waits on an mbarrier nothing arrives on, bounded by timeout_ns,
+// then records kErrTimeout in *status (the failure path of every pipeline wait).
+cudaError_t launch_wait_selftest(int* status, uint64_t timeout_ns, cudaStream_t s);
 
 // ---- shared host state (api.cu) ----------------------------------------------
 // Address of the current device's status word (looked up once per device).

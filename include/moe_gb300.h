@@ -284,6 +284,15 @@ MOE_API int moe_status(moe_stream_t stream);
 /* Message for the last error returned on this thread ("" if none). */
 MOE_API const char* moe_last_error(void);
 
+/* Self-test of the failure path that every pipeline wait of the GEMM kernels
+ * takes: enqueues one GPU thread that waits on an mbarrier no one arrives on,
+ * bounded by timeout_us microseconds (1 .. 2,000,000), through the same wait
+ * routine; when the limit passes it records MOE_ERR_TIMEOUT in the device
+ * status word and returns, leaving the context usable.  moe_status(stream)
+ * then returns MOE_ERR_TIMEOUT.  Returns MOE_OK once enqueued, or
+ * MOE_ERR_INVALID_ARG for a timeout out of range. */
+MOE_API int moe_selftest_wait_timeout(uint32_t timeout_us, moe_stream_t stream);
+
 /* ------------------------------------------------------------------------ */
 /* Tracing: timing probe                                                     */
 /* ------------------------------------------------------------------------ */

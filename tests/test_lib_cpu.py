@@ -99,6 +99,12 @@ def test_bwd_full_gradients_need_permuted_rows(lib):
     assert b"permuted rows" in lib.moe_last_error()
 
 
+def test_wait_selftest_argument_range(lib):
+    from expert_routing_grouped_moe_gb300 import _lib
+    assert lib.moe_selftest_wait_timeout(0, None) == _lib.MOE_ERR_INVALID_ARG
+    assert lib.moe_selftest_wait_timeout(2000001, None) == _lib.MOE_ERR_INVALID_ARG
+
+
 def test_route_argument_errors_before_launch(lib):
     from expert_routing_grouped_moe_gb300 import _lib
     P = ctypes.c_void_p
