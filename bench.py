@@ -84,8 +84,9 @@ def layer_counts(cfg, full_grads=False):
         "gate_up": (2 * N * d * 2 * f + 2 * N * r * 2 * f,
                     rows_d + W_gu + pair_r + B_gu + 4 * N * hs + pair_f),
         "xa_dn": (2 * N * f * r, pair_f + A_dn + pair_r),
-        "down": (2 * N * f * d + 2 * N * r * d, 2 * N * f + W_dn + pair_r + B_dn + 4 * N + rows_d),
-        "u": (2 * N * d * r, rows_d + B_dn + pair_r + 4 * N + 3 * pair_r),
+        # down reads the high halves of act' and xa_dn (both carry w)
+        "down": (2 * N * f * d + 2 * N * r * d, 2 * N * f + W_dn + 2 * N * r + B_dn + rows_d),
+        "u": (2 * N * d * r, rows_d + B_dn + pair_r),
         "dgrad_dn": (2 * N * d * f + 2 * N * r * f,
                      rows_d + W_dn + pair_r + A_dn + 4 * N * hs + 4 * N + 2 * pair_f
                      + 4 * N * nparts),
