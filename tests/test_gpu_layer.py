@@ -163,6 +163,16 @@ EDGE = {
     "exact_tiles": (synth.LayerConfig("exact_tiles", T=256, d=128, f=128, E=4, k=2, r=16,
                                       alpha=32),
                     lambda T, E, k, rng: np.stack([[t % 4, (t + 1) % 4] for t in range(T)])),
+    # many experts: the GEMMs keep only tile_off in shared memory (G + 1 > 224)
+    "experts_300": (synth.LayerConfig("experts_300", T=600, d=128, f=64, E=300, k=4, r=8,
+                                      alpha=16),
+                    lambda T, E, k, rng: np.stack([rng.choice(E, size=k, replace=False)
+                                                   for _ in range(T)])),
+    # more: the tile scheduler searches global memory (G + 1 > 448)
+    "experts_600": (synth.LayerConfig("experts_600", T=700, d=128, f=64, E=600, k=4, r=8,
+                                      alpha=16),
+                    lambda T, E, k, rng: np.stack([rng.choice(E, size=k, replace=False)
+                                                   for _ in range(T)])),
 }
 
 
