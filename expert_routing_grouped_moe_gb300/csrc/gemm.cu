@@ -10,21 +10,26 @@
 //               the low-rank LoRA correction (A = the saved s*X A^T, B = the
 //               other adapter matrix) and the low halves of hi/lo operand
 //               pairs, all into the same fp32 accumulator.
-//   wgrad mode  D[M tile of a weight dimension, 128] = sum over the group's
-//               rows of A[rows, M]^T [B_hi | B_lo][rows, 128] -- the per-expert
-//               dA / dB reductions, one CTA per output tile, deterministic.
+//   wgrad mode  D[M tile of a weight dimension, BN] = sum over the group's
+//               rows of A[rows, M]^T B[rows, BN] -- the per-expert dA / dB
+//               reductions (B = [B_hi | B_lo] of a rank-r operand, halves
+//               added) and the full weight gradients (B = one wide row matrix
+//               in 256-column tiles), one CTA per output tile, deterministic.
 //
 // Warp roles (320 threads, one CTA per SM, persistent over tiles):
-//   warp 0      TMA producer: 128B-swizzled A and B tiles into a STAGES-deep
-//               shared-memory ring (mbarrier full/empty handshake)
+//   warp 0      producer: lane 0 issues the TMA copies of 128B-swizzled A and
+//               B tiles into a STAGES-deep shared-memory ring (mbarrier
+//               full/empty handshake); all 32 lanes copy gathered token rows
+//               with cp.async when the A rows are gathered
 //   warp 1      allocates TMEM (2 x BN fp32 columns: double-buffered
 //               accumulators); lane 0 issues tcgen05.mma and tcgen05.commit
 //   warps 2-9   epilogue, two warps per TMEM lane quadrant (warp w reads lanes
 //               32*(w%4)..), each owning half of the tile's columns: tcgen05.ld,
-//               fused SwiGLU / routing-weight scale / SwiGLU backward / LoRA
+//               fused SwiGLU / SwiGLU backward / LoRA / weight-gradient
 //               outputs.  Wide row traffic goes through a per-warp swizzled
 //               shared-memory staging tile so that global loads and stores are
-//               full 128-byte lines.  The accumulator is then freed, so the
+//               full 128-byte lines (the SwiGLU backward also stores through
+//               TMA from a second tile).  The accumulator is then freed, so the
 //               epilogue of one tile overlaps the mainloop of the next.
 //
 // Every wait is bounded (see mbar_wait): on timeout the CTA raises an abort
