@@ -121,15 +121,6 @@ __device__ __forceinline__ void store8_pair(uint16_t* hi, int64_t pair, const fl
   *reinterpret_cast<uint4*>(hi) = a;
   *reinterpret_cast<uint4*>(hi + pair) = b;
 }
-__device__ __forceinline__ void load8(const uint16_t* src, float (&v)[8]) {
-  const uint4 x = __ldg(reinterpret_cast<const uint4*>(src));
-  const uint32_t w[4] = {x.x, x.y, x.z, x.w};
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    v[2 * i] = bf16lo(w[i]);
-    v[2 * i + 1] = bf16hi(w[i]);
-  }
-}
 __device__ __forceinline__ uint4 f4_as_u4(float a, float b, float c, float d) {
   return make_uint4(__float_as_uint(a), __float_as_uint(b), __float_as_uint(c),
                     __float_as_uint(d));
@@ -811,7 +802,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
         }
       }
     }
-    if (lanes_arrive) cp_async_wait<0>();  // no copy outlives the producer
+    if (lanes_arrive) cp_async_wait_all();  // no copy outlives the producer
     if (!ok && lane == 0) {
       // drain copies still in flight into this CTA's shared memory
       for (int i = 0; i < S; ++i)

@@ -137,7 +137,7 @@ struct GemmParams {
   int* status;
 };
 
-// Kernel shapes: BN in {64, 128, 256}; B operand K-major or MN-major; two modes.
+// Kernel shapes: BN in {64, 128, 192, 256}; B operand K-major or MN-major; two modes.
 struct GemmShape {
   int BN;
   bool b_mn;

@@ -93,8 +93,8 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, u
       : "memory");
 }
 // 16-byte asynchronous copy global -> shared through the LSU (zero-filled
-// when src_bytes is 0).  Completion is tracked per thread, with commit / wait
-// groups or with cp_async_mbar_arrive_noinc.  The data is written by the
+// when src_bytes is 0).  Completion is tracked per thread, with
+// cp_async_mbar_arrive_noinc or cp_async_wait_all.  The data is written by the
 // generic proxy: a fence_proxy_async_smem() between its completion and the
 // tcgen05.mma that reads it is required.
 __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, uint32_t src_bytes) {
@@ -102,12 +102,9 @@ __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, uint32
                "r"(src_bytes)
                : "memory");
 }
-__device__ __forceinline__ void cp_async_commit() {
-  asm volatile("cp.async.commit_group;" ::: "memory");
-}
-template <int N>
-__device__ __forceinline__ void cp_async_wait() {
-  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+// Waits until all of this thread's cp.async copies have completed.
+__device__ __forceinline__ void cp_async_wait_all() {
+  asm volatile("cp.async.wait_all;" ::: "memory");
 }
 // Arrive on `bar` once all of this thread's earlier cp.async copies have
 // completed; the arrival is one of the barrier's expected arrivals (.noinc).
