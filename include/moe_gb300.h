@@ -300,7 +300,8 @@ MOE_API int moe_selftest_wait_timeout(uint32_t timeout_us, moe_stream_t stream);
 /* Kernel names the probe knows, i = 0, 1, ...; NULL past the last one:
  * route, permute, combine, router_topk, the grouped GEMMs xa_gu, gate_up,
  * xa_dn, down, u, dgrad_dn, v, dgrad_gu, the weight-gradient GEMMs dB_dn,
- * dA_dn, dB_gu, dA_gu, and dw_reduce.  ("route" covers its three kernels.) */
+ * dA_dn, dB_gu, dA_gu, dw_reduce, and the full weight-gradient GEMMs dW_dn
+ * and dW_gu.  ("route" covers its three kernels.) */
 MOE_API const char* moe_kernel_name(int32_t i);
 
 /* Arms the probe of one kernel: its next n launches record start_events[i]
