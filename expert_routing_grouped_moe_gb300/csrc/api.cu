@@ -526,6 +526,7 @@ int moe_lora_grouped_mlp_fwd(const moe_dims* dims, const moe_bf16* Xp, const moe
   const int G = dims->E + dims->shared_expert;
   const int64_t N = static_cast<int64_t>(dims->T) * (dims->k + dims->shared_expert);
   const int64_t R = max_row_tiles(dims->T, dims->k + dims->shared_expert, G);
+  const int64_t RG = (N + 127) / 128;  // tiles of the plain 128-row grid (rank-r products)
   const GemmParams base = base_params(dims, offsets, tile_off, sorted_src, topk_w, st->status);
   cudaStream_t s = stream;
 
@@ -534,7 +535,8 @@ int moe_lora_grouped_mlp_fwd(const moe_dims* dims, const moe_bf16* Xp, const moe
     GemmParams p = base;
     SLICE_ROWS(p, 0, Xp, X, d, MAP3(p.sl[0].b, A_gu, G, r, d, 64, 64), d);
     p.nslices = 1; p.N = r; p.n_ntiles = (r + 63) / 64; p.out0 = xa_gu; p.ld0 = r; p.pair = Nr;
-    if ((rc = run_gemm({64, false, false, Epi::kLoRA}, p, R, st->num_sms, s, "xa_gu"))) return rc;
+    if ((rc = run_gemm({128, false, false, Epi::kLoRAGrid}, p, RG, st->num_sms, s, "xa_gu")))
+      return rc;
   }
   {  // h = Xp W_gu^T + (s xa) B_gu^T (fp32) ; act pair = w * silu(gate) * up
     GemmParams p = base;
@@ -560,7 +562,8 @@ int moe_lora_grouped_mlp_fwd(const moe_dims* dims, const moe_bf16* Xp, const moe
     SLICE(p, 0, act, N, f, MAP3(p.sl[0].b, A_dn, G, r, f, 64, 64), f);
     SLICE(p, 1, act + Nf, N, f, MAP3(p.sl[1].b, A_dn, G, r, f, 64, 64), f);
     p.nslices = 2; p.N = r; p.n_ntiles = (r + 63) / 64; p.out0 = xa_dn; p.ld0 = r; p.pair = Nr;
-    if ((rc = run_gemm({64, false, false, Epi::kLoRA}, p, R, st->num_sms, s, "xa_dn"))) return rc;
+    if ((rc = run_gemm({128, false, false, Epi::kLoRAGrid}, p, RG, st->num_sms, s, "xa_dn")))
+      return rc;
   }
   {  // Yp = act W_dn^T + xa_dn B_dn^T = w * (o)   (act and xa_dn carry w)
     GemmParams p = base;
@@ -621,6 +624,7 @@ int moe_lora_grouped_mlp_bwd(const moe_dims* dims, const moe_bf16* dYp, const mo
   const int G = dims->E + dims->shared_expert;
   const int64_t N = static_cast<int64_t>(dims->T) * (dims->k + dims->shared_expert);
   const int64_t R = max_row_tiles(dims->T, dims->k + dims->shared_expert, G);
+  const int64_t RG = (N + 127) / 128;  // tiles of the plain 128-row grid (rank-r products)
   const GemmParams base = base_params(dims, offsets, tile_off, sorted_src, topk_w, st->status);
   cudaStream_t s = stream;
   const int ntiles_f = (f + kDgradBN - 1) / kDgradBN;
@@ -692,7 +696,7 @@ int moe_lora_grouped_mlp_bwd(const moe_dims* dims, const moe_bf16* dYp, const mo
     SLICE_ROWS(p, 0, dYp, dY, d, MAP3(p.sl[0].b, B_dn, G, d, r, 64, 64), d);
     p.nslices = 1; p.N = r; p.n_ntiles = (r + 63) / 64; p.ld0 = r; p.pair = Nr;
     p.out0 = w.us;
-    if ((rc = run_gemm({64, true, false, Epi::kLoRA}, p, R, st->num_sms, s, "u"))) return rc;
+    if ((rc = run_gemm({128, true, false, Epi::kLoRAGrid}, p, RG, st->num_sms, s, "u"))) return rc;
   }
   if ((rc = stream_dep(st->ev[0], s, aux))) return rc;
   if ((rc = wgrad(jobs[0], aux))) return rc;  // dB_dn
@@ -737,7 +741,7 @@ int moe_lora_grouped_mlp_bwd(const moe_dims* dims, const moe_bf16* dYp, const mo
     SLICE(p, 0, w.dh, N, 2 * f, MAP3(p.sl[0].b, B_gu, G, 2 * f, r, 64, 64), 2 * f);
     SLICE(p, 1, w.dh + N2f, N, 2 * f, MAP3(p.sl[1].b, B_gu, G, 2 * f, r, 64, 64), 2 * f);
     p.nslices = 2; p.N = r; p.n_ntiles = (r + 63) / 64; p.ld0 = r; p.pair = Nr; p.out0 = w.vs;
-    if ((rc = run_gemm({64, true, false, Epi::kLoRA}, p, R, st->num_sms, s, "v"))) return rc;
+    if ((rc = run_gemm({128, true, false, Epi::kLoRAGrid}, p, RG, st->num_sms, s, "v"))) return rc;
   }
   if ((rc = stream_dep(st->ev[2], s, aux))) return rc;
   if ((rc = wgrad(jobs[3], aux))) return rc;  // dA_gu

@@ -10,6 +10,11 @@
 //               the low-rank LoRA correction (A = the saved s*X A^T, B = the
 //               other adapter matrix) and the low halves of hi/lo operand
 //               pairs, all into the same fp32 accumulator.
+//   grid mode   the rank-r products (N = r <= 64) on the plain 128-row grid of
+//               the permuted rows: a tile whose rows belong to two groups
+//               stacks the groups' B blocks into one 128-column B tile, so one
+//               MMA per K step serves both (more groups: more passes over the
+//               tile); no rows past a group's end are computed.
 //   wgrad mode  D[M tile of a weight dimension, BN] = sum over the group's
 //               rows of A[rows, M]^T B[rows, BN] -- the per-expert dA / dB
 //               reductions (B = [B_hi | B_lo] of a rank-r operand, halves
@@ -68,14 +73,17 @@ template <int BN, int EPI>
 struct Cfg {
   static constexpr uint32_t kBStageBytes = BN * BK * 2;
   static constexpr uint32_t kStageBytes = kAStageBytes + kBStageBytes;
+  static constexpr bool kGrid = EPI == static_cast<int>(Epi::kLoRAGrid);
   // staging per epilogue warp: one tile, two for the SwiGLU backward (h in,
-  // dh out through TMA stores)
+  // dh out through TMA stores), none for the grid-mode LoRA products (whose
+  // rows leave straight from registers; the ring takes the room instead)
   static constexpr uint32_t kStgBytes =
-      (EPI == static_cast<int>(Epi::kDgradDn) ? 2 : 1) * kStgTileBytes;
+      kGrid ? 0u : (EPI == static_cast<int>(Epi::kDgradDn) ? 2 : 1) * kStgTileBytes;
   static constexpr uint32_t kRingFit =
       (kSmemMax - kFixedSmem - kEpiWarps * kStgBytes) / kStageBytes * kStageBytes;
-  // 4 / 4 / 6 / 8 stages for BN 256 / 192 (dgrad) / 128 / 64
-  static constexpr int kStages = (kRingFit < kRingMax ? kRingFit : kRingMax) / kStageBytes;
+  static constexpr uint32_t kRingCap = kGrid ? kRingFit : kRingMax;
+  // 4 / 4 / 6 / 8 stages for BN 256 / 192 (dgrad) / 128 / 64; 7 in grid mode
+  static constexpr int kStages = (kRingFit < kRingCap ? kRingFit : kRingCap) / kStageBytes;
   static constexpr uint32_t kTmemCols = pow2_at_least(2 * BN);  // power of two >= 32
   static constexpr size_t kSmemBytes =
       kFixedSmem + static_cast<size_t>(kStages) * kStageBytes + kEpiWarps * kStgBytes;
@@ -90,6 +98,20 @@ __device__ __forceinline__ int group_of_tile(const int32_t* __restrict__ tile_of
   while (lo < hi) {
     const int mid = (lo + hi + 1) >> 1;
     if ((tab ? tab[mid] : __ldg(tile_off + mid)) <= mt) lo = mid;
+    else hi = mid - 1;
+  }
+  return lo;
+}
+
+// Group owning permuted row `row` (< offsets[G]): the largest g with
+// offsets[g] <= row.  `tab` is the CTA's shared-memory copy of offsets, or
+// nullptr (search global memory).
+__device__ __forceinline__ int group_of_row(const int32_t* __restrict__ offsets, const int* tab,
+                                            int G, int row) {
+  int lo = 0, hi = G - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if ((tab ? tab[mid] : __ldg(offsets + mid)) <= row) lo = mid;
     else hi = mid - 1;
   }
   return lo;
@@ -214,7 +236,69 @@ struct TileInfo {
   int row0;    // first permuted row: of the tile (rows mode) / of the group (wgrad)
   int nvalid;  // rows mode: rows of the group in this tile (<= 128); wgrad: group rows
   int nkb;     // wgrad: 64-row K blocks per slice
+  // grid mode: groups g .. g + nx - 1 of this pass own rows [rlo, rhi) of the
+  // tile; rows from rmid on belong to group g + 1 (B block / accumulator slot 1)
+  int nx, rlo, rmid, rhi;
 };
+
+// Grid mode: tile t covers permuted rows [128 t, 128 t + 128) clipped to the
+// valid rows; its rows belong to groups g0 .. g1, taken two per pass.
+constexpr int kGridSlots = 2;
+struct GridTile {
+  int g0, g1, npass;
+};
+template <bool GRID>
+__device__ __forceinline__ GridTile grid_tile(const GemmParams& p, int t, const int* tab) {
+  GridTile gt{0, 0, 1};
+  if constexpr (GRID) {
+    const int nv = tab ? tab[p.G] : __ldg(p.offsets + p.G);
+    const int r0 = t * BM, r1 = min(r0 + BM, nv) - 1;
+    gt.g0 = group_of_row(p.offsets, tab, p.G, r0);
+    gt.g1 = group_of_row(p.offsets, tab, p.G, r1);
+    gt.npass = (gt.g1 - gt.g0) / kGridSlots + 1;
+  }
+  return gt;
+}
+__device__ __forceinline__ TileInfo grid_info(const GemmParams& p, int t, const GridTile& gt,
+                                              int pass, const int* tab) {
+  auto off = [&](int g) { return tab ? tab[g] : __ldg(p.offsets + g); };
+  TileInfo ti;
+  ti.g = gt.g0 + pass * kGridSlots;
+  ti.nx = min(kGridSlots, gt.g1 - ti.g + 1);
+  ti.mt = t;
+  ti.nt = 0;
+  ti.nk = 0;
+  for (int s = 0; s < p.nslices; ++s) ti.nk += (p.sl[s].K + BK - 1) / BK;
+  ti.row0 = t * BM;
+  const int nv = off(p.G);
+  ti.nvalid = min(BM, nv - ti.row0);
+  ti.rlo = max(ti.row0, off(ti.g));
+  ti.rmid = off(ti.g + 1);
+  ti.rhi = min(ti.row0 + ti.nvalid, off(ti.g + ti.nx));
+  ti.nkb = 0;
+  return ti;
+}
+
+// The sequence of work units every role of a CTA walks: its tiles t =
+// blockIdx.x + i * gridDim.x and, in grid mode, each tile's passes.
+struct Unit {
+  int t, ps;
+  GridTile gt;
+};
+template <bool GRID>
+__device__ __forceinline__ Unit unit_first(const GemmParams& p, const int* tab, int num_tiles) {
+  Unit u{static_cast<int>(blockIdx.x), 0, GridTile{0, 0, 1}};
+  if (GRID && u.t < num_tiles) u.gt = grid_tile<GRID>(p, u.t, tab);
+  return u;
+}
+template <bool GRID>
+__device__ __forceinline__ void unit_next(Unit& u, const GemmParams& p, const int* tab,
+                                          int num_tiles) {
+  if (GRID && ++u.ps < u.gt.npass) return;
+  u.ps = 0;
+  u.t += gridDim.x;
+  if (GRID && u.t < num_tiles) u.gt = grid_tile<GRID>(p, u.t, tab);
+}
 
 // ROWS = false skips the row range (row0, nvalid) of a rows-mode tile, which
 // the MMA issuer does not need.
@@ -495,6 +579,42 @@ __device__ __forceinline__ void epi_lora(const GemmParams& p, const TileInfo& ti
   }
 }
 
+// Grid mode: out0 = s * acc as a hi/lo pair for the rows of this pass; a
+// row's accumulator is slot 0 (columns [0,64)) or, from rmid on, slot 1
+// (columns [64,128)).  This warp: its 32 rows from rowq, columns hf*32 + [0,32).
+__device__ __forceinline__ void epi_lora_grid(const GemmParams& p, const TileInfo& ti,
+                                              uint32_t tq, int hf, int64_t rowq, int lane) {
+  const int64_t row = rowq + lane;
+  const bool valid = row >= ti.rlo && row < ti.rhi;
+  const bool second = row >= ti.rmid;
+  const bool any0 = __any_sync(0xffffffffu, valid && !second);
+  const bool any1 = __any_sync(0xffffffffu, valid && second);
+  const float s = p.scale;
+#pragma unroll 1
+  for (int c0 = hf * 32; c0 < hf * 32 + 32; c0 += 16) {
+    float v16[16];
+    if (any0) tmem_ld16(tq + c0, v16);
+    if (any1) {
+      float w16[16];
+      tmem_ld16(tq + 64 + c0, w16);
+      if (second) {
+#pragma unroll
+        for (int i = 0; i < 16; ++i) v16[i] = w16[i];
+      }
+    }
+#pragma unroll
+    for (int h8 = 0; h8 < 2; ++h8) {
+      const int j = c0 + h8 * 8;
+      if (valid && j < p.N) {
+        float ov[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) ov[i] = s * v16[h8 * 8 + i];
+        store8_pair(p.out0 + row * p.ld0 + j, p.pair, ov);
+      }
+    }
+  }
+}
+
 __device__ __forceinline__ void epi_wgrad(const GemmParams& p, const TileInfo& ti, uint32_t tq,
                                           int hf, int q, int lane, uint32_t stg) {
   // columns [0,64) = A * B_hi, [64,128) = A * B_lo; this warp: n in hf*32 + [0,32)
@@ -588,6 +708,7 @@ template <int BN, bool B_MN, bool WGRAD, int EPI>
 __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant__ GemmParams p) {
   using C = Cfg<BN, EPI>;
   constexpr int S = C::kStages;
+  constexpr bool GRID = EPI == static_cast<int>(Epi::kLoRAGrid);
   extern __shared__ uint8_t smem_raw[];
   // 1024-byte aligned stage ring (128B swizzle atoms are 8 rows x 128 B)
   const uint32_t raw_addr = smem_u32(smem_raw);
@@ -603,7 +724,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   // shared-memory copy of the routing tables the tile scheduler reads:
   // tile_off then offsets (row tiles; offsets only when both fit), or
-  // offsets (weight-gradient tiles)
+  // offsets (weight-gradient and grid tiles)
   int* tile_tab = reinterpret_cast<int*>(reinterpret_cast<uint8_t*>(full_bar) + 256);
   const int* tab = p.G + 1 <= kTileTabInts ? tile_tab : nullptr;
 
@@ -646,9 +767,9 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
   // (routing tables, permuted rows, intermediates) are read
   pdl_wait();
   if (tab != nullptr) {
-    const int32_t* src = WGRAD ? p.offsets : p.tile_off;
+    const int32_t* src = (WGRAD || GRID) ? p.offsets : p.tile_off;
     for (int i = threadIdx.x; i <= p.G; i += blockDim.x) tile_tab[i] = __ldg(src + i);
-    if (!WGRAD && 2 * (p.G + 1) <= kTileTabInts)
+    if (!WGRAD && !GRID && 2 * (p.G + 1) <= kTileTabInts)
       for (int i = threadIdx.x; i <= p.G; i += blockDim.x)
         tile_tab[p.G + 1 + i] = __ldg(p.offsets + i);
   }
@@ -657,8 +778,9 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
   const uint32_t tmem_base = *tmem_slot;
 
   const int num_tiles =
-      WGRAD ? p.G * p.n_ntiles * p.n_btiles
-            : min(__ldg(p.tile_off + p.G) * p.n_ntiles, p.max_tiles);
+      WGRAD  ? p.G * p.n_ntiles * p.n_btiles
+      : GRID ? min((__ldg(p.offsets + p.G) + BM - 1) / BM, p.max_tiles)
+             : min(__ldg(p.tile_off + p.G) * p.n_ntiles, p.max_tiles);
 
   if (warp == 0 && (lane == 0 || p.gather_any)) {
     // ------------------------------------------------------------ producer
@@ -685,8 +807,10 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
       }
     };
     int y[4] = {0, 0, 0, 0};
-    for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
-      const TileInfo ti = tile_info<WGRAD>(p, t, tab);
+    for (Unit u = unit_first<GRID>(p, tab, num_tiles); u.t < num_tiles && ok;
+         unit_next<GRID>(u, p, tab, num_tiles)) {
+      const TileInfo ti =
+          GRID ? grid_info(p, u.t, u.gt, u.ps, tab) : tile_info<WGRAD>(p, u.t, tab);
       if (!WGRAD && p.gather_any) lane_rows(ti.row0, ti.nvalid, 4, y);
       int cs = 0, ckc = 0;  // rows mode: slice and K offset of the next K block
       for (int kb = 0; kb < ti.nk; ++kb) {
@@ -714,13 +838,20 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
         if (lane == 0) {
           w_ok = mbar_wait(empty_bar + stage, phase ^ 1u, abort_flag, kWaitTimeoutNs);
           if (w_ok) {
-            mbar_expect_tx(fb, gat ? C::kBStageBytes : C::kStageBytes);
+            const uint32_t b_bytes = GRID ? ti.nx * kChunkBytes : C::kBStageBytes;
+            mbar_expect_tx(fb, (gat ? 0u : kAStageBytes) + b_bytes);
             armed_bits |= 1u << stage;
             armed_phase = (armed_phase & ~(1u << stage)) | (phase << stage);
             if (!WGRAD) {
               const CUtensorMap* mb = &p.sl[s].b;
               if (!gat) tma_load_2d(sa, &p.sl[s].a, fb, kc, ti.row0);
-              if (p.b4d) {
+              if (GRID) {
+                // one 64-row (K-major) / 64-column (MN-major) block per group
+                for (int x = 0; x < ti.nx; ++x) {
+                  if (!B_MN) tma_load_3d(sb + x * kChunkBytes, mb, fb, kc, 0, ti.g + x);
+                  else tma_load_3d(sb + x * kChunkBytes, mb, fb, 0, kc, ti.g + x);
+                }
+              } else if (p.b4d) {
                 // the whole B tile in one box: gate/up halves or MN chunks
                 if (!B_MN) tma_load_4d(sb, mb, fb, kc, ti.nt * (BN / 2), 0, ti.g);
                 else tma_load_4d(sb, mb, fb, 0, kc, ti.nt * (BN / 64), ti.g);
@@ -816,13 +947,17 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
     // Lane 0 waits and issues.  In the weight-gradient kernel the whole warp
     // runs this loop and zeroes the rows past a group's end in the group's
     // last K block; elsewhere lane 0 runs it alone.
-    constexpr uint32_t idesc = idesc_bf16(BM, BN, WGRAD, B_MN || WGRAD);
+    constexpr uint32_t idesc_full = idesc_bf16(BM, BN, WGRAD, B_MN || WGRAD);
+    constexpr uint32_t idesc_one = idesc_bf16(BM, 64, false, B_MN);  // grid pass of one group
     int stage = 0;
     uint32_t phase = 0;
     int local = 0;
     bool ok = true;
-    for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x, ++local) {
-      const TileInfo ti = tile_info<WGRAD, WGRAD>(p, t, tab);
+    for (Unit u = unit_first<GRID>(p, tab, num_tiles); u.t < num_tiles && ok;
+         unit_next<GRID>(u, p, tab, num_tiles), ++local) {
+      const TileInfo ti =
+          GRID ? grid_info(p, u.t, u.gt, u.ps, tab) : tile_info<WGRAD, WGRAD>(p, u.t, tab);
+      const uint32_t idesc = (GRID && ti.nx == 1) ? idesc_one : idesc_full;
       const int buf = local & 1;
       const uint32_t use = static_cast<uint32_t>(local >> 1);
       int w_ok = 1;
@@ -921,8 +1056,10 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
     const int hf = ew >> 2;   // column half owned by this warp
     const uint32_t stg = smem_u32(stage_tiles + ew * C::kStgBytes);
     int local = 0;
-    for (int t = blockIdx.x; t < num_tiles; t += gridDim.x, ++local) {
-      const TileInfo ti = tile_info<WGRAD>(p, t, tab);
+    for (Unit u = unit_first<GRID>(p, tab, num_tiles); u.t < num_tiles;
+         unit_next<GRID>(u, p, tab, num_tiles), ++local) {
+      const TileInfo ti =
+          GRID ? grid_info(p, u.t, u.gt, u.ps, tab) : tile_info<WGRAD>(p, u.t, tab);
       const int buf = local & 1;
       const uint32_t use = static_cast<uint32_t>(local >> 1);
       if (!mbar_wait(tfull_bar + buf, use & 1u, abort_flag, kWaitTimeoutNs)) break;
@@ -943,6 +1080,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
         epi_store<BN>(p, ti, tq, hf, row0, nrows, lane, stg);
       } else if constexpr (EPI == static_cast<int>(Epi::kLoRA)) {
         epi_lora<BN>(p, ti, tq, hf, row0, nrows, lane);
+      } else if constexpr (GRID) {
+        epi_lora_grid(p, ti, tq, hf, row0, lane);
       } else if constexpr (EPI == static_cast<int>(Epi::kDgradDn)) {
         epi_dgrad_dn<BN>(p, ti, tq, hf, row0, nrows, lane, stg);
       }
@@ -1027,6 +1166,12 @@ cudaError_t launch_gemm(const GemmShape& sh, const GemmParams& p, int num_sms, c
   if (sh.BN == 64 && e == kLo) {
     if (sh.b_mn) return launch_one<64, true, false, kLo>(p, num_sms, s);
     return launch_one<64, false, false, kLo>(p, num_sms, s);
+  }
+  constexpr int kLg = static_cast<int>(Epi::kLoRAGrid);
+  if (sh.BN == 128 && e == kLg) {
+    if (p.N > 64) return cudaErrorInvalidValue;  // one 64-column block per group
+    if (sh.b_mn) return launch_one<128, true, false, kLg>(p, num_sms, s);
+    return launch_one<128, false, false, kLg>(p, num_sms, s);
   }
   return cudaErrorInvalidValue;
 }

@@ -82,6 +82,8 @@ enum class Epi : int {
   kDgradDn = 4,  // SwiGLU backward from fp32 h (fin): dh pair (out0), dw partial (fout)
   kWgrad = 5,    // fp32 per-group weight gradient: acc[:, n] + acc[:, 64 + n]
   kWgradFull = 6,  // fp32 per-group full weight gradient: acc (B = one wide matrix)
+  kLoRAGrid = 7,   // as kLoRA (N <= 64) on the plain 128-row grid; up to two groups
+                   // per pass, their B blocks stacked (BN = 128)
 };
 
 constexpr int kMaxSlices = 4;
