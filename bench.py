@@ -116,6 +116,33 @@ def layer_counts(cfg, full_grads=False):
 AUX_STREAM_KERNELS = ("dB_dn", "dA_dn", "dw_reduce", "dB_gu", "dA_gu", "dW_dn", "dW_gu")
 
 
+def read_stream_gbs(torch, L, dev, reps=5):
+    """Rate at which this GPU streams reads alone: the library's read-stream
+    probe (32 KB bulk copies into shared memory, the GEMMs' copy engine, no
+    compute) over a 1 GiB buffer, L2 evicted before each call; median of
+    `reps` calls.  Context for read-dominated kernels: the copy peak in
+    MEASURED_PEAKS.json mixes reads and writes."""
+    x = torch.ones(1 << 29, dtype=torch.bfloat16, device=dev)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    L.moe_probe_read_stream(x)
+    times = []
+    for i in range(reps):
+        flush.fill_(i)
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record()
+        L.moe_probe_read_stream(x)
+        e1.record()
+        torch.cuda.synchronize()
+        times.append(e0.elapsed_time(e1))
+    if L.moe_status() != L.MOE_OK:
+        raise SystemExit("device status error in the read-stream probe")
+    times.sort()
+    del x, flush
+    torch.cuda.empty_cache()
+    return (1 << 30) / (times[len(times) // 2] / 1e3) / 1e9
+
+
 def kernel_roofline(name, flops, nbytes, dur_s, peaks):
     """Roofline of one launch: bound = whichever of the tensor time
     (flops / sustained bf16 peak) and the HBM time (bytes / copy peak) is
@@ -533,6 +560,7 @@ def run_ours(args):
         return None
 
     peaks, peak_src = load_peaks()
+    read_gbs = read_stream_gbs(torch, L, dev)
     tokens_s = world * cfg.T / (ms_max / 1e3)
     tflops = world * counts["flops"] / (ms_max / 1e3) / 1e12
     # dominant kernel and its roofline
@@ -547,6 +575,12 @@ def run_ours(args):
         roof["traffic"] = NCU_TRAFFIC_BYTES.get((dom, args.config))
         roof["peak_source"] = "%s (%s)" % (peak_src, "bf16 sustained" if roof["bound"] == "tensor"
                                            else "HBM copy")
+        if roof["bound"] == "hbm" and read_gbs:
+            roof["context"] = {"read_stream_gbs": round(read_gbs, 1),
+                               "frac_of_read_stream": roof["achieved"] / read_gbs,
+                               "read_stream_how": "moe_probe_read_stream: 32 KB bulk copies "
+                                                  "of a 1 GiB buffer into shared memory, no "
+                                                  "compute, L2 evicted, median of 5"}
     route = None
     if "route" in kstats:
         rb = counts["kernels"]["route"][1]

@@ -30,7 +30,7 @@ EXPORTED = (
     "moe_permute", "moe_unpermute_combine", "moe_lora_grouped_mlp_fwd",
     "moe_mlp_bwd_workspace_size", "moe_lora_grouped_mlp_bwd", "moe_status",
     "moe_last_error", "moe_abi_version", "moe_kernel_name", "moe_probe_arm", "moe_probe_count",
-    "moe_route_noalloc", "moe_selftest_wait_timeout",
+    "moe_route_noalloc", "moe_selftest_wait_timeout", "moe_probe_read_stream",
 )
 
 
@@ -92,6 +92,7 @@ def load(path: str = LIB_PATH):
                                              ctypes.POINTER(_P), _I]),
             "moe_probe_count": (_I, [ctypes.c_char_p]),
             "moe_route_noalloc": (ctypes.c_int, [_P, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P]),
+            "moe_probe_read_stream": (ctypes.c_int, [_P, _SZ, _P]),
         }
         for name, (res, args) in sig.items():
             fn = getattr(lib, name)
@@ -149,6 +150,12 @@ def moe_router_topk(logits, k, ids, weights, stream=None):
     T, E = logits.shape
     _check(load().moe_router_topk(_f32(logits, "logits"), T, E, int(k), _i32(ids, "ids"),
                                   _f32(weights, "weights"), _stream(stream)), "moe_router_topk")
+
+
+def moe_probe_read_stream(buf, stream=None):
+    """Stream the bytes of a device tensor into shared memory (measurement)."""
+    _check(load().moe_probe_read_stream(_ptr(buf, name="buf"), buf.numel() * buf.element_size(),
+                                        _stream(stream)), "moe_probe_read_stream")
 
 
 def moe_route_workspace_size(T, K, G) -> int:

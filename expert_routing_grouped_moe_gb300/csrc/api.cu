@@ -424,6 +424,19 @@ int moe_selftest_wait_timeout(uint32_t timeout_us, moe_stream_t stream) {
   return ok();
 }
 
+int moe_probe_read_stream(const void* src, size_t bytes, moe_stream_t stream) {
+  if (src == nullptr || !aligned16(src)) return fail(MOE_ERR_INVALID_ARG, "src NULL or misaligned");
+  if (bytes == 0 || bytes % 16 != 0 || bytes > (size_t(1) << 40))
+    return fail(MOE_ERR_INVALID_ARG, "bytes must be a positive multiple of 16");
+  DevState* st = nullptr;
+  int rc = device_state(&st);
+  if (rc) return rc;
+  const cudaError_t e = launch_read_stream(src, static_cast<int64_t>(bytes), st->num_sms,
+                                           st->status, stream);
+  if (e != cudaSuccess) return cuda_fail(e, "read-stream probe launch");
+  return ok();
+}
+
 int moe_router_topk(const float* logits, int32_t T, int32_t E, int32_t k, int32_t* ids,
                     float* weights, moe_stream_t stream) {
   if (logits == nullptr || ids == nullptr || weights == nullptr)

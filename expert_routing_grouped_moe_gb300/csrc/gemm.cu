@@ -82,7 +82,7 @@ struct Cfg {
   static constexpr uint32_t kRingFit =
       (kSmemMax - kFixedSmem - kEpiWarps * kStgBytes) / kStageBytes * kStageBytes;
   static constexpr uint32_t kRingCap = kGrid ? kRingFit : kRingMax;
-  // 4 / 4 / 6 / 8 stages for BN 256 / 192 (dgrad) / 128 / 64; 7 in grid mode
+  // 4 / 4 / 6 stages for BN 256 / 192 (dgrad) / 128 (weight gradients); 7 in grid mode
   static constexpr int kStages = (kRingFit < kRingCap ? kRingFit : kRingCap) / kStageBytes;
   static constexpr uint32_t kTmemCols = pow2_at_least(2 * BN);  // power of two >= 32
   static constexpr size_t kSmemBytes =
@@ -553,30 +553,6 @@ __device__ __forceinline__ void epi_dgrad_dn(const GemmParams& p, const TileInfo
   }
   if (lane < nrows)
     p.fout[static_cast<int64_t>(ti.nt * kDwPartsPerTile + hf) * p.fstride + row0 + lane] = dot;
-}
-
-template <int BN>
-__device__ __forceinline__ void epi_lora(const GemmParams& p, const TileInfo& ti, uint32_t tq,
-                                         int hf, int64_t row0, int nrows, int lane) {
-  // out0 = s * acc as a hi/lo pair
-  const int64_t row = row0 + lane;
-  const bool valid = lane < nrows;
-  const float s = p.scale;
-#pragma unroll 1
-  for (int c0 = hf * (BN / 2); c0 < (hf + 1) * (BN / 2); c0 += 16) {
-    float v16[16];
-    tmem_ld16(tq + c0, v16);
-#pragma unroll
-    for (int h8 = 0; h8 < 2; ++h8) {
-      const int j = ti.nt * BN + c0 + h8 * 8;
-      if (valid && j < p.N) {
-        float ov[8];
-#pragma unroll
-        for (int i = 0; i < 8; ++i) ov[i] = s * v16[h8 * 8 + i];
-        store8_pair(p.out0 + row * p.ld0 + j, p.pair, ov);
-      }
-    }
-  }
 }
 
 // Grid mode: out0 = s * acc as a hi/lo pair for the rows of this pass; a
@@ -1078,8 +1054,6 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
         epi_swiglu<BN>(p, ti, tq, hf, row0, nrows, lane, stg);
       } else if constexpr (EPI == static_cast<int>(Epi::kStore)) {
         epi_store<BN>(p, ti, tq, hf, row0, nrows, lane, stg);
-      } else if constexpr (EPI == static_cast<int>(Epi::kLoRA)) {
-        epi_lora<BN>(p, ti, tq, hf, row0, nrows, lane);
       } else if constexpr (GRID) {
         epi_lora_grid(p, ti, tq, hf, row0, lane);
       } else if constexpr (EPI == static_cast<int>(Epi::kDgradDn)) {
@@ -1142,7 +1116,6 @@ cudaError_t launch_wait_selftest(int* status, uint64_t timeout_ns, cudaStream_t 
 cudaError_t launch_gemm(const GemmShape& sh, const GemmParams& p, int num_sms, cudaStream_t s) {
   constexpr int kSw = static_cast<int>(Epi::kSwiGLU);
   constexpr int kSt = static_cast<int>(Epi::kStore);
-  constexpr int kLo = static_cast<int>(Epi::kLoRA);
   constexpr int kDd = static_cast<int>(Epi::kDgradDn);
   constexpr int kWg = static_cast<int>(Epi::kWgrad);
   const int e = static_cast<int>(sh.epi);
@@ -1163,10 +1136,6 @@ cudaError_t launch_gemm(const GemmShape& sh, const GemmParams& p, int num_sms, c
   }
   if (sh.BN == kDgradBN && sh.b_mn && e == kDd)
     return launch_one<kDgradBN, true, false, kDd>(p, num_sms, s);
-  if (sh.BN == 64 && e == kLo) {
-    if (sh.b_mn) return launch_one<64, true, false, kLo>(p, num_sms, s);
-    return launch_one<64, false, false, kLo>(p, num_sms, s);
-  }
   constexpr int kLg = static_cast<int>(Epi::kLoRAGrid);
   if (sh.BN == 128 && e == kLg) {
     if (p.N > 64) return cudaErrorInvalidValue;  // one 64-column block per group

@@ -78,12 +78,11 @@ cudaError_t launch_sum_parts(const float* parts, int nparts, int64_t stride, int
 enum class Epi : int {
   kSwiGLU = 0,   // h = acc (fp32, gate|up halves), act' = w*silu(gate)*up as a hi/lo pair
   kStore = 2,    // out0 = bf16(acc)
-  kLoRA = 3,     // out0 = s*acc as a hi/lo pair
   kDgradDn = 4,  // SwiGLU backward from fp32 h (fin): dh pair (out0), dw partial (fout)
   kWgrad = 5,    // fp32 per-group weight gradient: acc[:, n] + acc[:, 64 + n]
   kWgradFull = 6,  // fp32 per-group full weight gradient: acc (B = one wide matrix)
-  kLoRAGrid = 7,   // as kLoRA (N <= 64) on the plain 128-row grid; up to two groups
-                   // per pass, their B blocks stacked (BN = 128)
+  kLoRAGrid = 7,   // out0 = s*acc as a hi/lo pair (N <= 64), on the plain 128-row
+                   // grid; up to two groups per pass, their B blocks stacked (BN = 128)
 };
 
 constexpr int kMaxSlices = 4;
@@ -139,7 +138,7 @@ struct GemmParams {
   int* status;
 };
 
-// Kernel shapes: BN in {64, 128, 192, 256}; B operand K-major or MN-major; two modes.
+// Kernel shapes: BN in {128, 192, 256}; B operand K-major or MN-major; two modes.
 struct GemmShape {
   int BN;
   bool b_mn;
@@ -149,6 +148,12 @@ struct GemmShape {
 
 cudaError_t launch_gemm(const GemmShape& shape, const GemmParams& p, int num_sms,
                         cudaStream_t s);
+// ---- read-stream probe (probe.cu) ------------------------------------------
+// Streams `bytes` (a multiple of 16) from src (16-byte aligned) into shared
+// memory with bulk copies, one CTA per SM, and discards them.
+cudaError_t launch_read_stream(const void* src, int64_t bytes, int num_sms, int* status,
+                               cudaStream_t s);
+
 // One thread waits on an mbarrier nothing arrives on, bounded by timeout_ns,
 // then records kErrTimeout in *status (the failure path of every pipeline wait).
 cudaError_t launch_wait_selftest(int* status, uint64_t timeout_ns, cudaStream_t s);

@@ -293,6 +293,17 @@ MOE_API const char* moe_last_error(void);
  * MOE_ERR_INVALID_ARG for a timeout out of range. */
 MOE_API int moe_selftest_wait_timeout(uint32_t timeout_us, moe_stream_t stream);
 
+/* Read-stream probe (measurement): reads `bytes` of device memory at `src`
+ * into shared memory with 32 KB bulk asynchronous copies -- the copy engine
+ * the grouped GEMMs load their operands with -- one CTA per SM, and
+ * discards them.  Timing it (caller-owned events on `stream`) gives the rate
+ * at which this GPU streams reads alone, the ceiling for read-dominated
+ * kernels (a copy peak mixes reads and writes).  src: device pointer, 16-byte
+ * aligned; bytes: > 0, a multiple of 16.  Returns MOE_OK once enqueued,
+ * MOE_ERR_INVALID_ARG for a bad pointer or size.  Its waits are bounded like
+ * the GEMMs' (MOE_ERR_TIMEOUT in the status word). */
+MOE_API int moe_probe_read_stream(const void* src, size_t bytes, moe_stream_t stream);
+
 /* ------------------------------------------------------------------------ */
 /* Tracing: timing probe                                                     */
 /* ------------------------------------------------------------------------ */

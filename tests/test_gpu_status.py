@@ -37,3 +37,12 @@ def test_bounded_wait_times_out_and_context_survives():
     assert L.moe_status() == L.MOE_OK
     P = oracle_params(wts, cfg)
     assert_close_bf16(to64(Y), oracle.layer_forward(to64(act["X"]), ids_np, w_np, P), "Y")
+
+
+def test_read_stream_probe_runs_and_reports_ok():
+    """The read-stream probe (a measurement kernel) streams a buffer whose
+    size is not a multiple of its 32 KB copy and leaves the status clean."""
+    buf = torch.empty((64 << 20) + 48, dtype=torch.uint8, device="cuda")
+    L.moe_probe_read_stream(buf)
+    torch.cuda.synchronize()
+    assert L.moe_status() == L.MOE_OK

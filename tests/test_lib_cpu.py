@@ -43,6 +43,15 @@ def test_sizes(lib):
     assert lib.moe_route_workspace_size(0, 8, 128) == 0
 
 
+def test_read_stream_probe_argument_checks(lib):
+    from expert_routing_grouped_moe_gb300 import _lib
+    assert lib.moe_probe_read_stream(None, 1024, None) == _lib.MOE_ERR_INVALID_ARG
+    assert lib.moe_probe_read_stream(ctypes.c_void_p(4096 + 8), 1024, None) == \
+        _lib.MOE_ERR_INVALID_ARG
+    assert lib.moe_probe_read_stream(ctypes.c_void_p(4096), 0, None) == _lib.MOE_ERR_INVALID_ARG
+    assert lib.moe_probe_read_stream(ctypes.c_void_p(4096), 100, None) == _lib.MOE_ERR_INVALID_ARG
+
+
 def _dims(**kw):
     from expert_routing_grouped_moe_gb300 import _lib
     base = dict(T=256, d=128, f=64, E=8, k=2, r=8, lora_scale=2.0, shared_expert=0)
