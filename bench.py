@@ -117,30 +117,34 @@ AUX_STREAM_KERNELS = ("dB_dn", "dA_dn", "dw_reduce", "dB_gu", "dA_gu", "dW_dn", 
 
 
 def read_stream_gbs(torch, L, dev, reps=5):
-    """Rate at which this GPU streams reads alone: the library's read-stream
-    probe (32 KB bulk copies into shared memory, the GEMMs' copy engine, no
-    compute) over a 1 GiB buffer, L2 evicted before each call; median of
-    `reps` calls.  Context for read-dominated kernels: the copy peak in
-    MEASURED_PEAKS.json mixes reads and writes."""
+    """Rates at which this GPU streams reads alone, from the library's
+    read-stream probe over a 1 GiB buffer (no compute), L2 evicted before each
+    call, median of `reps` calls: linear 32 KB bulk copies, and GEMM-operand
+    tiles (TMA boxes of 128 rows x 128 bytes, each SM on its own rows).
+    Context for read-dominated kernels: the copy peak in MEASURED_PEAKS.json
+    mixes reads and writes."""
     x = torch.ones(1 << 29, dtype=torch.bfloat16, device=dev)
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
-    L.moe_probe_read_stream(x)
-    times = []
-    for i in range(reps):
-        flush.fill_(i)
-        e0 = torch.cuda.Event(enable_timing=True)
-        e1 = torch.cuda.Event(enable_timing=True)
-        e0.record()
-        L.moe_probe_read_stream(x)
-        e1.record()
-        torch.cuda.synchronize()
-        times.append(e0.elapsed_time(e1))
+    out = {}
+    for name, pattern in (("linear", L.MOE_PROBE_LINEAR), ("tiles", L.MOE_PROBE_TILES)):
+        L.moe_probe_read_stream(x, pattern)
+        times = []
+        for i in range(reps):
+            flush.fill_(i)
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record()
+            L.moe_probe_read_stream(x, pattern)
+            e1.record()
+            torch.cuda.synchronize()
+            times.append(e0.elapsed_time(e1))
+        times.sort()
+        out[name] = (1 << 30) / (times[len(times) // 2] / 1e3) / 1e9
     if L.moe_status() != L.MOE_OK:
         raise SystemExit("device status error in the read-stream probe")
-    times.sort()
     del x, flush
     torch.cuda.empty_cache()
-    return (1 << 30) / (times[len(times) // 2] / 1e3) / 1e9
+    return out
 
 
 def kernel_roofline(name, flops, nbytes, dur_s, peaks):
@@ -576,11 +580,13 @@ def run_ours(args):
         roof["peak_source"] = "%s (%s)" % (peak_src, "bf16 sustained" if roof["bound"] == "tensor"
                                            else "HBM copy")
         if roof["bound"] == "hbm" and read_gbs:
-            roof["context"] = {"read_stream_gbs": round(read_gbs, 1),
-                               "frac_of_read_stream": roof["achieved"] / read_gbs,
-                               "read_stream_how": "moe_probe_read_stream: 32 KB bulk copies "
-                                                  "of a 1 GiB buffer into shared memory, no "
-                                                  "compute, L2 evicted, median of 5"}
+            roof["context"] = {
+                "read_stream_gbs": {k: round(v, 1) for k, v in read_gbs.items()},
+                "frac_of_read_stream": {k: roof["achieved"] / v for k, v in read_gbs.items()},
+                "read_stream_how": "moe_probe_read_stream over 1 GiB, no compute, L2 evicted, "
+                                   "median of 5: linear = 32 KB bulk copies, neighbouring SMs "
+                                   "on neighbouring chunks; tiles = TMA boxes of 128 rows x "
+                                   "128 B, each SM on its own rows (a GEMM operand's pattern)"}
     route = None
     if "route" in kstats:
         rb = counts["kernels"]["route"][1]

@@ -24,6 +24,8 @@ MOE_ERR_WORKSPACE = -3
 MOE_ERR_CUDA = -4
 MOE_ERR_BAD_IDS = -5
 MOE_ERR_TIMEOUT = -6
+MOE_PROBE_LINEAR = 0
+MOE_PROBE_TILES = 1
 
 EXPORTED = (
     "moe_router_topk", "moe_route_workspace_size", "moe_route",
@@ -92,7 +94,7 @@ def load(path: str = LIB_PATH):
                                              ctypes.POINTER(_P), _I]),
             "moe_probe_count": (_I, [ctypes.c_char_p]),
             "moe_route_noalloc": (ctypes.c_int, [_P, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P]),
-            "moe_probe_read_stream": (ctypes.c_int, [_P, _SZ, _P]),
+            "moe_probe_read_stream": (ctypes.c_int, [_P, _SZ, _I, _P]),
         }
         for name, (res, args) in sig.items():
             fn = getattr(lib, name)
@@ -152,10 +154,11 @@ def moe_router_topk(logits, k, ids, weights, stream=None):
                                   _f32(weights, "weights"), _stream(stream)), "moe_router_topk")
 
 
-def moe_probe_read_stream(buf, stream=None):
-    """Stream the bytes of a device tensor into shared memory (measurement)."""
+def moe_probe_read_stream(buf, pattern=0, stream=None):
+    """Stream the bytes of a device tensor into shared memory (measurement);
+    pattern MOE_PROBE_LINEAR or MOE_PROBE_TILES."""
     _check(load().moe_probe_read_stream(_ptr(buf, name="buf"), buf.numel() * buf.element_size(),
-                                        _stream(stream)), "moe_probe_read_stream")
+                                        int(pattern), _stream(stream)), "moe_probe_read_stream")
 
 
 def moe_route_workspace_size(T, K, G) -> int:

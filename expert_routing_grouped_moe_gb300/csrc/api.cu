@@ -424,15 +424,23 @@ int moe_selftest_wait_timeout(uint32_t timeout_us, moe_stream_t stream) {
   return ok();
 }
 
-int moe_probe_read_stream(const void* src, size_t bytes, moe_stream_t stream) {
+int moe_probe_read_stream(const void* src, size_t bytes, int32_t pattern, moe_stream_t stream) {
   if (src == nullptr || !aligned16(src)) return fail(MOE_ERR_INVALID_ARG, "src NULL or misaligned");
-  if (bytes == 0 || bytes % 16 != 0 || bytes > (size_t(1) << 40))
-    return fail(MOE_ERR_INVALID_ARG, "bytes must be a positive multiple of 16");
+  if (pattern != MOE_PROBE_LINEAR && pattern != MOE_PROBE_TILES)
+    return fail(MOE_ERR_INVALID_ARG, "pattern must be MOE_PROBE_LINEAR or MOE_PROBE_TILES");
+  const size_t unit = pattern == MOE_PROBE_TILES ? size_t(128) * 4096 : 16;
+  if (bytes == 0 || bytes % unit != 0 || bytes > (size_t(1) << 40))
+    return fail(MOE_ERR_INVALID_ARG, "bytes must be a positive multiple of %zu", unit);
   DevState* st = nullptr;
   int rc = device_state(&st);
   if (rc) return rc;
-  const cudaError_t e = launch_read_stream(src, static_cast<int64_t>(bytes), st->num_sms,
-                                           st->status, stream);
+  CUtensorMap map;
+  if (pattern == MOE_PROBE_TILES && !make_map_2d(&map, src, bytes / 4096, 2048, 128, 64))
+    return fail(MOE_ERR_CUDA, "tensor map encode failed (probe)");
+  const cudaError_t e =
+      launch_read_stream(src, static_cast<int64_t>(bytes),
+                         pattern == MOE_PROBE_TILES ? &map : nullptr, st->num_sms, st->status,
+                         stream);
   if (e != cudaSuccess) return cuda_fail(e, "read-stream probe launch");
   return ok();
 }

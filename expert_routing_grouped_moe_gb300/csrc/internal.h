@@ -149,10 +149,13 @@ struct GemmShape {
 cudaError_t launch_gemm(const GemmShape& shape, const GemmParams& p, int num_sms,
                         cudaStream_t s);
 // ---- read-stream probe (probe.cu) ------------------------------------------
-// Streams `bytes` (a multiple of 16) from src (16-byte aligned) into shared
-// memory with bulk copies, one CTA per SM, and discards them.
-cudaError_t launch_read_stream(const void* src, int64_t bytes, int num_sms, int* status,
-                               cudaStream_t s);
+// Streams `bytes` from src into shared memory, one CTA per SM, and discards
+// them: linear 32 KB bulk copies (tiles_map NULL; src 16-byte aligned, bytes
+// a multiple of 16), or GEMM-operand tiles through tiles_map, a 128B-swizzled
+// bf16 map of src as [bytes / 4096, 2048] with 128 x 64 boxes (bytes a
+// multiple of 128 * 4096).
+cudaError_t launch_read_stream(const void* src, int64_t bytes, const CUtensorMap* tiles_map,
+                               int num_sms, int* status, cudaStream_t s);
 
 // One thread waits on an mbarrier nothing arrives on, bounded by timeout_ns,
 // then records kErrTimeout in *status (the failure path of every pipeline wait).

@@ -294,15 +294,23 @@ MOE_API const char* moe_last_error(void);
 MOE_API int moe_selftest_wait_timeout(uint32_t timeout_us, moe_stream_t stream);
 
 /* Read-stream probe (measurement): reads `bytes` of device memory at `src`
- * into shared memory with 32 KB bulk asynchronous copies -- the copy engine
- * the grouped GEMMs load their operands with -- one CTA per SM, and
- * discards them.  Timing it (caller-owned events on `stream`) gives the rate
- * at which this GPU streams reads alone, the ceiling for read-dominated
- * kernels (a copy peak mixes reads and writes).  src: device pointer, 16-byte
- * aligned; bytes: > 0, a multiple of 16.  Returns MOE_OK once enqueued,
- * MOE_ERR_INVALID_ARG for a bad pointer or size.  Its waits are bounded like
- * the GEMMs' (MOE_ERR_TIMEOUT in the status word). */
-MOE_API int moe_probe_read_stream(const void* src, size_t bytes, moe_stream_t stream);
+ * into shared memory with the asynchronous copies the grouped GEMMs load
+ * their operands with, one CTA per SM, computes nothing and discards them.
+ * Timing it (caller-owned events on `stream`) gives the rate at which this
+ * GPU streams reads alone -- the ceiling for read-dominated kernels, which a
+ * copy peak (reads and writes mixed) does not show.  Patterns:
+ *   MOE_PROBE_LINEAR  32 KB bulk copies, neighbouring CTAs on neighbouring
+ *                     chunks; bytes a multiple of 16
+ *   MOE_PROBE_TILES   src as a [bytes/4096, 2048] bf16 matrix read the way a
+ *                     GEMM reads an operand: 128B-swizzled TMA boxes of 128
+ *                     rows x 64 columns, each CTA over the whole K extent of
+ *                     its own 128-row blocks; bytes a multiple of 512 KiB
+ * src: device pointer, 16-byte aligned.  Returns MOE_OK once enqueued,
+ * MOE_ERR_INVALID_ARG for a bad pointer, pattern or size.  Its waits are
+ * bounded like the GEMMs' (MOE_ERR_TIMEOUT in the status word). */
+enum { MOE_PROBE_LINEAR = 0, MOE_PROBE_TILES = 1 };
+MOE_API int moe_probe_read_stream(const void* src, size_t bytes, int32_t pattern,
+                                  moe_stream_t stream);
 
 /* ------------------------------------------------------------------------ */
 /* Tracing: timing probe                                                     */

@@ -41,8 +41,11 @@ def test_bounded_wait_times_out_and_context_survives():
 
 def test_read_stream_probe_runs_and_reports_ok():
     """The read-stream probe (a measurement kernel) streams a buffer whose
-    size is not a multiple of its 32 KB copy and leaves the status clean."""
+    size is not a multiple of its 32 KB stage, and a buffer as GEMM-operand
+    tiles, and leaves the status clean."""
     buf = torch.empty((64 << 20) + 48, dtype=torch.uint8, device="cuda")
-    L.moe_probe_read_stream(buf)
+    L.moe_probe_read_stream(buf, L.MOE_PROBE_LINEAR)
+    tiles = torch.empty(300 * (128 * 4096), dtype=torch.uint8, device="cuda")
+    L.moe_probe_read_stream(tiles, L.MOE_PROBE_TILES)
     torch.cuda.synchronize()
     assert L.moe_status() == L.MOE_OK

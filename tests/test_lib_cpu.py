@@ -45,11 +45,15 @@ def test_sizes(lib):
 
 def test_read_stream_probe_argument_checks(lib):
     from expert_routing_grouped_moe_gb300 import _lib
-    assert lib.moe_probe_read_stream(None, 1024, None) == _lib.MOE_ERR_INVALID_ARG
-    assert lib.moe_probe_read_stream(ctypes.c_void_p(4096 + 8), 1024, None) == \
-        _lib.MOE_ERR_INVALID_ARG
-    assert lib.moe_probe_read_stream(ctypes.c_void_p(4096), 0, None) == _lib.MOE_ERR_INVALID_ARG
-    assert lib.moe_probe_read_stream(ctypes.c_void_p(4096), 100, None) == _lib.MOE_ERR_INVALID_ARG
+    lin, til = _lib.MOE_PROBE_LINEAR, _lib.MOE_PROBE_TILES
+    bad = _lib.MOE_ERR_INVALID_ARG
+    assert lib.moe_probe_read_stream(None, 1024, lin, None) == bad
+    assert lib.moe_probe_read_stream(ctypes.c_void_p(4096 + 8), 1024, lin, None) == bad
+    assert lib.moe_probe_read_stream(ctypes.c_void_p(4096), 0, lin, None) == bad
+    assert lib.moe_probe_read_stream(ctypes.c_void_p(4096), 100, lin, None) == bad
+    assert lib.moe_probe_read_stream(ctypes.c_void_p(4096), 1024, 2, None) == bad
+    # tiles: whole 128-row blocks of a [rows, 2048] bf16 matrix (512 KiB each)
+    assert lib.moe_probe_read_stream(ctypes.c_void_p(4096), 1 << 18, til, None) == bad
 
 
 def _dims(**kw):
