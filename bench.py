@@ -267,6 +267,12 @@ def max_over_ranks(torch, dist, value, device):
     return float(t.item())
 
 
+def replica_throughput(world, tokens_per_rank, ms_max):
+    """Whole-job tokens/s of `world` replicas that each process
+    `tokens_per_rank` tokens per step, timed by the slowest rank."""
+    return world * tokens_per_rank / (ms_max / 1e3)
+
+
 def barrier(dist, torch, device):
     if dist is not None:
         if device.type == "cuda":
@@ -565,7 +571,7 @@ def run_ours(args):
 
     peaks, peak_src = load_peaks()
     read_gbs = read_stream_gbs(torch, L, dev)
-    tokens_s = world * cfg.T / (ms_max / 1e3)
+    tokens_s = replica_throughput(world, cfg.T, ms_max)
     tflops = world * counts["flops"] / (ms_max / 1e3) / 1e12
     # dominant kernel and its roofline
     # dominant kernel (largest share of the step among the main-stream
