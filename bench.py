@@ -38,7 +38,7 @@ PEAKS_FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # dram__bytes_read.sum + dram__bytes_write.sum of one launch of the dominant
 # kernel, read from one ncu --set full capture of the current kernel
 # (kernel, workload)
-NCU_TRAFFIC_BYTES = {("gate_up", "qwen3_30b_a3b"): 1018265600 + 273068544}
+NCU_TRAFFIC_BYTES = {("gate_up", "qwen3_30b_a3b"): 1030659840 + 273544960}
 
 
 def parse_args(argv=None):
