@@ -41,6 +41,12 @@ PEAKS_FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 NCU_TRAFFIC_BYTES = {("gate_up", "qwen3_30b_a3b"): 1030659840 + 273544960}
 
 
+def workload(synth, args):
+    """The named layer workload, with T replaced when --tokens is given."""
+    cfg = synth.CONFIGS[args.config]
+    return synth.scaled(cfg, T=args.tokens) if args.tokens > 0 else cfg
+
+
 def parse_args(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -48,6 +54,8 @@ def parse_args(argv=None):
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--config", default="qwen3_30b_a3b")
+    ap.add_argument("--tokens", type=int, default=0,
+                    help="override the workload's token count T (0: the workload's own)")
     ap.add_argument("--seed", type=int, default=1)
     ap.add_argument("--e2e-steps", type=int, default=0, help="0: same as --steps (capped)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -485,7 +493,7 @@ def run_ours(args):
     torch.cuda.set_device(dev)
     build.build()
     L.load()
-    cfg = synth.CONFIGS[args.config]
+    cfg = workload(synth, args)
     seed = args.seed + 1000 * rank
     weights = synth.layer_weights(cfg, seed, device=dev)
     act = synth.layer_activations(cfg, seed, device=dev)
@@ -582,7 +590,8 @@ def run_ours(args):
     if dom is not None:
         fl, nb = counts["kernels"][dom]
         roof = kernel_roofline(dom, fl, nb, kstats[dom]["ms_per_launch"] / 1e3, peaks)
-        roof["traffic"] = NCU_TRAFFIC_BYTES.get((dom, args.config))
+        # the ncu figure holds for the workload's own T only
+        roof["traffic"] = NCU_TRAFFIC_BYTES.get((dom, args.config)) if args.tokens <= 0 else None
         roof["peak_source"] = "%s (%s)" % (peak_src, "bf16 sustained" if roof["bound"] == "tensor"
                                            else "HBM copy")
         if roof["bound"] == "hbm" and read_gbs:
@@ -620,8 +629,9 @@ def run_ours(args):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_max,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic (seeded; random-init weights of the layer shape)",
-        "config": {"workload": "%s-shaped MoE-LoRA layer fwd+bwd%s" % (
-                       cfg.name, " with full weight gradients" if args.full_grads else ""),
+        "config": {"workload": "%s-shaped MoE-LoRA layer fwd+bwd%s%s" % (
+                       cfg.name, " with full weight gradients" if args.full_grads else "",
+                       " at T=%d" % cfg.T if args.tokens > 0 else ""),
                    "T": cfg.T,
                    "d": cfg.d, "f": cfg.f, "E": cfg.E, "k": cfg.k, "r": cfg.r,
                    "alpha": cfg.alpha, "shared_expert": cfg.shared,
@@ -659,7 +669,7 @@ def run_reference(args):
     import numpy as np
     import oracle
     from expert_routing_grouped_moe_gb300 import synth
-    cfg = synth.CONFIGS[args.config]
+    cfg = workload(synth, args)
     weights = synth.layer_weights(cfg, args.seed, device="cpu")
     act = synth.layer_activations(cfg, args.seed, device="cpu")
     ids, w = oracle.router_topk(act["logits"].numpy(), cfg.k)
@@ -686,8 +696,9 @@ def run_reference(args):
         "n_gpus": int(os.environ.get("WORLD_SIZE", "1")), "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": "%s-shaped MoE-LoRA layer fwd+bwd%s" % (
-                       cfg.name, " with full weight gradients" if args.full_grads else ""),
+        "config": {"workload": "%s-shaped MoE-LoRA layer fwd+bwd%s%s" % (
+                       cfg.name, " with full weight gradients" if args.full_grads else "",
+                       " at T=%d" % cfg.T if args.tokens > 0 else ""),
                    "T": cfg.T,
                    "d": cfg.d, "f": cfg.f, "E": cfg.E, "k": cfg.k, "r": cfg.r},
         "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cpu_cores(),
