@@ -74,7 +74,7 @@ typedef struct CUstream_st* moe_stream_t;  /* same type as cudaStream_t */
 typedef enum {
   MOE_OK = 0,
   MOE_ERR_INVALID_ARG = -1, /* null pointer, bad size, misaligned pointer */
-  MOE_ERR_UNSUPPORTED = -2, /* valid but outside what this build supports */
+  MOE_ERR_UNSUPPORTED = -2, /* valid but outside what this library supports */
   MOE_ERR_WORKSPACE = -3,   /* workspace too small */
   MOE_ERR_CUDA = -4,        /* a CUDA runtime / driver call failed */
   MOE_ERR_BAD_IDS = -5,     /* (device) an expert id outside [0,E) was seen */
