@@ -2,7 +2,8 @@
 
 d, f and r are drawn as any multiple of 8 in range, E, k and T at random, with
 or without a shared expert, in the permuted or the gathered-row mode, and
-sometimes with an expert id repeated inside a token.  Tiles, K slices, TMA
+sometimes with an expert id repeated inside a token; the shapes in the
+permuted-row mode also compute the full weight gradients.  Tiles, K slices, TMA
 boxes, grid-mode passes and epilogue masks thus meet shapes that no
 hand-written case picked.  Every element of Y, dX, dw and the four LoRA
 gradients is compared."""
@@ -55,8 +56,10 @@ def test_random_shape_matches_oracle(sh):
         w_np = synth.combine_weights(cfg.T, cfg.k, seed=seed).numpy()
     else:
         ids_np, w_np = oracle.router_topk(act["logits"].cpu().numpy(), cfg.k)
+    full = not sh["gather"]  # the full weight gradients need the permuted rows
     layer = MoELoRALayer(cfg.T, cfg.d, cfg.f, cfg.E, cfg.k, cfg.r, cfg.alpha, wts,
-                         shared_expert=cfg.shared, device=DEV, gather=sh["gather"])
+                         shared_expert=cfg.shared, device=DEV, gather=sh["gather"],
+                         full_grads=full)
     ids = torch.from_numpy(np.ascontiguousarray(ids_np, dtype=np.int32)).to(DEV)
     w = torch.from_numpy(np.ascontiguousarray(w_np, dtype=np.float32)).to(DEV)
     Y = layer.forward(act["X"], ids, w).clone()
@@ -66,8 +69,8 @@ def test_random_shape_matches_oracle(sh):
     X, dY = to64(act["X"]), to64(act["dY"])
     tag = sh["name"]
     assert_close_bf16(to64(Y), oracle.layer_forward(X, ids_np, w_np, P), tag + " Y")
-    ref = oracle.layer_backward(X, ids_np, w_np, dY, P)
+    ref = oracle.layer_backward(X, ids_np, w_np, dY, P, full=full)
     assert_close_bf16(to64(g["dX"]), ref["dX"], tag + " dX")
     assert_close_bf16(g["dw"].cpu().numpy(), ref["dw"], tag + " dw")
-    for n in ("dA_gu", "dB_gu", "dA_dn", "dB_dn"):
+    for n in ("dA_gu", "dB_gu", "dA_dn", "dB_dn") + (("dW_gu", "dW_dn") if full else ()):
         assert_close_bf16(g[n].cpu().numpy(), ref[n], tag + " " + n)
