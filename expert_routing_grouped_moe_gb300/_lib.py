@@ -33,6 +33,7 @@ EXPORTED = (
     "moe_mlp_bwd_workspace_size", "moe_lora_grouped_mlp_bwd", "moe_status",
     "moe_last_error", "moe_abi_version", "moe_kernel_name", "moe_probe_arm", "moe_probe_count",
     "moe_route_noalloc", "moe_selftest_wait_timeout", "moe_probe_read_stream",
+    "moe_route_kernel_count",
 )
 
 
@@ -95,6 +96,7 @@ def load(path: str = LIB_PATH):
             "moe_probe_count": (_I, [ctypes.c_char_p]),
             "moe_route_noalloc": (ctypes.c_int, [_P, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P]),
             "moe_probe_read_stream": (ctypes.c_int, [_P, _SZ, _I, _P]),
+            "moe_route_kernel_count": (_I, [_I, _I, _I]),
         }
         for name, (res, args) in sig.items():
             fn = getattr(lib, name)
@@ -159,6 +161,13 @@ def moe_probe_read_stream(buf, pattern=0, stream=None):
     pattern MOE_PROBE_LINEAR or MOE_PROBE_TILES."""
     _check(load().moe_probe_read_stream(_ptr(buf, name="buf"), buf.numel() * buf.element_size(),
                                         int(pattern), _stream(stream)), "moe_probe_read_stream")
+
+
+def moe_route_kernel_count(T, K, G) -> int:
+    """Kernels moe_route launches for this shape (2 or 3)."""
+    n = int(load().moe_route_kernel_count(int(T), int(K), int(G)))
+    _check(n if n < 0 else MOE_OK, "moe_route_kernel_count")
+    return n
 
 
 def moe_route_workspace_size(T, K, G) -> int:

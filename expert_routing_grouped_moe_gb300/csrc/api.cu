@@ -399,6 +399,12 @@ size_t moe_route_workspace_size(int32_t T, int32_t K, int32_t G) {
   return route_ws_bytes(static_cast<int64_t>(T) * K, G);
 }
 
+int32_t moe_route_kernel_count(int32_t T, int32_t K, int32_t G) {
+  if (T <= 0 || K <= 0 || G <= 0) return fail(MOE_ERR_INVALID_ARG, "bad T/K/G");
+  ok();
+  return route_kernel_count(static_cast<int64_t>(T) * K, G);
+}
+
 int moe_status(moe_stream_t stream) {
   DevState* st = nullptr;
   int rc = device_state(&st);

@@ -59,6 +59,10 @@ cudaError_t launch_router_topk(const float* logits, int T, int E, int k, int32_t
 cudaError_t launch_route(const int32_t* ids, int T, int k, int E, int shared, int32_t* counts,
                          int32_t* offsets, int32_t* tile_off, int32_t* sorted_src,
                          int32_t* dest_pos, int32_t* hist, int* status, cudaStream_t s);
+// Kernels launch_route issues for n assignments and G groups: 2 when the
+// per-CTA histogram is small enough for the scatter kernel to scan it itself,
+// else 3 (histogram, scan, scatter).
+int route_kernel_count(int64_t n, int G);
 
 // ---- row gather / combine (rows.cu) ------------------------------------------
 // Permuted rows are in sorted order: row p holds sorted position p, N = T * K rows.

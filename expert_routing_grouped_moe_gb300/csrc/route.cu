@@ -4,13 +4,15 @@
 // routing done in one grouped pass": flatten the [T,k] assignments, stable-
 // sort them by expert id, one bincount, offsets from the counts, slice the
 // token list by offsets -- with no per-expert data-dependent query.  On the
-// GPU this is a counting sort in three kernels:
+// GPU this is a counting sort in three kernels (two for small inputs):
 //
 //   route_hist     per-CTA expert histogram of a contiguous chunk of the flat
 //                  assignment list (per-warp shared-memory counters), written
 //                  expert-major: hist[g][cta]
 //   route_scan     one CTA per expert: exclusive scan of hist[g][:] over the
-//                  CTAs (block prefix sum), total -> counts[g]
+//                  CTAs (block prefix sum), total -> counts[g].  Skipped when
+//                  the table is small (C <= kFusedScanCtas): each scatter CTA
+//                  then sums its own column prefix and the totals itself.
 //   route_scatter  every CTA scans counts -> offsets (and tile offsets) in one
 //                  warp, re-walks its chunk in the same warp order and ranks
 //                  equal ids among earlier lanes with a ballot-per-bit warp
@@ -187,25 +189,34 @@ __global__ void __launch_bounds__(1024) route_scan_kernel(int32_t* __restrict__ 
   if (threadIdx.x == 0) counts[blockIdx.x] = total;
 }
 
+// Routing CTAs up to which the scatter kernel scans the per-CTA histogram
+// itself (G * C loads per CTA) instead of a separate scan kernel.
+constexpr int kFusedScanCtas = 64;
+
 // Shared memory of the scatter kernel, in ints.
 __host__ __device__ constexpr int scatter_smem_ints(int G, int chunk) {
   return (G + 1) /*off*/ + kRouteWarps * G /*cnt*/ + (G + 1) /*lbase*/ + G /*delta*/ +
+         2 * G /*fused scan: totals, this CTA's prefix*/ +
          chunk /*flat index at each chunk-local sorted position*/;
 }
 
 template <int PER, bool SHARED, int NB>
 __global__ void __launch_bounds__(kRouteThreads, 4) route_scatter_kernel(
     const int32_t* __restrict__ ids, int N, int k, int K, int E, int G, int C,
-    const int32_t* __restrict__ hist, const int32_t* __restrict__ counts,
+    const int32_t* __restrict__ hist, int32_t* __restrict__ counts, int fused,
     int32_t* __restrict__ offsets, int32_t* __restrict__ tile_off,
     int32_t* __restrict__ sorted_src, int32_t* __restrict__ dest_pos) {
+  // fused: hist holds raw per-CTA counts (no scan kernel ran); else hist
+  // holds the exclusive prefix over CTAs and counts the totals
   constexpr int CH = kRouteThreads * PER;
   extern __shared__ int sm[];
   int* off = sm;                      // [G+1] global offsets
   int* cnt = off + (G + 1);           // [8][G] per-warp counts -> per-warp local starts
   int* lbase = cnt + kRouteWarps * G;  // [G+1] start of group g inside this CTA's chunk
   int* delta = lbase + (G + 1);       // [G]   global position - chunk-local position, group g
-  int* stage = delta + G;             // [CH]  flat index at each chunk-local sorted position
+  int* tot = delta + G;               // [G]   fused: total of group g over all CTAs
+  int* pre = tot + G;                 // [G]   fused: group g in the CTAs before this one
+  int* stage = pre + G;               // [CH]  flat index at each chunk-local sorted position
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   pdl_wait();
 
@@ -215,13 +226,29 @@ __global__ void __launch_bounds__(kRouteThreads, 4) route_scatter_kernel(
 #pragma unroll
   for (int it = 0; it < PER; ++it) ev[it] = flat_id<SHARED>(ids, base + it * 32 + lane, N, k, K, E);
 
+  if (fused) {
+    for (int g = threadIdx.x; g < G; g += blockDim.x) {
+      const int32_t* h = hist + static_cast<int64_t>(g) * C;
+      int before = 0, all = 0;
+      for (int c = 0; c < C; ++c) {
+        const int v = __ldg(h + c);
+        before += c < static_cast<int>(blockIdx.x) ? v : 0;
+        all += v;
+      }
+      tot[g] = all;
+      pre[g] = before;
+      if (blockIdx.x == 0) counts[g] = all;
+    }
+    __syncthreads();
+  }
+
   // offsets (and tile offsets) = exclusive scans of counts, by warp 0
   if (warp == 0) {
     const int per = (G + 31) / 32;
     const int lo = min(G, lane * per), hi = min(G, lo + per);
     int s = 0, st = 0;
     for (int g = lo; g < hi; ++g) {
-      const int c = __ldg(counts + g);
+      const int c = fused ? tot[g] : __ldg(counts + g);
       s += c;
       st += (c + kTileM - 1) / kTileM;
     }
@@ -236,7 +263,7 @@ __global__ void __launch_bounds__(kRouteThreads, 4) route_scatter_kernel(
     }
     int run = xs - s, trun = xt - st;
     for (int g = lo; g < hi; ++g) {
-      const int c = __ldg(counts + g);
+      const int c = fused ? tot[g] : __ldg(counts + g);
       off[g] = run;
       if (blockIdx.x == 0) {
         offsets[g] = run;
@@ -280,7 +307,9 @@ __global__ void __launch_bounds__(kRouteThreads, 4) route_scatter_kernel(
     int run = block_excl_scan(s, &total);
     for (int g = lo; g < hi; ++g) {
       lbase[g] = run;
-      delta[g] = off[g] + __ldg(hist + static_cast<int64_t>(g) * C + blockIdx.x) - run;
+      const int before =
+          fused ? pre[g] : __ldg(hist + static_cast<int64_t>(g) * C + blockIdx.x);
+      delta[g] = off[g] + before - run;
 #pragma unroll
       for (int w = 0; w < kRouteWarps; ++w) {
         const int c = cnt[w * G + g];
@@ -403,6 +432,11 @@ __global__ void __launch_bounds__(256) router_topk_kernel(const float* __restric
 
 }  // namespace
 
+int route_kernel_count(int64_t n, int G) {
+  (void)G;
+  return route_ctas(n > 0 ? n : 1) <= kFusedScanCtas ? 2 : 3;
+}
+
 cudaError_t launch_router_topk(const float* logits, int T, int E, int k, int32_t* ids, float* w,
                                cudaStream_t s) {
   if (T == 0) return cudaSuccess;
@@ -431,12 +465,13 @@ cudaError_t launch_route_per(const int32_t* ids, int N, int k, int K, int E, int
   const int vec = (reinterpret_cast<uintptr_t>(ids) & 15u) == 0 ? 1 : 0;
   e = launch_pdl(route_hist_kernel<PER, SHARED>, dim3(C), dim3(kRouteThreads), sm_hist, s, ids,
                  N, k, K, E, G, C, vec, hist, status);
-  if (e == cudaSuccess)
+  const int fused = C <= kFusedScanCtas ? 1 : 0;
+  if (e == cudaSuccess && !fused)
     e = launch_pdl(route_scan_kernel, dim3(G), dim3(1024), 0, s, hist, C, counts);
   if (e == cudaSuccess)
     e = launch_pdl(route_scatter_kernel<PER, SHARED, NB>, dim3(C), dim3(kRouteThreads), sm_scat,
-                   s, ids, N, k, K, E, G, C, static_cast<const int32_t*>(hist),
-                   static_cast<const int32_t*>(counts), offsets, tile_off, sorted_src, dest_pos);
+                   s, ids, N, k, K, E, G, C, static_cast<const int32_t*>(hist), counts, fused,
+                   offsets, tile_off, sorted_src, dest_pos);
   return e;
 }
 

@@ -18,10 +18,10 @@ import torch
 from . import _lib as L
 
 # Kernel launches issued by one forward / one backward in the default
-# (permuted) mode: route 3, permute 1, forward GEMMs 4, combine 1; backward:
-# permute 1, GEMMs 4 + weight-gradient GEMMs 4, partial-sum 1, combine 1.
-# The gather mode issues no permute.
-LAUNCHES_FWD = 9
+# (permuted) mode: route 2 or 3 (L.moe_route_kernel_count), permute 1,
+# forward GEMMs 4, combine 1; backward: permute 1, GEMMs 4 + weight-gradient
+# GEMMs 4, partial-sum 1, combine 1.  The gather mode issues no permute.
+LAUNCHES_FWD = 6   # besides the route's
 LAUNCHES_BWD = 11
 
 
@@ -82,8 +82,8 @@ class MoELoRALayer:
 
     def launches_per_step(self):
         """Kernel launches of one forward + backward in this layer's mode."""
-        return (LAUNCHES_FWD + LAUNCHES_BWD - (2 if self.gather else 0)
-                + (2 if self.full_grads else 0))
+        return (L.moe_route_kernel_count(self.T, self.K, self.G) + LAUNCHES_FWD + LAUNCHES_BWD
+                - (2 if self.gather else 0) + (2 if self.full_grads else 0))
 
     # ------------------------------------------------------------------ steps
     def route(self, ids, stream=None):

@@ -110,6 +110,12 @@ MOE_API int moe_router_topk(const float* logits, int32_t T, int32_t E, int32_t k
 /* Bytes of scratch moe_route needs for T tokens, K slots, G groups. */
 MOE_API size_t moe_route_workspace_size(int32_t T, int32_t K, int32_t G);
 
+/* Kernels moe_route (and moe_route_noalloc) launch for T tokens, K slots and
+ * G groups: 3 (per-chunk histogram, scan over chunks, scatter), or 2 when
+ * there are at most 64 chunks and the scatter kernel scans the histogram
+ * itself.  MOE_ERR_INVALID_ARG for a non-positive size. */
+MOE_API int32_t moe_route_kernel_count(int32_t T, int32_t K, int32_t G);
+
 /* Flatten ids [T,k] row-major (the shared slot j = k carries id E when
  * shared_expert = 1), stable-sort by expert id, bincount, offsets:
  *   counts    [G]    counts[g] = #{i : id(i) = g}
@@ -320,7 +326,7 @@ MOE_API int moe_probe_read_stream(const void* src, size_t bytes, int32_t pattern
  * route, permute, combine, router_topk, the grouped GEMMs xa_gu, gate_up,
  * xa_dn, down, u, dgrad_dn, v, dgrad_gu, the weight-gradient GEMMs dB_dn,
  * dA_dn, dB_gu, dA_gu, dw_reduce, and the full weight-gradient GEMMs dW_dn
- * and dW_gu.  ("route" covers its three kernels.) */
+ * and dW_gu.  ("route" covers all of its kernels: moe_route_kernel_count.) */
 MOE_API const char* moe_kernel_name(int32_t i);
 
 /* Arms the probe of one kernel: its next n launches record start_events[i]

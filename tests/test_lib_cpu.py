@@ -43,6 +43,13 @@ def test_sizes(lib):
     assert lib.moe_route_workspace_size(0, 8, 128) == 0
 
 
+def test_route_kernel_count(lib):
+    from expert_routing_grouped_moe_gb300 import _lib
+    assert lib.moe_route_kernel_count(4096, 8, 128) == 2        # 32 chunks: scan fused
+    assert lib.moe_route_kernel_count(1 << 20, 8, 128) == 3     # 2048 chunks
+    assert lib.moe_route_kernel_count(0, 8, 128) == _lib.MOE_ERR_INVALID_ARG
+
+
 def test_read_stream_probe_argument_checks(lib):
     from expert_routing_grouped_moe_gb300 import _lib
     lin, til = _lib.MOE_PROBE_LINEAR, _lib.MOE_PROBE_TILES
