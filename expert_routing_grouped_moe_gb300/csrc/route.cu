@@ -6,9 +6,10 @@
 // token list by offsets -- with no per-expert data-dependent query.  On the
 // GPU this is a counting sort in three kernels (two for small inputs):
 //
-//   route_hist     per-CTA expert histogram of a contiguous chunk of the flat
+//   route_hist     expert histogram of each contiguous chunk of the flat
 //                  assignment list (per-warp shared-memory counters), written
-//                  expert-major: hist[g][cta]
+//                  expert-major: hist[g][chunk]; persistent CTAs walk the
+//                  chunks with the next chunk's ids in flight
 //   route_scan     one CTA per expert: exclusive scan of hist[g][:] over the
 //                  CTAs (block prefix sum), total -> counts[g].  Skipped when
 //                  the table is small (C <= kFusedScanCtas): each scatter CTA
@@ -141,33 +142,47 @@ __device__ __forceinline__ void load_ids_any_order(const int32_t* __restrict__ i
   }
 }
 
+// Persistent over chunks: CTA b counts chunks b, b + gridDim.x, ..., with
+// the next chunk's ids in flight while the current one is counted.
 template <int PER, bool SHARED>
-__global__ void __launch_bounds__(kRouteThreads) route_hist_kernel(
+__global__ void __launch_bounds__(kRouteThreads, 4) route_hist_kernel(
     const int32_t* __restrict__ ids, int N, int k, int K, int E, int G, int C, int vec,
     int32_t* __restrict__ hist, int* __restrict__ status) {
+  constexpr int CH = kRouteThreads * PER;
   extern __shared__ int cnt[];  // [kRouteWarps][G]
-  for (int x = threadIdx.x; x < kRouteWarps * G; x += blockDim.x) cnt[x] = 0;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int base = blockIdx.x * (kRouteThreads * PER) + warp * (32 * PER);
-  pdl_wait();
-  int ev[PER];
-  load_ids_any_order<PER, SHARED>(ids, base, lane, N, k, K, E, vec != 0, ev);
-  __syncthreads();
   int* my = cnt + warp * G;
+  pdl_wait();
+  int ev[PER], nx[PER];
+  int c = blockIdx.x;
+  if (c < C)
+    load_ids_any_order<PER, SHARED>(ids, c * CH + warp * (32 * PER), lane, N, k, K, E, vec != 0,
+                                    ev);
   bool bad = false;
+  for (; c < C; c += gridDim.x) {
+    const int cn = c + gridDim.x;
+    if (cn < C)
+      load_ids_any_order<PER, SHARED>(ids, cn * CH + warp * (32 * PER), lane, N, k, K, E,
+                                      vec != 0, nx);
+    for (int x = threadIdx.x; x < kRouteWarps * G; x += blockDim.x) cnt[x] = 0;
+    __syncthreads();
 #pragma unroll
-  for (int it = 0; it < PER; ++it) {
-    bad |= (ev[it] == -2);
-    if (ev[it] >= 0) atomicAdd(my + ev[it], 1);
+    for (int it = 0; it < PER; ++it) {
+      bad |= (ev[it] == -2);
+      if (ev[it] >= 0) atomicAdd(my + ev[it], 1);
+    }
+    __syncthreads();
+    for (int e = threadIdx.x; e < G; e += blockDim.x) {
+      int s = 0;
+#pragma unroll
+      for (int w = 0; w < kRouteWarps; ++w) s += cnt[w * G + e];
+      hist[static_cast<int64_t>(e) * C + c] = s;
+    }
+    __syncthreads();  // the counters are read before the next chunk clears them
+#pragma unroll
+    for (int it = 0; it < PER; ++it) ev[it] = nx[it];
   }
   if (bad) atomicCAS(status, 0, kErrBadIds);
-  __syncthreads();
-  for (int e = threadIdx.x; e < G; e += blockDim.x) {
-    int s = 0;
-#pragma unroll
-    for (int w = 0; w < kRouteWarps; ++w) s += cnt[w * G + e];
-    hist[static_cast<int64_t>(e) * C + blockIdx.x] = s;
-  }
 }
 
 __global__ void __launch_bounds__(1024) route_scan_kernel(int32_t* __restrict__ hist, int C,
@@ -197,7 +212,8 @@ constexpr int kFusedScanCtas = 64;
 __host__ __device__ constexpr int scatter_smem_ints(int G, int chunk) {
   return (G + 1) /*off*/ + kRouteWarps * G /*cnt*/ + (G + 1) /*lbase*/ + G /*delta*/ +
          2 * G /*fused scan: totals, this CTA's prefix*/ +
-         chunk /*flat index at each chunk-local sorted position*/;
+         chunk /*flat index at each chunk-local sorted position*/ +
+         chunk / 2 /*its group, 16 bits*/;
 }
 
 template <int PER, bool SHARED, int NB>
@@ -217,6 +233,7 @@ __global__ void __launch_bounds__(kRouteThreads, 4) route_scatter_kernel(
   int* tot = delta + G;               // [G]   fused: total of group g over all CTAs
   int* pre = tot + G;                 // [G]   fused: group g in the CTAs before this one
   int* stage = pre + G;               // [CH]  flat index at each chunk-local sorted position
+  uint16_t* stage_g = reinterpret_cast<uint16_t*>(stage + CH);  // [CH] its group
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   pdl_wait();
 
@@ -332,6 +349,7 @@ __global__ void __launch_bounds__(kRouteThreads, 4) route_scatter_kernel(
       const unsigned m = warp_match<NB>(static_cast<unsigned>(e));
       const int lp = my[e] + __popc(m & lt);
       stage[lp] = base + it * 32 + lane;
+      stage_g[lp] = static_cast<uint16_t>(e);
       dp[it * 32] = delta[e] + lp;
       __syncwarp();
       if ((m >> lane) == 1u) my[e] = lp + 1;  // the last matching lane
@@ -349,6 +367,7 @@ __global__ void __launch_bounds__(kRouteThreads, 4) route_scatter_kernel(
       if (e >= 0) {
         lp = my[e] + __popc(m & lt);
         stage[lp] = i;
+        stage_g[lp] = static_cast<uint16_t>(e);
         dp[it * 32] = delta[e] + lp;
       } else if (i < N) {
         dp[it * 32] = -1;
@@ -360,13 +379,11 @@ __global__ void __launch_bounds__(kRouteThreads, 4) route_scatter_kernel(
   }
   __syncthreads();
 
-  // sorted_src: group g's run of this chunk is contiguous both in the stage
-  // and in global memory; one warp copies it
-  for (int g = warp; g < G; g += kRouteWarps) {
-    const int lo = lbase[g], n = lbase[g + 1] - lo;
-    int32_t* dst = sorted_src + (delta[g] + lo);
-    for (int x = lane; x < n; x += 32) dst[x] = stage[lo + x];
-  }
+  // sorted_src: each group's run of this chunk is contiguous both in the
+  // stage and in global memory (position q of the stage goes to delta[g] + q);
+  // consecutive threads copy consecutive positions
+  for (int q = threadIdx.x; q < lbase[G]; q += kRouteThreads)
+    sorted_src[delta[stage_g[q]] + q] = stage[q];
   // sorted positions past the valid total (only when some ids were bad)
   for (int p = off[G] + blockIdx.x * blockDim.x + threadIdx.x; p < N;
        p += gridDim.x * blockDim.x)
@@ -463,8 +480,13 @@ cudaError_t launch_route_per(const int32_t* ids, int N, int k, int K, int E, int
                                        static_cast<int>(sm_scat));
   if (e != cudaSuccess) return e;
   const int vec = (reinterpret_cast<uintptr_t>(ids) & 15u) == 0 ? 1 : 0;
-  e = launch_pdl(route_hist_kernel<PER, SHARED>, dim3(C), dim3(kRouteThreads), sm_hist, s, ids,
-                 N, k, K, E, G, C, vec, hist, status);
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms < 1)
+    sms = 1;
+  const int hist_grid = C < 4 * sms ? C : 4 * sms;  // persistent: 4 CTAs per SM
+  e = launch_pdl(route_hist_kernel<PER, SHARED>, dim3(hist_grid), dim3(kRouteThreads), sm_hist,
+                 s, ids, N, k, K, E, G, C, vec, hist, status);
   const int fused = C <= kFusedScanCtas ? 1 : 0;
   if (e == cudaSuccess && !fused)
     e = launch_pdl(route_scan_kernel, dim3(G), dim3(1024), 0, s, hist, C, counts);
