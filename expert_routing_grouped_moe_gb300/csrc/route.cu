@@ -6,10 +6,9 @@
 // token list by offsets -- with no per-expert data-dependent query.  On the
 // GPU this is a counting sort in three kernels (two for small inputs):
 //
-//   route_hist     expert histogram of each contiguous chunk of the flat
+//   route_hist     per-CTA expert histogram of a contiguous chunk of the flat
 //                  assignment list (per-warp shared-memory counters), written
-//                  expert-major: hist[g][chunk]; persistent CTAs walk the
-//                  chunks with the next chunk's ids in flight
+//                  expert-major: hist[g][cta]
 //   route_scan     one CTA per expert: exclusive scan of hist[g][:] over the
 //                  CTAs (block prefix sum), total -> counts[g].  Skipped when
 //                  the table is small (C <= kFusedScanCtas): each scatter CTA
@@ -142,47 +141,33 @@ __device__ __forceinline__ void load_ids_any_order(const int32_t* __restrict__ i
   }
 }
 
-// Persistent over chunks: CTA b counts chunks b, b + gridDim.x, ..., with
-// the next chunk's ids in flight while the current one is counted.
 template <int PER, bool SHARED>
-__global__ void __launch_bounds__(kRouteThreads, 4) route_hist_kernel(
+__global__ void __launch_bounds__(kRouteThreads) route_hist_kernel(
     const int32_t* __restrict__ ids, int N, int k, int K, int E, int G, int C, int vec,
     int32_t* __restrict__ hist, int* __restrict__ status) {
-  constexpr int CH = kRouteThreads * PER;
   extern __shared__ int cnt[];  // [kRouteWarps][G]
+  for (int x = threadIdx.x; x < kRouteWarps * G; x += blockDim.x) cnt[x] = 0;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  int* my = cnt + warp * G;
+  const int base = blockIdx.x * (kRouteThreads * PER) + warp * (32 * PER);
   pdl_wait();
-  int ev[PER], nx[PER];
-  int c = blockIdx.x;
-  if (c < C)
-    load_ids_any_order<PER, SHARED>(ids, c * CH + warp * (32 * PER), lane, N, k, K, E, vec != 0,
-                                    ev);
+  int ev[PER];
+  load_ids_any_order<PER, SHARED>(ids, base, lane, N, k, K, E, vec != 0, ev);
+  __syncthreads();
+  int* my = cnt + warp * G;
   bool bad = false;
-  for (; c < C; c += gridDim.x) {
-    const int cn = c + gridDim.x;
-    if (cn < C)
-      load_ids_any_order<PER, SHARED>(ids, cn * CH + warp * (32 * PER), lane, N, k, K, E,
-                                      vec != 0, nx);
-    for (int x = threadIdx.x; x < kRouteWarps * G; x += blockDim.x) cnt[x] = 0;
-    __syncthreads();
 #pragma unroll
-    for (int it = 0; it < PER; ++it) {
-      bad |= (ev[it] == -2);
-      if (ev[it] >= 0) atomicAdd(my + ev[it], 1);
-    }
-    __syncthreads();
-    for (int e = threadIdx.x; e < G; e += blockDim.x) {
-      int s = 0;
-#pragma unroll
-      for (int w = 0; w < kRouteWarps; ++w) s += cnt[w * G + e];
-      hist[static_cast<int64_t>(e) * C + c] = s;
-    }
-    __syncthreads();  // the counters are read before the next chunk clears them
-#pragma unroll
-    for (int it = 0; it < PER; ++it) ev[it] = nx[it];
+  for (int it = 0; it < PER; ++it) {
+    bad |= (ev[it] == -2);
+    if (ev[it] >= 0) atomicAdd(my + ev[it], 1);
   }
   if (bad) atomicCAS(status, 0, kErrBadIds);
+  __syncthreads();
+  for (int e = threadIdx.x; e < G; e += blockDim.x) {
+    int s = 0;
+#pragma unroll
+    for (int w = 0; w < kRouteWarps; ++w) s += cnt[w * G + e];
+    hist[static_cast<int64_t>(e) * C + blockIdx.x] = s;
+  }
 }
 
 __global__ void __launch_bounds__(1024) route_scan_kernel(int32_t* __restrict__ hist, int C,
@@ -480,13 +465,8 @@ cudaError_t launch_route_per(const int32_t* ids, int N, int k, int K, int E, int
                                        static_cast<int>(sm_scat));
   if (e != cudaSuccess) return e;
   const int vec = (reinterpret_cast<uintptr_t>(ids) & 15u) == 0 ? 1 : 0;
-  int dev = 0, sms = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess ||
-      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms < 1)
-    sms = 1;
-  const int hist_grid = C < 4 * sms ? C : 4 * sms;  // persistent: 4 CTAs per SM
-  e = launch_pdl(route_hist_kernel<PER, SHARED>, dim3(hist_grid), dim3(kRouteThreads), sm_hist,
-                 s, ids, N, k, K, E, G, C, vec, hist, status);
+  e = launch_pdl(route_hist_kernel<PER, SHARED>, dim3(C), dim3(kRouteThreads), sm_hist, s, ids,
+                 N, k, K, E, G, C, vec, hist, status);
   const int fused = C <= kFusedScanCtas ? 1 : 0;
   if (e == cudaSuccess && !fused)
     e = launch_pdl(route_scan_kernel, dim3(G), dim3(1024), 0, s, hist, C, counts);
