@@ -10,6 +10,9 @@ Pins (checked by ``tests/test_oracle_*.py`` on the CPU):
 
 * ``route``            -- pinned: brute-force per-expert ``where`` loop, hand-worked
                           golden example, counting invariants.
+* ``permute``, ``combine`` -- pinned: hand-worked golden example, the
+                          round trip combine(permute(X)) = (sum of weights) X,
+                          combine of per-row expert outputs = ``layer_forward``.
 * ``router_topk``      -- pinned: brute-force sort on tiny inputs, hand-worked
                           golden example, softmax-over-selected identity.
 * ``layer_forward``    -- pinned: merged-weight (PEFT) evaluation, hand-worked
@@ -22,6 +25,8 @@ from .moe_oracle import (  # noqa: F401
     router_topk,
     route,
     route_where_loop,
+    permute,
+    combine,
     silu,
     dsilu,
     OracleParams,

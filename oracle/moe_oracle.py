@@ -116,6 +116,43 @@ def route_where_loop(ids, E: int):
     return out
 
 
+def permute(X, sorted_src, K: int):
+    """Step 5 of [R] applied to the token rows: the rows in expert-grouped
+    order.  Sorted position p holds the assignment with flat index
+    i = sorted_src[p] = t*K + j, so row p of the result is token t's row:
+        Xp[p] = X[sorted_src[p] // K]
+    (K slots per token: the top-k slots, plus the shared expert's slot when
+    there is one).  A pure gather; no value changes."""
+    X = np.asarray(X)
+    src = np.asarray(sorted_src, dtype=np.int64)
+    if src.size and (src.min() < 0 or src.max() >= X.shape[0] * K):
+        raise ValueError("sorted_src entry out of range")
+    return X[src // K]
+
+
+def combine(rows, dest_pos, K: int, weights=None):
+    """Weighted combine of permuted rows back into token order (the top-k
+    mixture; the pages do not print this step).  Token t's slot j sits at
+    permuted row dest_pos[t*K + j]; with c_j its coefficient,
+        Y[t] = sum_j c_j * rows[dest_pos[t*K + j]]
+    c_j = weights[t, j] for the weights' k columns and 1 for any further slot
+    (the shared expert's), or 1 for every slot when weights is None.  Exact
+    fp64 sum (no rounding order to match)."""
+    R = np.asarray(rows, dtype=np.float64)
+    dp = np.asarray(dest_pos, dtype=np.int64)
+    if dp.size % K:
+        raise ValueError("dest_pos length is not a multiple of K")
+    T = dp.size // K
+    c = np.ones((T, K))
+    if weights is not None:
+        w = np.asarray(weights, dtype=np.float64)
+        c[:, :w.shape[1]] = w
+    Y = np.zeros((T, R.shape[1]))
+    for j in range(K):
+        Y += c[:, j:j + 1] * R[dp.reshape(T, K)[:, j]]
+    return Y
+
+
 # ---------------------------------------------------------------------------
 # Expert MLP with split LoRA [G], [L], [S]
 # ---------------------------------------------------------------------------
