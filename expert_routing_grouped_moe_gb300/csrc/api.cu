@@ -3,6 +3,7 @@
 // except moe_status().  See include/moe_gb300.h for the contract of each call.
 #include <cstdarg>
 #include <cstdio>
+#include <cstdlib>
 #include <cstring>
 #include <atomic>
 #include <mutex>
@@ -97,32 +98,6 @@ int kernel_index(const char* name) {
   return -1;
 }
 
-// Records the start event of the next free probe slot of `name`; returns the
-// slot (or -1 when the kernel is not being probed).
-int probe_begin(const char* name, cudaStream_t s) {
-  if (g_probe_armed.load(std::memory_order_relaxed) == 0) return -1;
-  const int id = kernel_index(name);
-  if (id < 0) return -1;
-  std::lock_guard<std::mutex> lk(g_probe_mu);
-  Probe& pr = g_probe[id];
-  if (pr.used >= static_cast<int>(pr.start.size())) return -1;
-  const int slot = pr.used++;
-  cudaEventRecord(static_cast<cudaEvent_t>(pr.start[slot]), s);
-  return id * (1 << 24) + slot;
-}
-void probe_end(int token, cudaStream_t s) {
-  if (token < 0) return;
-  std::lock_guard<std::mutex> lk(g_probe_mu);
-  const Probe& pr = g_probe[token >> 24];
-  cudaEventRecord(static_cast<cudaEvent_t>(pr.stop[token & ((1 << 24) - 1)]), s);
-}
-struct ProbeScope {
-  int token;
-  cudaStream_t s;
-  ProbeScope(const char* name, cudaStream_t st) : token(probe_begin(name, st)), s(st) {}
-  ~ProbeScope() { probe_end(token, s); }
-};
-
 // The device's second stream and its fork/join events, created once.  Callers
 // hold st->aux_mu while enqueueing work that uses them.
 int aux_stream(DevState* st, cudaStream_t* out) {
@@ -167,9 +142,44 @@ EncodeTiledFn encode_fn() {
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-// Upper bound on the 128-row tiles of all groups: sum_g ceil(counts[g] / 128).
-int64_t max_row_tiles(int64_t T, int64_t K, int64_t G) {
-  return (T * K + G * (kTileM - 1) + kTileM - 1) / kTileM;
+// The same for the 256-row tiles of CTA pairs.
+int64_t max_pair_tiles(int64_t T, int64_t K, int64_t G) {
+  return (T * K + G * (kPairTileM - 1) + kPairTileM - 1) / kPairTileM;
+}
+
+// Which of the large row-tile GEMMs run on CTA pairs (256-row tiles, tcgen05
+// cta_group::2, each CTA staging half of the B tile) instead of single CTAs
+// (128-row tiles).  A pair halves the B bytes each SM stages per MMA, but a
+// group's rows are padded to a multiple of 256 instead of 128: with ~256
+// rows per group about half the groups carry one idle 128-row half.  So
+// gate_up (whose B tile is the largest share of its staging) always pairs,
+// the others when groups average at least 512 rows.  MOE_PAIR_TILES in the
+// environment overrides this: "0" (none), "1" (all), or a comma-separated
+// list of gate_up, down, dgrad_dn, dgrad_gu.
+enum PairKernel { kPairGateUp = 1, kPairDown = 2, kPairDgradDn = 4, kPairDgradGu = 8 };
+int pair_override() {
+  static const int mask = [] {
+    const char* v = std::getenv("MOE_PAIR_TILES");
+    if (v == nullptr || *v == 0) return -1;
+    if (std::strcmp(v, "0") == 0) return 0;
+    if (std::strcmp(v, "1") == 0) return 15;
+    int m = 0;
+    if (std::strstr(v, "gate_up")) m |= kPairGateUp;
+    if (std::strstr(v, "down")) m |= kPairDown;
+    if (std::strstr(v, "dgrad_dn")) m |= kPairDgradDn;
+    if (std::strstr(v, "dgrad_gu")) m |= kPairDgradGu;
+    return m;
+  }();
+  return mask;
+}
+bool pair_tiles(const moe_dims* dm, PairKernel which, bool a_rows_by_tma) {
+  const int G = dm->E + dm->shared_expert;
+  if (!a_rows_by_tma || G + 1 > kTileTabInts) return false;
+  const int forced = pair_override();
+  if (forced >= 0) return (forced & which) != 0;
+  if (which == kPairGateUp) return true;
+  const int64_t rows = static_cast<int64_t>(dm->T) * (dm->k + dm->shared_expert);
+  return rows >= 512 * static_cast<int64_t>(G);
 }
 
 int check_dims(const moe_dims* dm) {
@@ -185,8 +195,7 @@ int check_dims(const moe_dims* dm) {
     return fail(MOE_ERR_INVALID_ARG, "d, f and r must be multiples of 8");
   if (dm->r > 64) return fail(MOE_ERR_UNSUPPORTED, "LoRA rank r=%d > 64", dm->r);
   const int64_t K = dm->k + dm->shared_expert, G = dm->E + dm->shared_expert;
-  if (max_row_tiles(dm->T, K, G) * kTileM >= (int64_t(1) << 31))
-    return fail(MOE_ERR_UNSUPPORTED, "too many routed rows");
+  if (!routed_rows_fit(dm->T, K, G)) return fail(MOE_ERR_UNSUPPORTED, "too many routed rows");
   return MOE_OK;
 }
 
@@ -198,6 +207,25 @@ int check_dims(const moe_dims* dm) {
 
 }  // namespace
 
+// Records the start event of the next free probe slot of `name`; returns the
+// slot (or -1 when the kernel is not being probed).
+int probe_begin(const char* name, cudaStream_t s) {
+  if (g_probe_armed.load(std::memory_order_relaxed) == 0) return -1;
+  const int id = kernel_index(name);
+  if (id < 0) return -1;
+  std::lock_guard<std::mutex> lk(g_probe_mu);
+  Probe& pr = g_probe[id];
+  if (pr.used >= static_cast<int>(pr.start.size())) return -1;
+  const int slot = pr.used++;
+  cudaEventRecord(static_cast<cudaEvent_t>(pr.start[slot]), s);
+  return id * (1 << 24) + slot;
+}
+void probe_end(int token, cudaStream_t s) {
+  if (token < 0) return;
+  std::lock_guard<std::mutex> lk(g_probe_mu);
+  const Probe& pr = g_probe[token >> 24];
+  cudaEventRecord(static_cast<cudaEvent_t>(pr.stop[token & ((1 << 24) - 1)]), s);
+}
 int device_status_word(int** out) {
   DevState* st = nullptr;
   const int rc = device_state(&st);
@@ -473,8 +501,7 @@ int moe_route(const int32_t* ids, int32_t T, int32_t k, int32_t E, int32_t share
   if (k > E) return fail(MOE_ERR_INVALID_ARG, "k=%d > E=%d", k, E);
   if (E > kMaxExperts || k > 32) return fail(MOE_ERR_UNSUPPORTED, "E > 1024 or k > 32");
   const int64_t K = k + shared_expert, G = E + shared_expert;
-  if (max_row_tiles(T, K, G) * kTileM >= (int64_t(1) << 31))
-    return fail(MOE_ERR_UNSUPPORTED, "too many routed rows");
+  if (!routed_rows_fit(T, K, G)) return fail(MOE_ERR_UNSUPPORTED, "too many routed rows");
   if (!aligned16(ws)) return fail(MOE_ERR_INVALID_ARG, "ws not 16-byte aligned");
   if (ws_bytes < moe_route_workspace_size(T, static_cast<int32_t>(K), static_cast<int32_t>(G)))
     return fail(MOE_ERR_WORKSPACE, "route workspace too small");
@@ -565,14 +592,18 @@ int moe_lora_grouped_mlp_fwd(const moe_dims* dims, const moe_bf16* Xp, const moe
     if ((rc = run_gemm({128, false, false, Epi::kLoRAGrid}, p, RG, st->num_sms, s, "xa_gu")))
       return rc;
   }
+  const bool pair_x = pair_tiles(dims, kPairGateUp, Xp != nullptr);
+  const bool pair_rows = pair_tiles(dims, kPairDown, true);
+  const int64_t R2 = max_pair_tiles(dims->T, dims->k + dims->shared_expert, G);
   {  // h = Xp W_gu^T + (s xa) B_gu^T (fp32) ; act pair = w * silu(gate) * up
+    // (B boxes of 128 rows: one gate or up half; a CTA pair stages one each)
     GemmParams p = base;
     SLICE_ROWS(p, 0, Xp, X, d, MAP3(p.sl[0].b, W_gu, G, 2 * f, d, 128, 64), d);
     SLICE(p, 1, xa_gu, N, r, MAP3(p.sl[1].b, B_gu, G, 2 * f, r, 128, 64), r);
     SLICE(p, 2, xa_gu + Nr, N, r, MAP3(p.sl[2].b, B_gu, G, 2 * f, r, 128, 64), r);
     p.nslices = 3; p.N = f; p.n_ntiles = (f + 127) / 128; p.b_split = f;
     p.fout = h; p.ldf = 32 * ((f + 15) / 16); p.ld0 = 2 * f; p.out0 = act; p.pair = Nf;
-    {  // one 4-D box per K block for both halves (the 3-D maps stay as fallback)
+    if (!pair_x) {  // one 4-D box per K block for both halves (the 3-D maps stay as fallback)
       GemmSlice q[3] = {p.sl[0], p.sl[1], p.sl[2]};
       if (make_map_split4d(&q[0].b, W_gu, G, f, d, 128, 64) &&
           make_map_split4d(&q[1].b, B_gu, G, f, r, 128, 64) &&
@@ -581,7 +612,8 @@ int moe_lora_grouped_mlp_fwd(const moe_dims* dims, const moe_bf16* Xp, const moe
         p.b4d = 1;
       }
     }
-    if ((rc = run_gemm({256, false, false, Epi::kSwiGLU}, p, R, st->num_sms, s, "gate_up")))
+    if ((rc = run_gemm({256, false, false, Epi::kSwiGLU, pair_x}, p, pair_x ? R2 : R, st->num_sms,
+                       s, "gate_up")))
       return rc;
   }
   {  // xa_dn pair = s * act A_dn^T   (act = hi + lo, already scaled by w)
@@ -594,10 +626,12 @@ int moe_lora_grouped_mlp_fwd(const moe_dims* dims, const moe_bf16* Xp, const moe
   }
   {  // Yp = act W_dn^T + xa_dn B_dn^T = w * (o)   (act and xa_dn carry w)
     GemmParams p = base;
-    SLICE(p, 0, act, N, f, MAP3(p.sl[0].b, W_dn, G, d, f, 256, 64), f);
-    SLICE(p, 1, xa_dn, N, r, MAP3(p.sl[1].b, B_dn, G, d, r, 256, 64), r);
+    const uint32_t bb = pair_rows ? 128 : 256;  // B box rows: a pair stages half each
+    SLICE(p, 0, act, N, f, MAP3(p.sl[0].b, W_dn, G, d, f, bb, 64), f);
+    SLICE(p, 1, xa_dn, N, r, MAP3(p.sl[1].b, B_dn, G, d, r, bb, 64), r);
     p.nslices = 2; p.N = d; p.n_ntiles = (d + 255) / 256; p.out0 = Yp; p.ld0 = d;
-    if ((rc = run_gemm({256, false, false, Epi::kStore}, p, R, st->num_sms, s, "down")))
+    if ((rc = run_gemm({256, false, false, Epi::kStore, pair_rows}, p, pair_rows ? R2 : R,
+                       st->num_sms, s, "down")))
       return rc;
   }
   return ok();
@@ -654,7 +688,12 @@ int moe_lora_grouped_mlp_bwd(const moe_dims* dims, const moe_bf16* dYp, const mo
   const int64_t RG = (N + 127) / 128;  // tiles of the plain 128-row grid (rank-r products)
   const GemmParams base = base_params(dims, offsets, tile_off, sorted_src, topk_w, st->status);
   cudaStream_t s = stream;
-  const int ntiles_f = (f + kDgradBN - 1) / kDgradBN;
+  const bool pair_dy = pair_tiles(dims, kPairDgradDn, dYp != nullptr);
+  const bool pair_rows = pair_tiles(dims, kPairDgradGu, true);
+  const int64_t R2 = max_pair_tiles(dims->T, dims->k + dims->shared_expert, G);
+  // down-projection dgrad: 256-feature tiles on CTA pairs, else 192
+  const int bn_dd = pair_dy ? 256 : kDgradBN;
+  const int ntiles_f = (f + bn_dd - 1) / bn_dd;
   const int nparts = kDwPartsPerTile * ntiles_f;
 
   const int64_t Nr = N * r, N2f = N * 2 * f;
@@ -736,11 +775,13 @@ int moe_lora_grouped_mlp_bwd(const moe_dims* dims, const moe_bf16* dYp, const mo
     SLICE(p, 1, w.us, N, r, MAP3(p.sl[1].b, A_dn, G, r, f, 64, 64), r);
     SLICE(p, 2, w.us + Nr, N, r, MAP3(p.sl[2].b, A_dn, G, r, f, 64, 64), r);
     p.nslices = 3; p.N = f; p.n_ntiles = ntiles_f;
-    {  // one 4-D box per K block (the 3-D maps stay as fallback)
+    {  // one 4-D box per K block (the 3-D maps stay as fallback); a pair's
+       // CTAs stage 128 columns each
+      const uint32_t chunks = (pair_dy ? bn_dd / 2 : bn_dd) / 64;
       GemmSlice q[3] = {p.sl[0], p.sl[1], p.sl[2]};
-      if (make_map_mn4d(&q[0].b, W_dn, G, d, f, 64, kDgradBN / 64) &&
-          make_map_mn4d(&q[1].b, A_dn, G, r, f, 64, kDgradBN / 64) &&
-          make_map_mn4d(&q[2].b, A_dn, G, r, f, 64, kDgradBN / 64)) {
+      if (make_map_mn4d(&q[0].b, W_dn, G, d, f, 64, chunks) &&
+          make_map_mn4d(&q[1].b, A_dn, G, r, f, 64, chunks) &&
+          make_map_mn4d(&q[2].b, A_dn, G, r, f, 64, chunks)) {
         for (int i = 0; i < 3; ++i) p.sl[i] = q[i];
         p.b4d = 1;
       }
@@ -750,8 +791,8 @@ int moe_lora_grouped_mlp_bwd(const moe_dims* dims, const moe_bf16* dYp, const mo
     // dh planes as TMA store targets: 16 features x 32 rows per store
     p.om_ok = make_map_2d(&p.om_hi, w.dh, N, 2 * f, 32, 16, false) &&
               make_map_2d(&p.om_lo, w.dh + N2f, N, 2 * f, 32, 16, false);
-    if ((rc = run_gemm({kDgradBN, true, false, Epi::kDgradDn}, p, R, st->num_sms, s,
-                       "dgrad_dn")))
+    if ((rc = run_gemm({bn_dd, true, false, Epi::kDgradDn, pair_dy}, p, pair_dy ? R2 : R,
+                       st->num_sms, s, "dgrad_dn")))
       return rc;
   }
   if ((rc = stream_dep(st->ev[1], s, aux))) return rc;
@@ -778,14 +819,16 @@ int moe_lora_grouped_mlp_bwd(const moe_dims* dims, const moe_bf16* dYp, const mo
     SLICE(p, 1, w.vs, N, r, MAP3(p.sl[1].b, A_gu, G, r, d, 64, 64), r);
     p.nslices = 2; p.N = d; p.n_ntiles = (d + 255) / 256; p.out0 = dXp; p.ld0 = d;
     {  // one 4-D box per K block (the 3-D maps stay as fallback)
+      const uint32_t chunks = pair_rows ? 2 : 4;
       GemmSlice q[2] = {p.sl[0], p.sl[1]};
-      if (make_map_mn4d(&q[0].b, W_gu, G, 2 * f, d, 64, 4) &&
-          make_map_mn4d(&q[1].b, A_gu, G, r, d, 64, 4)) {
+      if (make_map_mn4d(&q[0].b, W_gu, G, 2 * f, d, 64, chunks) &&
+          make_map_mn4d(&q[1].b, A_gu, G, r, d, 64, chunks)) {
         for (int i = 0; i < 2; ++i) p.sl[i] = q[i];
         p.b4d = 1;
       }
     }
-    if ((rc = run_gemm({256, true, false, Epi::kStore}, p, R, st->num_sms, s, "dgrad_gu")))
+    if ((rc = run_gemm({256, true, false, Epi::kStore, pair_rows}, p, pair_rows ? R2 : R,
+                       st->num_sms, s, "dgrad_gu")))
       return rc;
   }
   // join: everything on the second stream completes before later work on s

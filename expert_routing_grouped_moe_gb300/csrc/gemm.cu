@@ -57,9 +57,6 @@ constexpr uint32_t kChunkBytes = 64 * 128;      // one [64][64] bf16 swizzle blo
 constexpr uint32_t kStgTileBytes = 32 * 128;    // one staging tile: 32 rows x 128 B
 constexpr uint32_t kRingMax = 192 * 1024;
 constexpr uint32_t kSmemMax = 232448;           // opt-in shared memory per CTA
-// Groups whose tile offsets are kept in shared memory (G + 1 <= kTileTabInts);
-// beyond that the tile scheduler searches tile_off in global memory.
-constexpr int kTileTabInts = 448;
 constexpr uint32_t kFixedSmem = 1024 /*alignment slack*/ + 256 /*barriers*/ +
                                 kTileTabInts * 4 /*tile_off copy*/;
 
@@ -69,9 +66,10 @@ __host__ __device__ constexpr uint32_t pow2_at_least(uint32_t v) {
   return p;
 }
 
-template <int BN, int EPI>
+template <int BN, int EPI, bool PAIR = false>
 struct Cfg {
-  static constexpr uint32_t kBStageBytes = BN * BK * 2;
+  // a CTA of a pair stages half of B's BN columns
+  static constexpr uint32_t kBStageBytes = (PAIR ? BN / 2 : BN) * BK * 2;
   static constexpr uint32_t kStageBytes = kAStageBytes + kBStageBytes;
   static constexpr bool kGrid = EPI == static_cast<int>(Epi::kLoRAGrid);
   // staging per epilogue warp: one tile, two for the SwiGLU backward (h in,
@@ -82,7 +80,8 @@ struct Cfg {
   static constexpr uint32_t kRingFit =
       (kSmemMax - kFixedSmem - kEpiWarps * kStgBytes) / kStageBytes * kStageBytes;
   static constexpr uint32_t kRingCap = kGrid ? kRingFit : kRingMax;
-  // 4 / 4 / 6 stages for BN 256 / 192 (dgrad) / 128 (weight gradients); 7 in grid mode
+  // 4 / 4 / 6 stages for BN 256 / 192 (dgrad) / 128 (weight gradients); 7 in grid mode;
+  // pairs: 6 stages of 32 KB (5 with the SwiGLU backward's two staging tiles)
   static constexpr int kStages = (kRingFit < kRingCap ? kRingFit : kRingCap) / kStageBytes;
   static constexpr uint32_t kTmemCols = pow2_at_least(2 * BN);  // power of two >= 32
   static constexpr size_t kSmemBytes =
@@ -280,23 +279,26 @@ __device__ __forceinline__ TileInfo grid_info(const GemmParams& p, int t, const 
 }
 
 // The sequence of work units every role of a CTA walks: its tiles t =
-// blockIdx.x + i * gridDim.x and, in grid mode, each tile's passes.
+// first + i * stride (first = blockIdx.x, stride = gridDim.x; for CTA pairs
+// the pair's index and the number of pairs) and, in grid mode, each tile's
+// passes.
 struct Unit {
   int t, ps;
   GridTile gt;
 };
 template <bool GRID>
-__device__ __forceinline__ Unit unit_first(const GemmParams& p, const int* tab, int num_tiles) {
-  Unit u{static_cast<int>(blockIdx.x), 0, GridTile{0, 0, 1}};
+__device__ __forceinline__ Unit unit_first(const GemmParams& p, const int* tab, int num_tiles,
+                                           int first) {
+  Unit u{first, 0, GridTile{0, 0, 1}};
   if (GRID && u.t < num_tiles) u.gt = grid_tile<GRID>(p, u.t, tab);
   return u;
 }
 template <bool GRID>
 __device__ __forceinline__ void unit_next(Unit& u, const GemmParams& p, const int* tab,
-                                          int num_tiles) {
+                                          int num_tiles, int stride) {
   if (GRID && ++u.ps < u.gt.npass) return;
   u.ps = 0;
-  u.t += gridDim.x;
+  u.t += stride;
   if (GRID && u.t < num_tiles) u.gt = grid_tile<GRID>(p, u.t, tab);
 }
 
@@ -335,6 +337,63 @@ __device__ __forceinline__ TileInfo tile_info(const GemmParams& p, int t, const 
     ti.nkb = (ti.nvalid + BK - 1) / BK;
     ti.nk = ti.nkb * p.nslices;
   }
+  return ti;
+}
+
+// ------------------------------------------------------------ CTA pairs
+// A pair of CTAs (a cluster of two) computes 256-row tiles: pair tile i of
+// group g covers its rows [256 i, 256 i + 256), the even CTA rows
+// [256 i, 256 i + 128) and the odd one the next 128.  tab[g] = the pair tiles
+// of all earlier groups (sum of ceil(count / 256)), built in shared memory
+// by every CTA at start-up from the group offsets (G + 1 <= kTileTabInts);
+// offsets follow at tab + G + 1 when both fit.
+constexpr int kPairM = 2 * BM;
+
+__device__ __forceinline__ void pair_tile_table(const GemmParams& p, int* tab, int* wsum) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  auto tiles = [&](int g) {
+    return g < p.G ? (__ldg(p.offsets + g + 1) - __ldg(p.offsets + g) + kPairM - 1) / kPairM : 0;
+  };
+  // thread i: groups 2i and 2i + 1 (G + 1 <= 2 * blockDim.x)
+  const int g0 = 2 * static_cast<int>(threadIdx.x);
+  const int v0 = tiles(g0), v1 = tiles(g0 + 1);
+  int x = v0 + v1;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += y;
+  }
+  if (lane == 31) wsum[warp] = x;
+  __syncthreads();
+  int base = 0;
+  for (int w = 0; w < warp; ++w) base += wsum[w];
+  const int excl = base + x - v0 - v1;
+  if (g0 <= p.G) tab[g0] = excl;
+  if (g0 + 1 <= p.G) tab[g0 + 1] = excl + v0;
+}
+
+template <bool ROWS = true>
+__device__ __forceinline__ TileInfo pair_tile_info(const GemmParams& p, int t, const int* tab,
+                                                   uint32_t crank) {
+  TileInfo ti;
+  ti.mt = t / p.n_ntiles;
+  ti.nt = t - ti.mt * p.n_ntiles;
+  ti.g = group_of_tile(nullptr, tab, p.G, ti.mt);
+  ti.nk = 0;
+  for (int s = 0; s < p.nslices; ++s) ti.nk += (p.sl[s].K + BK - 1) / BK;
+  ti.row0 = 0;
+  ti.nvalid = 0;
+  if (ROWS) {
+    const int* otab = 2 * (p.G + 1) <= kTileTabInts ? tab + p.G + 1 : nullptr;
+    const int local = ti.mt - tab[ti.g];
+    const int off = otab ? otab[ti.g] : __ldg(p.offsets + ti.g);
+    const int cnt = (otab ? otab[ti.g + 1] : __ldg(p.offsets + ti.g + 1)) - off;
+    const int first = local * kPairM + static_cast<int>(crank) * BM;
+    ti.row0 = off + first;
+    ti.nvalid = min(BM, cnt - first);  // <= 0: this CTA's half lies past the group's end
+  }
+  ti.nkb = 0;
+  ti.nx = ti.rlo = ti.rmid = ti.rhi = 0;
   return ti;
 }
 
@@ -680,13 +739,15 @@ __device__ __forceinline__ void epi_wgrad_full(const GemmParams& p, const TileIn
   }
 }
 
-template <int BN, bool B_MN, bool WGRAD, int EPI>
+template <int BN, bool B_MN, bool WGRAD, int EPI, bool PAIR>
 __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant__ GemmParams p) {
-  using C = Cfg<BN, EPI>;
+  using C = Cfg<BN, EPI, PAIR>;
   constexpr int S = C::kStages;
   constexpr bool GRID = EPI == static_cast<int>(Epi::kLoRAGrid);
+  static_assert(!PAIR || (!WGRAD && !GRID), "CTA pairs serve the rows-mode tiles");
   extern __shared__ uint8_t smem_raw[];
-  // 1024-byte aligned stage ring (128B swizzle atoms are 8 rows x 128 B)
+  // 1024-byte aligned stage ring (128B swizzle atoms are 8 rows x 128 B); the
+  // same offsets in both CTAs of a pair (same kernel, same dynamic size)
   const uint32_t raw_addr = smem_u32(smem_raw);
   uint8_t* smem = smem_raw + ((1024 - (raw_addr & 1023)) & 1023);
   uint8_t* ring = smem;
@@ -698,15 +759,21 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
   uint64_t* drain_bar = tempty_bar + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain_bar + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  int* scan_tmp = reinterpret_cast<int*>(reinterpret_cast<uint8_t*>(full_bar) + 192);
   // shared-memory copy of the routing tables the tile scheduler reads:
-  // tile_off then offsets (row tiles; offsets only when both fit), or
-  // offsets (weight-gradient and grid tiles)
+  // tile_off then offsets (row tiles; offsets only when both fit), the pair
+  // tile offsets then offsets (CTA pairs), or offsets (weight-gradient and
+  // grid tiles)
   int* tile_tab = reinterpret_cast<int*>(reinterpret_cast<uint8_t*>(full_bar) + 256);
   const int* tab = p.G + 1 <= kTileTabInts ? tile_tab : nullptr;
 
-
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
+  // CTA pairs: this CTA's rank in the pair; the leader (rank 0) issues the MMAs
+  const uint32_t crank = PAIR ? cluster_ctarank() : 0u;
+  const bool leader = crank == 0;
+  const int first_unit = PAIR ? static_cast<int>(blockIdx.x >> 1) : static_cast<int>(blockIdx.x);
+  const int unit_stride = PAIR ? static_cast<int>(gridDim.x >> 1) : static_cast<int>(gridDim.x);
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < S; ++i) {
@@ -715,12 +782,15 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(tfull_bar + i, 1);
-      mbar_init(tempty_bar + i, kEpiWarps * 32);
+      // one arrival per epilogue warp (of both CTAs of a pair)
+      mbar_init(tempty_bar + i, kEpiWarps * (PAIR ? 2 : 1));
     }
     mbar_init(drain_bar, 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
+  // a pair's barriers are initialised before either CTA signals the other's
+  if constexpr (PAIR) cluster_sync();
   if (warp == 0 && lane == 0) {
     for (int s = 0; s < p.nslices; ++s) {
       prefetch_tmap(&p.sl[s].a);
@@ -736,13 +806,24 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
     }
   }
   if (warp == 1) {
-    tmem_alloc(tmem_slot, C::kTmemCols);
-    tmem_relinquish();
+    if constexpr (PAIR) {
+      tmem_alloc_pair(tmem_slot, C::kTmemCols);
+      tmem_relinquish_pair();
+    } else {
+      tmem_alloc(tmem_slot, C::kTmemCols);
+      tmem_relinquish();
+    }
   }
   // everything above overlaps the previous kernel; from here on its outputs
   // (routing tables, permuted rows, intermediates) are read
   pdl_wait();
-  if (tab != nullptr) {
+  if constexpr (PAIR) {
+    // the host launches pairs only when the table fits (tab != nullptr)
+    pair_tile_table(p, tile_tab, scan_tmp);
+    if (2 * (p.G + 1) <= kTileTabInts)
+      for (int i = threadIdx.x; i <= p.G; i += blockDim.x)
+        tile_tab[p.G + 1 + i] = __ldg(p.offsets + i);
+  } else if (tab != nullptr) {
     const int32_t* src = (WGRAD || GRID) ? p.offsets : p.tile_off;
     for (int i = threadIdx.x; i <= p.G; i += blockDim.x) tile_tab[i] = __ldg(src + i);
     if (!WGRAD && !GRID && 2 * (p.G + 1) <= kTileTabInts)
@@ -756,6 +837,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
   const int num_tiles =
       WGRAD  ? p.G * p.n_ntiles * p.n_btiles
       : GRID ? min((__ldg(p.offsets + p.G) + BM - 1) / BM, p.max_tiles)
+      : PAIR ? min(tile_tab[p.G] * p.n_ntiles, p.max_tiles)
              : min(__ldg(p.tile_off + p.G) * p.n_ntiles, p.max_tiles);
 
   if (warp == 0 && (lane == 0 || p.gather_any)) {
@@ -766,7 +848,9 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
     // 128B-swizzled layout TMA would produce.  When any slice gathers, every
     // lane arrives on each stage's full barrier (which then expects 1 + 32
     // arrivals) once its copies so far have completed; the MMA issuer fences
-    // them for the async proxy.
+    // them for the async proxy.  In a CTA pair each CTA copies its own A rows
+    // and its own half of B; both count their bytes on the leader's full
+    // barrier, which the leader arms with the bytes of both.
     int stage = 0;
     uint32_t phase = 0;
     uint32_t armed_bits = 0, armed_phase = 0;  // stages armed, and with which parity
@@ -783,10 +867,11 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
       }
     };
     int y[4] = {0, 0, 0, 0};
-    for (Unit u = unit_first<GRID>(p, tab, num_tiles); u.t < num_tiles && ok;
-         unit_next<GRID>(u, p, tab, num_tiles)) {
-      const TileInfo ti =
-          GRID ? grid_info(p, u.t, u.gt, u.ps, tab) : tile_info<WGRAD>(p, u.t, tab);
+    for (Unit u = unit_first<GRID>(p, tab, num_tiles, first_unit); u.t < num_tiles && ok;
+         unit_next<GRID>(u, p, tab, num_tiles, unit_stride)) {
+      const TileInfo ti = PAIR ? pair_tile_info(p, u.t, tab, crank)
+                          : GRID ? grid_info(p, u.t, u.gt, u.ps, tab)
+                                 : tile_info<WGRAD>(p, u.t, tab);
       if (!WGRAD && p.gather_any) lane_rows(ti.row0, ti.nvalid, 4, y);
       int cs = 0, ckc = 0;  // rows mode: slice and K offset of the next K block
       for (int kb = 0; kb < ti.nk; ++kb) {
@@ -806,6 +891,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
           row = ti.row0 + b * BK;
           if (p.sl[s].gather) lane_rows(row, ti.nvalid - b * BK, 2, y);
         }
+        (void)kext;
         const bool gat = p.sl[s].gather != 0;
         int w_ok = 1;
         uint64_t* fb = full_bar + stage;
@@ -814,49 +900,74 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
         if (lane == 0) {
           w_ok = mbar_wait(empty_bar + stage, phase ^ 1u, abort_flag, kWaitTimeoutNs);
           if (w_ok) {
-            const uint32_t b_bytes = GRID ? ti.nx * kChunkBytes : C::kBStageBytes;
-            mbar_expect_tx(fb, (gat ? 0u : kAStageBytes) + b_bytes);
             armed_bits |= 1u << stage;
             armed_phase = (armed_phase & ~(1u << stage)) | (phase << stage);
-            if (!WGRAD) {
+            if constexpr (PAIR) {
               const CUtensorMap* mb = &p.sl[s].b;
-              if (!gat) tma_load_2d(sa, &p.sl[s].a, fb, kc, ti.row0);
-              if (GRID) {
-                // one 64-row (K-major) / 64-column (MN-major) block per group
-                for (int x = 0; x < ti.nx; ++x) {
-                  if (!B_MN) tma_load_3d(sb + x * kChunkBytes, mb, fb, kc, 0, ti.g + x);
-                  else tma_load_3d(sb + x * kChunkBytes, mb, fb, 0, kc, ti.g + x);
-                }
-              } else if (p.b4d) {
-                // the whole B tile in one box: gate/up halves or MN chunks
-                if (!B_MN) tma_load_4d(sb, mb, fb, kc, ti.nt * (BN / 2), 0, ti.g);
-                else tma_load_4d(sb, mb, fb, 0, kc, ti.nt * (BN / 64), ti.g);
-              } else if (!B_MN) {
-                if (p.b_split) {
-                  const int n0 = ti.nt * (BN / 2);
-                  tma_load_3d(sb, mb, fb, kc, n0, ti.g);
-                  tma_load_3d(sb + (BN / 2) * 128, mb, fb, kc, n0 + p.b_split, ti.g);
+              const uint32_t fbl = mapa_shared(smem_u32(fb), 0u);  // the leader's barrier
+              if (leader) mbar_expect_tx(fb, 2u * C::kStageBytes);
+              tma_load_2d_pair(sa, &p.sl[s].a, fbl, kc, ti.row0);
+              // this CTA's half of the B tile: its BN / 2 columns
+              const int half = static_cast<int>(crank) * (BN / 2);
+              if (B_MN) {
+                if (p.b4d) {
+                  tma_load_4d_pair(sb, mb, fbl, 0, kc, (ti.nt * BN + half) / 64, ti.g);
                 } else {
-                  tma_load_3d(sb, mb, fb, kc, ti.nt * BN, ti.g);
-                }
-              } else {
 #pragma unroll
-                for (int c = 0; c < BN / 64; ++c)
-                  tma_load_3d(sb + c * kChunkBytes, mb, fb, ti.nt * BN + c * 64, kc, ti.g);
+                  for (int c = 0; c < BN / 128; ++c)
+                    tma_load_3d_pair(sb + c * kChunkBytes, mb, fbl, ti.nt * BN + half + c * 64, kc,
+                                     ti.g);
+                }
+              } else if (p.b_split) {
+                // gate_up: the even CTA stages the gate rows, the odd one the up rows
+                tma_load_3d_pair(sb, mb, fbl, kc,
+                                 ti.nt * (BN / 2) + static_cast<int>(crank) * p.b_split, ti.g);
+              } else {
+                tma_load_3d_pair(sb, mb, fbl, kc, ti.nt * BN + half, ti.g);
               }
             } else {
-              if (!gat) {
-                tma_load_2d(sa, &p.sl[s].a, fb, ti.mt * BM, row);
-                tma_load_2d(sa + kChunkBytes, &p.sl[s].a, fb, ti.mt * BM + 64, row);
-              }
-              if constexpr (EPI == static_cast<int>(Epi::kWgradFull)) {
-                // B = one wide row matrix: this tile's BN columns as 64-column chunks
+              const uint32_t b_bytes = GRID ? ti.nx * kChunkBytes : C::kBStageBytes;
+              mbar_expect_tx(fb, (gat ? 0u : kAStageBytes) + b_bytes);
+              if (!WGRAD) {
+                const CUtensorMap* mb = &p.sl[s].b;
+                if (!gat) tma_load_2d(sa, &p.sl[s].a, fb, kc, ti.row0);
+                if (GRID) {
+                  // one 64-row (K-major) / 64-column (MN-major) block per group
+                  for (int x = 0; x < ti.nx; ++x) {
+                    if (!B_MN) tma_load_3d(sb + x * kChunkBytes, mb, fb, kc, 0, ti.g + x);
+                    else tma_load_3d(sb + x * kChunkBytes, mb, fb, 0, kc, ti.g + x);
+                  }
+                } else if (p.b4d) {
+                  // the whole B tile in one box: gate/up halves or MN chunks
+                  if (!B_MN) tma_load_4d(sb, mb, fb, kc, ti.nt * (BN / 2), 0, ti.g);
+                  else tma_load_4d(sb, mb, fb, 0, kc, ti.nt * (BN / 64), ti.g);
+                } else if (!B_MN) {
+                  if (p.b_split) {
+                    const int n0 = ti.nt * (BN / 2);
+                    tma_load_3d(sb, mb, fb, kc, n0, ti.g);
+                    tma_load_3d(sb + (BN / 2) * 128, mb, fb, kc, n0 + p.b_split, ti.g);
+                  } else {
+                    tma_load_3d(sb, mb, fb, kc, ti.nt * BN, ti.g);
+                  }
+                } else {
 #pragma unroll
-                for (int c = 0; c < BN / 64; ++c)
-                  tma_load_2d(sb + c * kChunkBytes, &p.wb_hi, fb, ti.nt * BN + c * 64, row);
+                  for (int c = 0; c < BN / 64; ++c)
+                    tma_load_3d(sb + c * kChunkBytes, mb, fb, ti.nt * BN + c * 64, kc, ti.g);
+                }
               } else {
-                tma_load_2d(sb, &p.wb_hi, fb, 0, row);
-                tma_load_2d(sb + kChunkBytes, &p.wb_lo, fb, 0, row);
+                if (!gat) {
+                  tma_load_2d(sa, &p.sl[s].a, fb, ti.mt * BM, row);
+                  tma_load_2d(sa + kChunkBytes, &p.sl[s].a, fb, ti.mt * BM + 64, row);
+                }
+                if constexpr (EPI == static_cast<int>(Epi::kWgradFull)) {
+                  // B = one wide row matrix: this tile's BN columns as 64-column chunks
+#pragma unroll
+                  for (int c = 0; c < BN / 64; ++c)
+                    tma_load_2d(sb + c * kChunkBytes, &p.wb_hi, fb, ti.nt * BN + c * 64, row);
+                } else {
+                  tma_load_2d(sb, &p.wb_hi, fb, 0, row);
+                  tma_load_2d(sb + kChunkBytes, &p.wb_lo, fb, 0, row);
+                }
               }
             }
           }
@@ -911,28 +1022,41 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
     }
     if (lanes_arrive) cp_async_wait_all();  // no copy outlives the producer
     if (!ok && lane == 0) {
-      // drain copies still in flight into this CTA's shared memory
-      for (int i = 0; i < S; ++i)
-        if ((armed_bits >> i) & 1u) {
-          volatile int never = 0;
-          mbar_wait(full_bar + i, (armed_phase >> i) & 1u, &never, 200000000ull);
+      if (!PAIR || leader) {
+        // drain copies still in flight into this CTA's shared memory (a
+        // leader's barriers also count its partner's bytes)
+        for (int i = 0; i < S; ++i)
+          if ((armed_bits >> i) & 1u) {
+            volatile int never = 0;
+            mbar_wait(full_bar + i, (armed_phase >> i) & 1u, &never, 200000000ull);
+          }
+      } else if (armed_bits != 0u) {
+        // a partner's copies complete on the leader's barriers: give the ones
+        // in flight a fixed 2 ms to land before the CTA moves on
+        const uint64_t t0 = globaltimer_ns();
+        while (globaltimer_ns() - t0 < 2000000ull) {
         }
+      }
     }
-  } else if (warp == 1 && (WGRAD || lane == 0)) {
+  } else if (warp == 1 && (WGRAD || lane == 0) && (!PAIR || leader)) {
     // --------------------------------------------------------- MMA issuer
     // Lane 0 waits and issues.  In the weight-gradient kernel the whole warp
     // runs this loop and zeroes the rows past a group's end in the group's
-    // last K block; elsewhere lane 0 runs it alone.
-    constexpr uint32_t idesc_full = idesc_bf16(BM, BN, WGRAD, B_MN || WGRAD);
+    // last K block; elsewhere lane 0 runs it alone.  In a CTA pair only the
+    // leader issues (M = 256 over both CTAs' A rows and TMEM) and its commits
+    // arrive on the barriers of both CTAs.
+    constexpr int kM = PAIR ? kPairM : BM;
+    constexpr uint32_t idesc_full = idesc_bf16(kM, BN, WGRAD, B_MN || WGRAD);
     constexpr uint32_t idesc_one = idesc_bf16(BM, 64, false, B_MN);  // grid pass of one group
     int stage = 0;
     uint32_t phase = 0;
     int local = 0;
     bool ok = true;
-    for (Unit u = unit_first<GRID>(p, tab, num_tiles); u.t < num_tiles && ok;
-         unit_next<GRID>(u, p, tab, num_tiles), ++local) {
-      const TileInfo ti =
-          GRID ? grid_info(p, u.t, u.gt, u.ps, tab) : tile_info<WGRAD, WGRAD>(p, u.t, tab);
+    for (Unit u = unit_first<GRID>(p, tab, num_tiles, first_unit); u.t < num_tiles && ok;
+         unit_next<GRID>(u, p, tab, num_tiles, unit_stride), ++local) {
+      const TileInfo ti = PAIR ? pair_tile_info<false>(p, u.t, tab, crank)
+                          : GRID ? grid_info(p, u.t, u.gt, u.ps, tab)
+                                 : tile_info<WGRAD, WGRAD>(p, u.t, tab);
       const uint32_t idesc = (GRID && ti.nx == 1) ? idesc_one : idesc_full;
       const int buf = local & 1;
       const uint32_t use = static_cast<uint32_t>(local >> 1);
@@ -987,19 +1111,24 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
           constexpr uint32_t kBStep = ((B_MN || WGRAD) ? 2048u : 32u) >> 4;
           const uint64_t ad = sdesc_sw128(sa, WGRAD ? kChunkBytes : 16u, 1024);
           const uint64_t bd = sdesc_sw128(sb, (B_MN || WGRAD) ? kChunkBytes : 16u, 1024);
+          auto mma = [&](uint64_t a, uint64_t b, uint32_t acc) {
+            if constexpr (PAIR) tc_mma_bf16_pair(d_tmem, a, b, idesc, acc);
+            else tc_mma_bf16(d_tmem, a, b, idesc, acc);
+          };
           if (nk16 == 4) {
-            tc_mma_bf16(d_tmem, ad, bd, idesc, accum);
-            tc_mma_bf16(d_tmem, ad + kAStep, bd + kBStep, idesc, 1u);
-            tc_mma_bf16(d_tmem, ad + 2 * kAStep, bd + 2 * kBStep, idesc, 1u);
-            tc_mma_bf16(d_tmem, ad + 3 * kAStep, bd + 3 * kBStep, idesc, 1u);
+            mma(ad, bd, accum);
+            mma(ad + kAStep, bd + kBStep, 1u);
+            mma(ad + 2 * kAStep, bd + 2 * kBStep, 1u);
+            mma(ad + 3 * kAStep, bd + 3 * kBStep, 1u);
             accum = 1;
           } else {
             for (int kk = 0; kk < nk16; ++kk) {
-              tc_mma_bf16(d_tmem, ad + kk * kAStep, bd + kk * kBStep, idesc, accum);
+              mma(ad + kk * kAStep, bd + kk * kBStep, accum);
               accum = 1;
             }
           }
-          tc_commit(empty_bar + stage);
+          if constexpr (PAIR) tc_commit_pair_mc(empty_bar + stage, 3);
+          else tc_commit(empty_bar + stage);
         }
         if constexpr (WGRAD) __syncwarp();
         if (!WGRAD) {
@@ -1015,12 +1144,16 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
         }
       }
       if (!ok) break;
-      if (lane == 0) tc_commit(tfull_bar + buf);
+      if (lane == 0) {
+        if constexpr (PAIR) tc_commit_pair_mc(tfull_bar + buf, 3);
+        else tc_commit(tfull_bar + buf);
+      }
       if constexpr (WGRAD) __syncwarp();
     }
     // all MMAs issued by this warp complete before TMEM is released
     if (lane == 0) {
-      tc_commit(drain_bar);
+      if constexpr (PAIR) tc_commit_pair(drain_bar);
+      else tc_commit(drain_bar);
       volatile int never = 0;
       mbar_wait(drain_bar, 0, &never, 200000000ull);
     }
@@ -1032,10 +1165,11 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
     const int hf = ew >> 2;   // column half owned by this warp
     const uint32_t stg = smem_u32(stage_tiles + ew * C::kStgBytes);
     int local = 0;
-    for (Unit u = unit_first<GRID>(p, tab, num_tiles); u.t < num_tiles;
-         unit_next<GRID>(u, p, tab, num_tiles), ++local) {
-      const TileInfo ti =
-          GRID ? grid_info(p, u.t, u.gt, u.ps, tab) : tile_info<WGRAD>(p, u.t, tab);
+    for (Unit u = unit_first<GRID>(p, tab, num_tiles, first_unit); u.t < num_tiles;
+         unit_next<GRID>(u, p, tab, num_tiles, unit_stride), ++local) {
+      const TileInfo ti = PAIR ? pair_tile_info(p, u.t, tab, crank)
+                          : GRID ? grid_info(p, u.t, u.gt, u.ps, tab)
+                                 : tile_info<WGRAD>(p, u.t, tab);
       const int buf = local & 1;
       const uint32_t use = static_cast<uint32_t>(local >> 1);
       if (!mbar_wait(tfull_bar + buf, use & 1u, abort_flag, kWaitTimeoutNs)) break;
@@ -1060,7 +1194,12 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
         epi_dgrad_dn<BN>(p, ti, tq, hf, row0, nrows, lane, stg);
       }
       tc_fence_before();
-      mbar_arrive(tempty_bar + buf);
+      __syncwarp();
+      if (lane == 0) {
+        // the accumulator is free: the MMA issuer waits on the leader's barrier
+        if constexpr (PAIR) mbar_arrive_cluster(mapa_shared(smem_u32(tempty_bar + buf), 0u));
+        else mbar_arrive(tempty_bar + buf);
+      }
     }
     // TMA stores issued by this warp complete before the CTA's shared memory
     // goes away
@@ -1071,9 +1210,13 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
   }
 
   __syncthreads();
+  // neither CTA of a pair releases TMEM or exits while the other may still
+  // signal its barriers or (the leader's MMAs) read its shared memory
+  if constexpr (PAIR) cluster_sync();
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tmem_base, C::kTmemCols);
+    if constexpr (PAIR) tmem_dealloc_pair(tmem_base, C::kTmemCols);
+    else tmem_dealloc(tmem_base, C::kTmemCols);
   }
   if (threadIdx.x == 0 && *abort_flag) atomicCAS(p.status, 0, kErrTimeout);
 }
@@ -1092,16 +1235,45 @@ __global__ void wait_selftest_kernel(int* status, unsigned long long timeout_ns)
   }
 }
 
-template <int BN, bool B_MN, bool WGRAD, int EPI>
+template <int BN, bool B_MN, bool WGRAD, int EPI, bool PAIR = false>
 cudaError_t launch_one(const GemmParams& p, int num_sms, cudaStream_t s) {
-  using C = Cfg<BN, EPI>;
+  using C = Cfg<BN, EPI, PAIR>;
   static_assert(C::kSmemBytes <= 232448, "shared memory budget");
-  auto kern = gemm_kernel<BN, B_MN, WGRAD, EPI>;
+  auto kern = gemm_kernel<BN, B_MN, WGRAD, EPI, PAIR>;
   cudaError_t e =
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            static_cast<int>(C::kSmemBytes));
   if (e != cudaSuccess) return e;
   const int tiles = WGRAD ? p.G * p.n_ntiles * p.n_btiles : p.max_tiles;
+  if constexpr (PAIR) {
+    // persistent pairs: as many clusters of two as can be resident at once
+    // (one CTA per SM), looked up once per device
+    static int max_pairs[64] = {};
+    int dev = 0;
+    e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    if (max_pairs[dev] <= 0) {
+      cudaLaunchConfig_t cfg = {};
+      cfg.gridDim = dim3(2 * (num_sms / 2));
+      cfg.blockDim = dim3(kThreads);
+      cfg.dynamicSmemBytes = C::kSmemBytes;
+      cudaLaunchAttribute attr[1];
+      attr[0].id = cudaLaunchAttributeClusterDimension;
+      attr[0].val.clusterDim.x = 2;
+      attr[0].val.clusterDim.y = 1;
+      attr[0].val.clusterDim.z = 1;
+      cfg.attrs = attr;
+      cfg.numAttrs = 1;
+      int n = 0;
+      e = cudaOccupancyMaxActiveClusters(&n, kern, &cfg);
+      if (e != cudaSuccess) return e;
+      if (n <= 0) return cudaErrorInvalidConfiguration;
+      max_pairs[dev] = n < num_sms / 2 ? n : num_sms / 2;
+    }
+    const int pairs = tiles < max_pairs[dev] ? (tiles > 0 ? tiles : 1) : max_pairs[dev];
+    return launch_pdl_cluster(kern, dim3(2 * pairs), dim3(kThreads), C::kSmemBytes, s, 2u, p);
+  }
   const int grid = tiles < num_sms ? (tiles > 0 ? tiles : 1) : num_sms;
   return launch_pdl(kern, dim3(grid), dim3(kThreads), C::kSmemBytes, s, p);
 }
@@ -1125,6 +1297,15 @@ cudaError_t launch_gemm(const GemmShape& sh, const GemmParams& p, int num_sms, c
     if (sh.BN == 128 && e == kWg) return launch_one<128, true, true, kWg>(p, num_sms, s);
     if (sh.BN == 256 && e == static_cast<int>(Epi::kWgradFull))
       return launch_one<256, true, true, static_cast<int>(Epi::kWgradFull)>(p, num_sms, s);
+    return cudaErrorInvalidValue;
+  }
+  if (sh.pair) {
+    // 256-row tiles on CTA pairs; the tile table must fit in shared memory
+    if (p.G + 1 > kTileTabInts || p.gather_any || sh.BN != 256) return cudaErrorInvalidValue;
+    if (!sh.b_mn && e == kSw) return launch_one<256, false, false, kSw, true>(p, num_sms, s);
+    if (!sh.b_mn && e == kSt) return launch_one<256, false, false, kSt, true>(p, num_sms, s);
+    if (sh.b_mn && e == kSt) return launch_one<256, true, false, kSt, true>(p, num_sms, s);
+    if (sh.b_mn && e == kDd) return launch_one<256, true, false, kDd, true>(p, num_sms, s);
     return cudaErrorInvalidValue;
   }
   if (sh.BN == 256 && !sh.b_mn) {

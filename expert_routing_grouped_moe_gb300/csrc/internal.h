@@ -27,14 +27,68 @@ cudaError_t launch_pdl(void (*kernel)(Params...), dim3 grid, dim3 block, size_t 
   cfg.numAttrs = 1;
   return cudaLaunchKernelEx(&cfg, kernel, static_cast<Args&&>(args)...);
 }
+// The same with the CTAs grouped into clusters of cluster_x (CTA pairs: 2).
+template <typename... Params, typename... Args>
+cudaError_t launch_pdl_cluster(void (*kernel)(Params...), dim3 grid, dim3 block, size_t smem,
+                               cudaStream_t s, unsigned cluster_x, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (cluster_x > 1) {
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = cluster_x;
+    attr[1].val.clusterDim.y = 1;
+    attr[1].val.clusterDim.z = 1;
+    cfg.numAttrs = 2;
+  }
+  return cudaLaunchKernelEx(&cfg, kernel, static_cast<Args&&>(args)...);
+}
 
 constexpr int kTileM = 128;            // rows per M tile (= permuted layout granularity)
+constexpr int kPairTileM = 256;        // rows per tile of a CTA pair
+// Groups whose tile offsets the GEMMs keep in shared memory (G + 1 <=
+// kTileTabInts); beyond that the tile scheduler searches tile_off in global
+// memory, and the CTA-pair tiles (whose table is built in shared memory) are
+// not used.
+constexpr int kTileTabInts = 448;
 constexpr int kMaxExperts = 1024;      // routed experts supported
 constexpr uint64_t kWaitTimeoutNs = 4000000000ull;  // pipeline waits give up after 4 s
 
 // Error codes recorded in the device status word (same values as moe_status_t).
 constexpr int kErrBadIds = -5;
 constexpr int kErrTimeout = -6;
+
+// Upper bound on the 128-row tiles of all groups: sum_g ceil(counts[g] / 128)
+// for N = T * K routed rows in G groups.  Every entry point that produces or
+// consumes routing tables accepts a shape only if this many tiles of rows
+// stay below 2^31 rows.
+inline int64_t max_row_tiles(int64_t T, int64_t K, int64_t G) {
+  return (T * K + G * (kTileM - 1) + kTileM - 1) / kTileM;
+}
+inline bool routed_rows_fit(int64_t T, int64_t K, int64_t G) {
+  return max_row_tiles(T, K, G) * kTileM < (int64_t(1) << 31);
+}
+
+// ---- timing probe (api.cu) --------------------------------------------------
+// When the probe is armed for `name` (moe_probe_arm), records a caller-owned
+// CUDA event on the launch stream before and after the launches in scope.
+int probe_begin(const char* name, cudaStream_t s);
+void probe_end(int token, cudaStream_t s);
+struct ProbeScope {
+  int token;
+  cudaStream_t s;
+  ProbeScope(const char* name, cudaStream_t st) : token(probe_begin(name, st)), s(st) {}
+  ~ProbeScope() { probe_end(token, s); }
+  ProbeScope(const ProbeScope&) = delete;
+  ProbeScope& operator=(const ProbeScope&) = delete;
+};
 
 // ---- routing (route.cu) ----------------------------------------------------
 constexpr int kRouteThreads = 256;                  // 8 warps per CTA
@@ -148,6 +202,7 @@ struct GemmShape {
   bool b_mn;
   bool wgrad;  // wgrad: A and B both MN-major, K = group rows
   Epi epi;
+  bool pair = false;  // rows mode on CTA pairs: 256-row tiles, each CTA staging half of B
 };
 
 cudaError_t launch_gemm(const GemmShape& shape, const GemmParams& p, int num_sms,

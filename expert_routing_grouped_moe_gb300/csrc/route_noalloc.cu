@@ -64,7 +64,8 @@ int moe_route_noalloc(const int32_t* ids, int32_t T, int32_t k, int32_t E, int32
     return set_msg(MOE_ERR_UNSUPPORTED, "moe_route_noalloc: E > 1024 or k > 32");
   const int64_t K = k + shared_expert, G = E + shared_expert;
   const int64_t N = static_cast<int64_t>(T) * K;
-  if (N + G * (kTileM - 1) >= (int64_t(1) << 31))
+  // the same shape limit as moe_route: both accept exactly the same shapes
+  if (!routed_rows_fit(T, K, G))
     return set_msg(MOE_ERR_UNSUPPORTED, "moe_route_noalloc: too many routed rows");
   const size_t need = route_ws_bytes(N, static_cast<int>(G));
   if (need > kNoAllocHistInts * sizeof(int32_t))
@@ -78,7 +79,9 @@ int moe_route_noalloc(const int32_t* ids, int32_t T, int32_t k, int32_t E, int32
   rc = device_status_word(&status);
   if (rc != MOE_OK) return set_msg(rc, "moe_route_noalloc: status word lookup failed");
   // The histogram kernel writes every scratch entry the scan reads, so the
-  // previous call's contents need no clearing.
+  // previous call's contents need no clearing.  Traced by the timing probe
+  // under the name "route", like moe_route.
+  ProbeScope probe("route", stream);
   const cudaError_t e = launch_route(ids, T, k, E, shared_expert, counts, offsets, tile_off,
                                      sorted_src, dest_pos, scratch, status, stream);
   if (e != cudaSuccess) return set_msg(MOE_ERR_CUDA, cudaGetErrorString(e));

@@ -150,7 +150,9 @@ MOE_API int moe_route(const int32_t* ids, int32_t T, int32_t k, int32_t E, int32
  * device, with that device current); make that first call before any stream
  * capture.  All calls share the one array: calls whose work overlaps on the
  * GPU (other streams, other threads) race on it and must be serialised by the
- * caller.  The array is never cleared; no result depends on its old contents. */
+ * caller.  The array is never cleared; no result depends on its old contents.
+ * It accepts exactly the shapes moe_route accepts (plus the 2 MiB limit), and
+ * the timing probe traces it under the kernel name "route", like moe_route. */
 MOE_API int moe_route_noalloc(const int32_t* ids, int32_t T, int32_t k, int32_t E,
                               int32_t shared_expert, int32_t* counts, int32_t* offsets,
                               int32_t* tile_off, int32_t* sorted_src, int32_t* dest_pos,

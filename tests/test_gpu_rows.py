@@ -37,12 +37,31 @@ def expected_layout(ids_np, E, shared):
     """Host-side, from the oracle's routing: the source token of every
     permuted row (row p = sorted position p) and the permuted row of every
     flat index (its sorted position)."""
+    rt = oracle_route(ids_np, E, shared)
+    K = ids_np.shape[1] + int(shared)
+    return rt["sorted_src"] // K, rt["dest_pos"], ids_np.shape[0] * K
+
+
+def oracle_route(ids_np, E, shared):
     T = ids_np.shape[0]
     if shared:
         ids_np = np.concatenate([ids_np, np.full((T, 1), E, dtype=ids_np.dtype)], 1)
-    K = ids_np.shape[1]
-    rt = oracle.route(ids_np, E + int(shared))
-    return rt["sorted_src"] // K, rt["dest_pos"], T * K
+    return oracle.route(ids_np, E + int(shared))
+
+
+def assert_within_one_bf16_ulp(got, exact, abs_terms, nterms, name):
+    """A sum of fp32 terms rounded once to bf16: |got - exact| is at most one
+    bf16 ulp of the exact value, plus the fp32 rounding of the nterms
+    products and additions (2^-24 relative to the absolute terms each)."""
+    got = np.asarray(got, dtype=np.float64)
+    exact = np.asarray(exact, dtype=np.float64)
+    mag = np.maximum(np.abs(exact), 2.0 ** -126)
+    ulp = np.exp2(np.floor(np.log2(mag)) - 7)
+    bound = ulp + (2 * nterms) * 2.0 ** -24 * np.asarray(abs_terms, dtype=np.float64)
+    err = np.abs(got - exact)
+    bad = err > bound
+    assert not bad.any(), "%s: %d elements beyond one bf16 ulp (worst %.3g ulp)" % (
+        name, int(bad.sum()), float(np.max(err / ulp)))
 
 
 @pytest.mark.parametrize("T,E,k,dist,shared,d", [
@@ -56,10 +75,11 @@ def test_permute_bit_exact(T, E, k, dist, shared, d):
     Xp = torch.full((T * K, d), 7.0, dtype=torch.bfloat16, device=DEV)
     L.moe_permute(X, K, r["dest_pos"], Xp)
     torch.cuda.synchronize()
-    src_tok, _, N = expected_layout(ids.cpu().numpy(), E, shared)
+    rt = oracle_route(ids.cpu().numpy(), E, shared)
     got = Xp.view(torch.int16).cpu().numpy()
     Xb = X.view(torch.int16).cpu().numpy()
-    np.testing.assert_array_equal(got, Xb[src_tok])
+    # the oracle's permute on the bf16 bit patterns: a pure gather
+    np.testing.assert_array_equal(got, oracle.permute(Xb, rt["sorted_src"], K))
 
 
 @pytest.mark.parametrize("T,E,k,dist,shared,d,weighted", [
@@ -77,14 +97,15 @@ def test_combine(T, E, k, dist, shared, d, weighted):
     L.moe_unpermute_combine(rows, r["dest_pos"], k, shared, out, weights=w, row_scalars=scal,
                             slot_out=slot)
     torch.cuda.synchronize()
-    _, prow, _ = expected_layout(ids.cpu().numpy(), E, shared)
-    prow = prow.reshape(T, K)
+    rt = oracle_route(ids.cpu().numpy(), E, shared)
+    prow = rt["dest_pos"].reshape(T, K)
     R = to64(rows)
-    c = np.ones((T, K))
-    if weighted:
-        c[:, :k] = w.cpu().numpy()
-    exp = np.einsum("tj,tjd->td", c, R[prow])
+    wn = w.cpu().numpy() if weighted else None
+    exp = oracle.combine(R, rt["dest_pos"], K, wn)
+    abs_terms = oracle.combine(np.abs(R), rt["dest_pos"], K,
+                               None if wn is None else np.abs(wn))
     assert_close_bf16(to64(out), exp, "combine")
+    assert_within_one_bf16_ulp(to64(out), exp, abs_terms, K, "combine")
     np.testing.assert_array_equal(slot.cpu().numpy(), scal.cpu().numpy()[prow[:, :k]])
 
 
@@ -101,15 +122,30 @@ def test_permute_combine_full_size_sampled(T, E, k, dist):
     Y = torch.empty(T, d, dtype=torch.bfloat16, device=DEV)
     L.moe_unpermute_combine(Xp, r["dest_pos"], k, False, Y, weights=w)
     torch.cuda.synchronize()
-    # properties that hold at any size: the round trip gives sum_j w_j * X[t]
+    # sampled tokens: the oracle's permute and combine on the sample's own
+    # slots (rows gathered from the oracle's routing of the whole batch)
     rng = np.random.default_rng(0)
-    toks = rng.choice(T, size=64, replace=False)
+    rt = oracle.route(ids.cpu().numpy(), E)
+    toks = np.sort(rng.choice(T, size=1024, replace=False))
     Xs = to64(X[torch.from_numpy(toks).to(DEV)])
-    ws = w.cpu().numpy()[toks].astype(np.float64).sum(1, keepdims=True)
-    assert_close_bf16(to64(Y[torch.from_numpy(toks).to(DEV)]), ws * Xs, "roundtrip")
-    # and each sampled permuted row is the right token row, bit for bit
-    src_tok, _, N = expected_layout(ids.cpu().numpy(), E, False)
-    prows = rng.choice(N, size=256, replace=False)
+    # the sample's slots, in token order: their sorted positions and sources,
+    # with the sample's tokens renumbered 0..n-1
+    pos = rt["dest_pos"].reshape(T, k)[toks].reshape(-1)
+    local_src = (np.repeat(np.arange(toks.size), k) * k + np.tile(np.arange(k), toks.size))
+    rows_s = oracle.permute(Xs, local_src, k)
+    ws = w.cpu().numpy()[toks]
+    exp = oracle.combine(rows_s, np.arange(toks.size * k), k, ws)
+    abs_terms = oracle.combine(np.abs(rows_s), np.arange(toks.size * k), k, np.abs(ws))
+    got_y = to64(Y[torch.from_numpy(toks).to(DEV)])
+    assert_close_bf16(got_y, exp, "roundtrip")
+    assert_within_one_bf16_ulp(got_y, exp, abs_terms, k, "roundtrip")
+    # the sample's permuted rows and further random ones are the oracle's
+    # permute of X, bit for bit
+    prows = np.concatenate([pos, rng.choice(T * k, size=4096, replace=False)])
     got = Xp[torch.from_numpy(prows).to(DEV)].view(torch.int16).cpu().numpy()
-    ref = X.view(torch.int16)[torch.from_numpy(src_tok[prows]).to(DEV)].cpu().numpy()
+    src_rows = rt["sorted_src"][prows]
+    Xb_rows = X.view(torch.int16)[torch.from_numpy(np.unique(src_rows // k)).to(DEV)]
+    lookup = {t: i for i, t in enumerate(np.unique(src_rows // k))}
+    Xb = Xb_rows.cpu().numpy()
+    ref = oracle.permute(Xb, np.array([lookup[t] * k for t in src_rows // k]), k)
     np.testing.assert_array_equal(got, ref)

@@ -158,3 +158,25 @@ def test_product_path_has_no_oracle_or_fallback():
         if fn.endswith(".py"):
             src = open(os.path.join(pkg, fn)).read()
             assert "import oracle" not in src and "from oracle" not in src, fn
+
+
+def test_route_and_route_noalloc_accept_the_same_shapes(lib):
+    """Both routing entry points share one shape limit: a shape that
+    moe_route refuses for its row count is refused by moe_route_noalloc too,
+    before any device work (the checks fail before a pointer is used)."""
+    from expert_routing_grouped_moe_gb300 import _lib
+    P = ctypes.c_void_p
+    fake = P(1 << 20)
+    # E = 1, k = 1: the tile-rounded row count passes 2^31 while the routing
+    # histogram (one group) stays far below the no-alloc array's 2 MiB
+    T = (1 << 31) - 200
+    assert lib.moe_route_workspace_size(T, 1, 1) <= (2 << 20)
+    assert lib.moe_route(fake, T, 1, 1, 0, *([fake] * 6), 1 << 40, None) == \
+        _lib.MOE_ERR_UNSUPPORTED
+    assert lib.moe_route_noalloc(fake, T, 1, 1, 0, *([fake] * 5), None) == \
+        _lib.MOE_ERR_UNSUPPORTED
+    # just below the limit both accept the shape as far as the host checks go
+    # (moe_route then fails only on its too-small workspace)
+    T_ok = (1 << 31) - 256
+    assert lib.moe_route(fake, T_ok, 1, 1, 0, *([fake] * 6), 4, None) == \
+        _lib.MOE_ERR_WORKSPACE

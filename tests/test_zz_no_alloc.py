@@ -61,6 +61,9 @@ def _route_no_alloc(ids, E, shared):
 @pytest.mark.parametrize("first,second", [
     ((4096, 128, 8, "uniform", False), (300, 5, 3, "zipf", True)),
     ((1 << 20, 128, 8, "zipf", False), (1 << 14, 64, 4, "uniform", True)),
+    # the first call's histogram fills the 2 MiB array exactly (256 experts,
+    # 8,388,608 routed rows); the second reuses a small corner of it
+    ((1 << 20, 256, 8, "uniform", False), (1000, 16, 2, "zipf", False)),
 ])
 def test_no_alloc_route_matches_route_twice_in_a_row(first, second):
     cases = []
@@ -76,8 +79,36 @@ def test_no_alloc_route_matches_route_twice_in_a_row(first, second):
             assert torch.equal(g[key], r[key]), key
 
 
+def test_no_alloc_route_at_the_limit_is_exactly_2_mib():
+    assert L.moe_route_workspace_size(1 << 20, 8, 256) == 2 << 20
+    assert L.moe_route_workspace_size(1 << 20, 8, 257) > 2 << 20
+
+
+def test_no_alloc_route_bad_id_through_the_shared_array():
+    """An id outside [0, E) is reported through the status word and its slot
+    gets dest_pos -1, exactly as moe_route does; the next call is clean."""
+    T, k, E = 64, 2, 8
+    ids = synth.topk_ids(T, E, k, "uniform", seed=5, device=DEV)
+    bad = ids.clone()
+    bad[17, 1] = E + 3
+    assert L.moe_status() == L.MOE_OK
+    got = _route_no_alloc(bad, E, False)
+    assert L.moe_status() == L.MOE_ERR_BAD_IDS
+    ref = _route_with_ws(bad, E, False)
+    assert L.moe_status() == L.MOE_ERR_BAD_IDS
+    assert int(got["dest_pos"][17 * k + 1]) == -1
+    for key in ref:
+        assert torch.equal(got[key], ref[key]), key
+    assert int(got["counts"].sum()) == T * k - 1
+    clean = _route_no_alloc(ids, E, False)
+    assert L.moe_status() == L.MOE_OK
+    ref2 = _route_with_ws(ids, E, False)
+    for key in ref2:
+        assert torch.equal(clean[key], ref2[key]), key
+
+
 def test_no_alloc_route_rejects_too_large():
-    T, k, E = 1 << 20, 8, 1024   # its histogram would need 4 MiB
+    T, k, E = 1 << 20, 8, 1024   # its histogram would need 8 MiB
     ids = torch.zeros(1, 1, dtype=torch.int32, device=DEV)
     lib = L.load()
     dummy = ctypes.c_void_p(ids.data_ptr())
