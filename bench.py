@@ -32,13 +32,34 @@ if ROOT not in sys.path:
 METRIC = "MoE-LoRA layer fwd+bwd tokens/s and TFLOP/s vs BF16 peak; routing GB/s"
 PEAKS_FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
-# DRAM traffic per launch of the dominant kernel from one ncu capture
-# (dram__bytes_read.sum + dram__bytes_write.sum), keyed by kernel and workload;
-# None until captured for the current kernel version.
-# dram__bytes_read.sum + dram__bytes_write.sum of one launch of the dominant
-# kernel, read from one ncu --set full capture of the current kernel
-# (kernel, workload)
-NCU_TRAFFIC_BYTES = {("gate_up", "qwen3_30b_a3b"): 1030659840 + 273544960}
+# dram__bytes_read.sum + dram__bytes_write.sum of one launch, from one ncu
+# capture, keyed by (kernel, workload) and stamped with the digest of the GEMM
+# sources the capture ran (kernel_sources_digest); a figure whose stamp no
+# longer matches the sources is stale and reported as null.
+NCU_TRAFFIC = {}
+GEMM_SOURCES = ("csrc/gemm.cu", "csrc/ptx.cuh", "csrc/internal.h", "csrc/api.cu")
+
+
+def kernel_sources_digest():
+    """Short digest of the sources that define the GEMM kernels and their
+    launches (a captured traffic figure holds for these sources only)."""
+    import hashlib
+    h = hashlib.sha256()
+    for rel in GEMM_SOURCES:
+        with open(os.path.join(ROOT, "expert_routing_grouped_moe_gb300", rel), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:12]
+
+
+def ncu_traffic(kernel, config):
+    """(bytes, note): the captured DRAM traffic of one launch, or None with the
+    reason when there is no capture of the current kernel sources."""
+    rec = NCU_TRAFFIC.get((kernel, config))
+    if rec is None:
+        return None, "no ncu capture of this kernel and workload"
+    if rec["sources"] != kernel_sources_digest():
+        return None, "stale: the kernel sources changed since the capture (%s)" % rec["sources"]
+    return rec["bytes"], "ncu capture of sources %s" % rec["sources"]
 
 
 def workload(synth, args):
@@ -66,6 +87,9 @@ def parse_args(argv=None):
                     help="also compute the full weight gradients dW_gu, dW_dn each step")
     ap.add_argument("--route-only", action="store_true",
                     help="time only moe_route on the routing sweep points")
+    ap.add_argument("--sweep", action="store_true",
+                    help="time route, permute and combine at every routing-workload point "
+                         "(with --route-only: routing alone)")
     return ap.parse_args(argv)
 
 
@@ -73,46 +97,65 @@ def parse_args(argv=None):
 
 def layer_counts(cfg, full_grads=False):
     """Algorithmic work of one fwd+bwd step (split-LoRA counts; the dense
-    merged work is not counted) and, per kernel launch, its FLOPs and the
-    bytes it must move at least: each input read once, each output written
-    once, in the stored precisions (bf16 rows, hi/lo bf16 pairs, fp32 h).
-    full_grads adds the full weight gradients dW_gu and dW_dn."""
+    merged work is not counted) and, per kernel launch, its FLOPs and two
+    byte counts, each input read once and each output written once:
+
+    * method bytes: every saved intermediate as the single bf16 tensor the
+      method's step table sizes (h [N,2f], act [N,f], xa_gu / xa_dn / u / v
+      [N,r], dh [N,2f]), weights and rows in bf16, LoRA gradients in fp32;
+    * stored bytes: what this build stores -- fp32 h and hi/lo bf16 pairs for
+      the intermediates that feed a row reduction, routing-weight-gradient
+      partials.
+
+    The roofline is reported on the method bytes; the stored bytes show what
+    the precision plan costs.  full_grads adds the full weight gradients."""
     T, d, f, r, k = cfg.T, cfg.d, cfg.f, cfg.r, cfg.k
     N = cfg.rows                                   # routed rows (+ shared rows)
     G = cfg.groups
     hs = 32 * ((f + 15) // 16)                     # fp32 h row: [gate 16 | up 16] chunks
-    nparts = 2 * ((f + 191) // 192)                # dw partial slices (192-feature tiles)
+    nparts = 2 * ((f + 191) // 192)                # dw partial slices (at most)
     F_base = 2 * N * d * 2 * f + 2 * N * f * d     # gate_up + down
     F_lora = 2 * N * (d * r + r * 2 * f + f * r + r * d)
     W_gu, W_dn = 2 * G * 2 * f * d, 2 * G * d * f
     A_gu, B_gu, A_dn, B_dn = 2 * G * r * d, 2 * G * 2 * f * r, 2 * G * r * f, 2 * G * d * r
-    rows_d, pair_r, pair_f = 2 * N * d, 4 * N * r, 4 * N * f
-    kern = {  # per launch: (flops, bytes)
-        "xa_gu": (2 * N * d * r, rows_d + A_gu + pair_r),
+    rows_d = 2 * N * d
+    # method sizes (bf16) and stored sizes of the intermediates
+    m_r, m_f, m_2f = 2 * N * r, 2 * N * f, 2 * N * 2 * f
+    p_r, p_f, p_2f = 4 * N * r, 4 * N * f, 4 * N * 2 * f      # hi/lo pairs
+    h32 = 4 * N * hs
+    kern = {  # per launch: (flops, method bytes, stored bytes)
+        "xa_gu": (2 * N * d * r, rows_d + A_gu + m_r, rows_d + A_gu + p_r),
         "gate_up": (2 * N * d * 2 * f + 2 * N * r * 2 * f,
-                    rows_d + W_gu + pair_r + B_gu + 4 * N * hs + pair_f),
-        "xa_dn": (2 * N * f * r, pair_f + A_dn + pair_r),
+                    rows_d + W_gu + m_r + B_gu + m_2f + m_f,
+                    rows_d + W_gu + p_r + B_gu + h32 + p_f),
+        "xa_dn": (2 * N * f * r, m_f + A_dn + m_r, p_f + A_dn + p_r),
         # down reads the high halves of act' and xa_dn (both carry w)
-        "down": (2 * N * f * d + 2 * N * r * d, 2 * N * f + W_dn + 2 * N * r + B_dn + rows_d),
-        "u": (2 * N * d * r, rows_d + B_dn + pair_r),
+        "down": (2 * N * f * d + 2 * N * r * d, m_f + W_dn + m_r + B_dn + rows_d,
+                 2 * N * f + W_dn + 2 * N * r + B_dn + rows_d),
+        "u": (2 * N * d * r, rows_d + B_dn + m_r, rows_d + B_dn + p_r),
         "dgrad_dn": (2 * N * d * f + 2 * N * r * f,
-                     rows_d + W_dn + pair_r + A_dn + 4 * N * hs + 4 * N + 2 * pair_f
-                     + 4 * N * nparts),
-        "v": (2 * N * 2 * f * r, 2 * pair_f + B_gu + pair_r),
-        "dgrad_gu": (2 * N * 2 * f * d + 2 * N * r * d, pair_f + W_gu + 2 * N * r + A_gu + rows_d),
-        "dB_dn": (2 * N * d * r, rows_d + pair_r + 4 * G * d * r),
-        "dA_dn": (2 * N * f * r, pair_f + pair_r + 4 * G * r * f),
-        "dB_gu": (2 * N * 2 * f * r, 2 * pair_f + pair_r + 4 * G * 2 * f * r),
-        "dA_gu": (2 * N * d * r, rows_d + pair_r + 4 * G * r * d),
-        "route": (0, 4 * T * k + 8 * N + 12 * G),
-        "permute": (0, 2 * T * d + 2 * N * d + 4 * N),
-        "combine": (0, 2 * N * d + 2 * T * d + 8 * N + 4 * T * k),
-        "dw_reduce": (0, 4 * N * nparts + 4 * N),
+                     rows_d + W_dn + m_r + A_dn + m_2f + 8 * N + m_2f + 4 * N,
+                     rows_d + W_dn + p_r + A_dn + h32 + 8 * N + 2 * p_f + 4 * N * nparts),
+        "v": (2 * N * 2 * f * r, m_2f + B_gu + m_r, p_2f + B_gu + p_r),
+        "dgrad_gu": (2 * N * 2 * f * d + 2 * N * r * d, m_2f + W_gu + m_r + A_gu + rows_d,
+                     2 * N * 2 * f + W_gu + 2 * N * r + A_gu + rows_d),
+        "dB_dn": (2 * N * d * r, rows_d + m_r + 4 * G * d * r, rows_d + p_r + 4 * G * d * r),
+        "dA_dn": (2 * N * f * r, m_f + m_r + 4 * G * r * f, p_f + p_r + 4 * G * r * f),
+        "dB_gu": (2 * N * 2 * f * r, m_2f + m_r + 4 * G * 2 * f * r,
+                  p_2f + p_r + 4 * G * 2 * f * r),
+        "dA_gu": (2 * N * d * r, rows_d + m_r + 4 * G * r * d, rows_d + p_r + 4 * G * r * d),
+        "route": (0, 4 * T * k + 8 * N + 12 * G, 4 * T * k + 8 * N + 12 * G),
+        "permute": (0, 2 * T * d + 2 * N * d + 4 * N, 2 * T * d + 2 * N * d + 4 * N),
+        "combine": (0, 2 * N * d + 2 * T * d + 8 * N + 4 * T * k,
+                    2 * N * d + 2 * T * d + 8 * N + 4 * T * k),
+        "dw_reduce": (0, 4 * N * nparts + 4 * N, 4 * N * nparts + 4 * N),
     }
     F_full = 0
     if full_grads:
-        kern["dW_gu"] = (2 * N * 2 * f * d, 2 * pair_f + rows_d + 4 * G * 2 * f * d)
-        kern["dW_dn"] = (2 * N * d * f, pair_f + rows_d + 4 * G * d * f)
+        kern["dW_gu"] = (2 * N * 2 * f * d, m_2f + rows_d + 4 * G * 2 * f * d,
+                         p_2f + rows_d + 4 * G * 2 * f * d)
+        kern["dW_dn"] = (2 * N * d * f, m_f + rows_d + 4 * G * d * f,
+                         p_f + rows_d + 4 * G * d * f)
         F_full = 2 * N * 2 * f * d + 2 * N * d * f
     return {"flops": 2 * F_base + 3 * F_lora + F_full, "F_base": F_base, "F_lora": F_lora,
             "F_full": F_full, "kernels": kern, "launches": {"permute": 2, "combine": 2}}
@@ -155,10 +198,12 @@ def read_stream_gbs(torch, L, dev, reps=5):
     return out
 
 
-def kernel_roofline(name, flops, nbytes, dur_s, peaks):
-    """Roofline of one launch: bound = whichever of the tensor time
-    (flops / sustained bf16 peak) and the HBM time (bytes / copy peak) is
-    longer; achieved is the work of that kind per second."""
+def kernel_roofline(name, flops, nbytes, dur_s, peaks, stored_bytes=None):
+    """Roofline of one launch on the method's bytes: bound = whichever of the
+    tensor time (flops / sustained bf16 peak) and the HBM time (bytes / copy
+    peak) is longer; achieved is the work of that kind per second.  The
+    stored-precision bytes give the fraction this build's own traffic runs
+    at, as context."""
     t_tensor = flops / (peaks["bf16_tflops_sustained"] * 1e12)
     t_hbm = nbytes / (peaks["hbm_gbs"] * 1e9)
     if t_tensor >= t_hbm:
@@ -166,10 +211,15 @@ def kernel_roofline(name, flops, nbytes, dur_s, peaks):
             "TFLOP/s", "tensor"
     else:
         ach, peak, unit, bound = nbytes / dur_s / 1e9, peaks["hbm_gbs"], "GB/s", "hbm"
-    return {"kernel": name, "bound": bound, "achieved": ach, "peak": peak, "unit": unit,
-            "frac": ach / peak, "flops_per_launch": flops, "bytes_per_launch": nbytes,
-            "tensor_frac": flops / dur_s / 1e12 / peaks["bf16_tflops_sustained"],
-            "hbm_frac": nbytes / dur_s / 1e9 / peaks["hbm_gbs"]}
+    out = {"kernel": name, "bound": bound, "achieved": ach, "peak": peak, "unit": unit,
+           "frac": ach / peak, "flops_per_launch": flops, "bytes_per_launch": nbytes,
+           "bytes_basis": "method (bf16 intermediates)",
+           "tensor_frac": flops / dur_s / 1e12 / peaks["bf16_tflops_sustained"],
+           "hbm_frac": nbytes / dur_s / 1e9 / peaks["hbm_gbs"]}
+    if stored_bytes is not None:
+        out["stored_bytes_per_launch"] = stored_bytes
+        out["stored_hbm_frac"] = stored_bytes / dur_s / 1e9 / peaks["hbm_gbs"]
+    return out
 
 
 def load_peaks():
@@ -408,17 +458,22 @@ def run_e2e(torch, layer, X, dY, ids, topw, cfg, steps, main):
     return e0.elapsed_time(e1) / steps
 
 
-def routing_sweep(torch, L, synth, dev, peaks, points=((1 << 20, 128, 8), (1 << 18, 64, 4)),
-                  d=2048, reps=5, route_only=False):
-    """Route, permute and combine throughput (algorithmic GB/s) on the routing
-    workload's large points: T tokens, E experts, top-k, bf16 rows of d.
-    Each call is timed on its own with CUDA events, after a write of 256 MB
-    (twice L2) that evicts its inputs from L2.  route_only: routing alone,
-    with only the id and routing-table buffers allocated."""
+DEFAULT_SWEEP_POINTS = ((1 << 20, 128, 8, "uniform"), (1 << 20, 128, 8, "zipf"),
+                        (1 << 18, 64, 4, "uniform"))
+
+
+def routing_sweep(torch, L, synth, dev, peaks, points=DEFAULT_SWEEP_POINTS, d=2048, reps=5,
+                  route_only=False):
+    """Route, permute and combine throughput (algorithmic GB/s) on points of
+    the routing workload: T tokens, E experts, top-k ids (uniform or Zipf),
+    bf16 rows of d.  Each call is timed on its own with CUDA events, after a
+    write of 256 MB (twice L2) that evicts its inputs from L2; `pipeline` is
+    the three calls' bytes over their summed times.  route_only: routing
+    alone, with only the id and routing-table buffers allocated."""
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
     out = []
-    for T, E, k in points:
-        ids = synth.topk_ids(T, E, k, "uniform", seed=7, device=dev)
+    for T, E, k, dist in points:
+        ids = synth.topk_ids(T, E, k, dist, seed=7, device=dev)
         N = T * k
         counts = torch.empty(E, dtype=torch.int32, device=dev)
         offsets = torch.empty(E + 1, dtype=torch.int32, device=dev)
@@ -439,7 +494,8 @@ def routing_sweep(torch, L, synth, dev, peaks, points=((1 << 20, 128, 8), (1 << 
                                 2 * T * d + 2 * N * d + 4 * N)
             calls["combine"] = (lambda: L.moe_unpermute_combine(Xp, dst, k, False, Y, weights=w),
                                 2 * N * d + 2 * T * d + 8 * N + 4 * T * k)
-        res = {"T": T, "E": E, "k": k, "d": d}
+        res = {"T": T, "E": E, "k": k, "dist": dist, "d": d}
+        tot_ms, tot_b = 0.0, 0
         for name, (fn, nbytes) in calls.items():
             fn()
             torch.cuda.synchronize()
@@ -456,6 +512,11 @@ def routing_sweep(torch, L, synth, dev, peaks, points=((1 << 20, 128, 8), (1 << 
             ms = total / reps
             gbs = nbytes / (ms / 1e3) / 1e9
             res[name] = {"ms": ms, "gbs": gbs, "frac_of_hbm": gbs / peaks["hbm_gbs"]}
+            tot_ms += ms
+            tot_b += nbytes
+        if not route_only:
+            gbs = tot_b / (tot_ms / 1e3) / 1e9
+            res["pipeline"] = {"ms": tot_ms, "gbs": gbs, "frac_of_hbm": gbs / peaks["hbm_gbs"]}
         out.append(res)
         calls.clear()
         X = Xp = Y = w = None  # noqa: F841  (free this point's rows before the next)
@@ -463,6 +524,26 @@ def routing_sweep(torch, L, synth, dev, peaks, points=((1 << 20, 128, 8), (1 << 
     if L.moe_status() != L.MOE_OK:
         raise SystemExit("device status error in the routing sweep")
     return out
+
+
+def run_sweep(args):
+    """Every point of the routing workload (T in 1K..1M, E in 8..128, top-2/4/8,
+    uniform and Zipf ids): route, permute and combine GB/s, one JSON line."""
+    import torch
+    from expert_routing_grouped_moe_gb300 import _lib as L, build, synth
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    build.build()
+    L.load()
+    peaks, src = load_peaks()
+    res = routing_sweep(torch, L, synth, dev, peaks, points=synth.ROUTE_SWEEP,
+                        reps=max(1, min(args.steps, 5)), route_only=args.route_only)
+    return {"metric": "routing GB/s (route%s), every routing-workload point" % (
+                "" if args.route_only else ", permute, combine"),
+            "unit": "GB/s", "peak": {"hbm_gbs": peaks["hbm_gbs"], "source": src},
+            "timing": "CUDA events per call, L2 evicted by a 256 MB write before each, mean of "
+                      "%d calls" % max(1, min(args.steps, 5)),
+            "routing_sweep": res}
 
 
 def run_route_only(args):
@@ -475,11 +556,24 @@ def run_route_only(args):
     build.build()
     L.load()
     res = routing_sweep(torch, L, synth, dev, peaks=load_peaks()[0], reps=args.steps,
+                        points=((1 << 20, 128, 8, "uniform"), (1 << 18, 64, 4, "uniform")),
                         route_only=True)
     return {"metric": "routing GB/s (route only)", "unit": "GB/s", "routing_sweep": res}
 
 
 # ---------------------------------------------------------------- our arm
+
+def config_dict(cfg, args, world):
+    """The workload as both arms report it (the same keys and values)."""
+    return {"workload": "%s-shaped MoE-LoRA layer fwd+bwd%s%s" % (
+                cfg.name, " with full weight gradients" if args.full_grads else "",
+                " at T=%d" % cfg.T if args.tokens > 0 else ""),
+            "T": cfg.T, "d": cfg.d, "f": cfg.f, "E": cfg.E, "k": cfg.k, "r": cfg.r,
+            "alpha": cfg.alpha, "shared_expert": cfg.shared,
+            "global_batch_tokens": world * cfg.T, "parallelism": "replicas x%d" % world,
+            "l2": "inputs larger than L2 (%.2f GB of expert weights read per pass)" % (
+                2 * (cfg.groups * (2 * cfg.f * cfg.d + cfg.d * cfg.f)) / 1e9)}
+
 
 def run_ours(args):
     import torch
@@ -588,10 +682,14 @@ def run_ours(args):
     dom = max(main, key=lambda n: kstats[n]["share"]) if main else None
     roof = None
     if dom is not None:
-        fl, nb = counts["kernels"][dom]
-        roof = kernel_roofline(dom, fl, nb, kstats[dom]["ms_per_launch"] / 1e3, peaks)
-        # the ncu figure holds for the workload's own T only
-        roof["traffic"] = NCU_TRAFFIC_BYTES.get((dom, args.config)) if args.tokens <= 0 else None
+        fl, nb, sb = counts["kernels"][dom]
+        roof = kernel_roofline(dom, fl, nb, kstats[dom]["ms_per_launch"] / 1e3, peaks,
+                               stored_bytes=sb)
+        # the ncu figure holds for the workload's own T and the captured sources only
+        if args.tokens <= 0:
+            roof["traffic"], roof["traffic_source"] = ncu_traffic(dom, args.config)
+        else:
+            roof["traffic"], roof["traffic_source"] = None, "no capture at this T"
         roof["peak_source"] = "%s (%s)" % (peak_src, "bf16 sustained" if roof["bound"] == "tensor"
                                            else "HBM copy")
         if roof["bound"] == "hbm" and read_gbs:
@@ -604,15 +702,17 @@ def run_ours(args):
                                    "128 B, each SM on its own rows (a GEMM operand's pattern)"}
     route = None
     if "route" in kstats:
-        rb = counts["kernels"]["route"][1]
+        rb = counts["kernels"]["route"][1]  # method bytes (= stored: integer tables)
         gbs = rb / (kstats["route"]["ms_per_launch"] / 1e3) / 1e9
         route = {"gbs": gbs, "frac_of_hbm": gbs / peaks["hbm_gbs"], "bytes_per_launch": rb}
     kernels = {}
     for n, v in sorted(kstats.items(), key=lambda kv: -kv[1]["share"]):
-        rf = kernel_roofline(n, *counts["kernels"][n], v["ms_per_launch"] / 1e3, peaks)
+        fl, nb, sb = counts["kernels"][n]
+        rf = kernel_roofline(n, fl, nb, v["ms_per_launch"] / 1e3, peaks, stored_bytes=sb)
         kernels[n] = {"ms": round(v["ms_per_launch"], 5), "share": round(v["share"], 4),
                       "stream": "aux" if n in AUX_STREAM_KERNELS else "main",
-                      "bound": rf["bound"], "frac": round(rf["frac"], 3)}
+                      "bound": rf["bound"], "frac": round(rf["frac"], 3),
+                      "stored_hbm_frac": round(rf["stored_hbm_frac"], 3)}
     gemm_ms = sum(v["ms_per_launch"] * v["launches_per_step"] for n, v in kstats.items()
                   if counts["kernels"][n][0] > 0 and n not in AUX_STREAM_KERNELS)
 
@@ -629,15 +729,7 @@ def run_ours(args):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_max,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic (seeded; random-init weights of the layer shape)",
-        "config": {"workload": "%s-shaped MoE-LoRA layer fwd+bwd%s%s" % (
-                       cfg.name, " with full weight gradients" if args.full_grads else "",
-                       " at T=%d" % cfg.T if args.tokens > 0 else ""),
-                   "T": cfg.T,
-                   "d": cfg.d, "f": cfg.f, "E": cfg.E, "k": cfg.k, "r": cfg.r,
-                   "alpha": cfg.alpha, "shared_expert": cfg.shared,
-                   "global_batch_tokens": world * cfg.T, "parallelism": "replicas x%d" % world,
-                   "l2": "inputs larger than L2 (%.2f GB of expert weights read per pass)" % (
-                       2 * (cfg.groups * (2 * cfg.f * cfg.d + cfg.d * cfg.f)) / 1e9)},
+        "config": config_dict(cfg, args, world),
         "tflops": tflops,
         "tflops_frac": tflops / (world * peaks["bf16_tflops_sustained"]),
         "tflops_frac_of": "%s bf16 sustained %.1f TFLOP/s per GPU" % (
@@ -696,11 +788,7 @@ def run_reference(args):
         "n_gpus": int(os.environ.get("WORLD_SIZE", "1")), "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": "%s-shaped MoE-LoRA layer fwd+bwd%s%s" % (
-                       cfg.name, " with full weight gradients" if args.full_grads else "",
-                       " at T=%d" % cfg.T if args.tokens > 0 else ""),
-                   "T": cfg.T,
-                   "d": cfg.d, "f": cfg.f, "E": cfg.E, "k": cfg.k, "r": cfg.r},
+        "config": config_dict(cfg, args, int(os.environ.get("WORLD_SIZE", "1"))),
         "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cpu_cores(),
                          "kind": "oracle", "sample": sample},
         "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
@@ -710,7 +798,9 @@ def run_reference(args):
 
 def main(argv=None):
     args = parse_args(argv)
-    if args.route_only:
+    if args.sweep:
+        out = run_sweep(args)
+    elif args.route_only:
         out = run_route_only(args)
     else:
         out = run_reference(args) if args.impl == "reference" else run_ours(args)

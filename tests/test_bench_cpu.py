@@ -24,11 +24,20 @@ def test_layer_counts_qwen3_shape():
     F_lora = 2 * N * (2048 * 64 + 64 * 1536 + 768 * 64 + 64 * 2048)
     assert c["flops"] == 2 * F_base + 3 * F_lora
     assert abs(c["flops"] / 1e9 - 699.1) < 1.0   # ~699 GFLOP per fwd+bwd step
-    fl, nb = c["kernels"]["gate_up"]
+    fl, nb, sb = c["kernels"]["gate_up"]
     assert fl == 2 * N * 2048 * 1536 + 2 * N * 64 * 1536
-    # W_gu (128 experts x 1536 x 2048 bf16) alone is 805 MB of the gate_up bytes
-    assert nb > 128 * 1536 * 2048 * 2
+    # method bytes: W_gu 805.3 + Xp 134.2 + B_gu 25.2 + xa 4.2 + h (bf16) 100.7
+    # + act (bf16) 50.3 = 1119.9 MB, each read or written once
+    W_gu = 128 * 1536 * 2048 * 2
+    assert nb == W_gu + 2 * N * 2048 + 128 * 1536 * 64 * 2 + 2 * N * 64 + 2 * N * 1536 \
+        + 2 * N * 768
+    assert abs(nb / 1e6 - 1119.9) < 0.1
+    # stored bytes: fp32 h and the hi/lo pairs of xa and act
+    assert sb == W_gu + 2 * N * 2048 + 128 * 1536 * 64 * 2 + 4 * N * 64 + 4 * N * 1536 \
+        + 4 * N * 768
     assert c["kernels"]["route"][0] == 0 and c["kernels"]["route"][1] > 0
+    for name, (_, m, st) in c["kernels"].items():
+        assert 0 < m <= st, name
 
 
 def test_kernel_roofline_picks_the_longer_bound():
@@ -68,6 +77,27 @@ def test_reference_arm_json_line():
     assert line["impl"] == "reference" and line["unit"] == "tokens/s" and line["value"] > 0
     assert line["e2e"]["h2d_bytes_per_step"] == 0
     assert line["cpu_baseline"]["kind"] == "oracle"
+    # the same config dict as our arm's (so the two lines describe one workload)
+    args = bench.parse_args(["--config", "tiny"])
+    assert line["config"] == bench.config_dict(synth.CONFIGS["tiny"], args, 1)
+
+
+def test_ncu_traffic_is_tied_to_the_kernel_sources(monkeypatch):
+    digest = bench.kernel_sources_digest()
+    assert len(digest) == 12
+    monkeypatch.setitem(bench.NCU_TRAFFIC, ("k", "w"), {"bytes": 123, "sources": digest})
+    assert bench.ncu_traffic("k", "w")[0] == 123
+    monkeypatch.setitem(bench.NCU_TRAFFIC, ("k", "w"), {"bytes": 123, "sources": "0" * 12})
+    val, note = bench.ncu_traffic("k", "w")
+    assert val is None and "stale" in note
+    assert bench.ncu_traffic("nope", "w")[0] is None
+
+
+def test_sweep_points_cover_the_routing_workload():
+    pts = synth.ROUTE_SWEEP
+    assert len(pts) == 4 * 4 * 3 * 2
+    assert {p[3] for p in pts} == {"uniform", "zipf"}
+    assert {(p[0], p[1], p[2], p[3]) for p in bench.DEFAULT_SWEEP_POINTS} <= set(pts)
 
 
 def test_clock_sampler_parses_lines():
