@@ -33,7 +33,7 @@ EXPORTED = (
     "moe_mlp_bwd_workspace_size", "moe_lora_grouped_mlp_bwd", "moe_status",
     "moe_last_error", "moe_abi_version", "moe_kernel_name", "moe_probe_arm", "moe_probe_count",
     "moe_route_noalloc", "moe_selftest_wait_timeout", "moe_probe_read_stream",
-    "moe_route_kernel_count",
+    "moe_route_kernel_count", "moe_ep_row_weights", "moe_ep_segment_ids",
 )
 
 
@@ -97,6 +97,8 @@ def load(path: str = LIB_PATH):
             "moe_route_noalloc": (ctypes.c_int, [_P, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P]),
             "moe_probe_read_stream": (ctypes.c_int, [_P, _SZ, _I, _P]),
             "moe_route_kernel_count": (_I, [_I, _I, _I]),
+            "moe_ep_row_weights": (ctypes.c_int, [_P, _P, _I, _I, _I, _P, _P]),
+            "moe_ep_segment_ids": (ctypes.c_int, [_P, _I, _I, ctypes.c_int64, _P, _P]),
         }
         for name, (res, args) in sig.items():
             fn = getattr(lib, name)
@@ -244,6 +246,22 @@ def moe_lora_grouped_mlp_bwd(dims: MoeDims, dYp, dY, Xp, X, counts, offsets, til
         _f32(dW_gu, "dW_gu"), _f32(dW_dn, "dW_dn"),
         _ptr(ws, name="ws"), ws.numel() * ws.element_size(), _stream(stream)),
         "moe_lora_grouped_mlp_bwd")
+
+
+def moe_ep_row_weights(topk_w, dest_pos, shared_expert, row_w, stream=None):
+    """row_w[dest_pos[t*K + j]] = topk_w[t, j] (1 for the shared slot)."""
+    T, k = topk_w.shape
+    _check(load().moe_ep_row_weights(_f32(topk_w, "topk_w"), _i32(dest_pos, "dest_pos"), T, k,
+                                     1 if shared_expert else 0, _f32(row_w, "row_w"),
+                                     _stream(stream)), "moe_ep_row_weights")
+
+
+def moe_ep_segment_ids(counts, ids, stream=None):
+    """ids[i] = local expert of received row i, for counts [P, E_loc]."""
+    P, E_loc = counts.shape
+    _check(load().moe_ep_segment_ids(_i32(counts, "counts"), P, E_loc, ids.numel(),
+                                     _i32(ids, "ids") if ids.numel() else None, _stream(stream)),
+           "moe_ep_segment_ids")
 
 
 def moe_status(stream=None) -> int:

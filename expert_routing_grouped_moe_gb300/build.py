@@ -17,7 +17,7 @@ ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(BUILD, "libmoe_gb300.so")
-SOURCES = ["api.cu", "route.cu", "rows.cu", "gemm.cu", "route_noalloc.cu", "probe.cu"]
+SOURCES = ["api.cu", "route.cu", "rows.cu", "gemm.cu", "route_noalloc.cu", "probe.cu", "ep.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC,-fvisibility=hidden",
          "--expt-relaxed-constexpr", "-I" + os.path.join(ROOT, "include")]

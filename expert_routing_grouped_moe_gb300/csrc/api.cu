@@ -80,7 +80,7 @@ int device_state(DevState** out) {
 const char* const kKernelNames[] = {
     "route", "permute", "combine", "router_topk", "xa_gu", "gate_up", "xa_dn", "down",
     "u", "dgrad_dn", "v", "dgrad_gu", "dB_dn", "dA_dn", "dB_gu", "dA_gu", "dw_reduce",
-    "dW_dn", "dW_gu"};
+    "dW_dn", "dW_gu", "ep_row_weights", "ep_segment_ids"};
 constexpr int kNumKernels = sizeof(kKernelNames) / sizeof(kKernelNames[0]);
 
 struct Probe {

@@ -118,6 +118,10 @@ cudaError_t launch_route(const int32_t* ids, int T, int k, int E, int shared, in
 // else 3 (histogram, scan, scatter).
 int route_kernel_count(int64_t n, int G);
 
+// ---- expert-parallel helpers (ep.cu) -------------------------------------------
+// Blocks (rank, local expert) of a received-row count matrix: P * E_loc.
+constexpr int64_t kMaxEpBlocks = 16384;
+
 // ---- row gather / combine (rows.cu) ------------------------------------------
 // Permuted rows are in sorted order: row p holds sorted position p, N = T * K rows.
 cudaError_t launch_permute(const uint16_t* src, int T, int d, int K, const int32_t* dest_pos,

@@ -281,6 +281,40 @@ MOE_API int moe_lora_grouped_mlp_bwd(const moe_dims* dims, const moe_bf16* dYp,
                              void* ws, size_t ws_bytes, moe_stream_t stream);
 
 /* ------------------------------------------------------------------------ */
+/* Expert parallelism                                                        */
+/* ------------------------------------------------------------------------ */
+/* With the experts split into contiguous ranges over P ranks (the Unsloth x
+ * NVIDIA article's closing section points multi-GPU training at data and
+ * expert sharding), a rank's permuted rows for the experts of rank q are the
+ * contiguous slice [offsets[e_q], offsets[e_{q+1}]) of its sorted order, so
+ * one all-to-all per direction moves them (the collective itself is the
+ * caller's: NCCL through torch.distributed in the Python layer).  Received
+ * rows arrive rank-major, expert-minor; moe_route on their local expert ids
+ * (moe_ep_segment_ids) regroups them by expert, moe_permute with K = 1 moves
+ * them, and moe_unpermute_combine with K = 1 moves results back.  These two
+ * calls are the only kernels expert parallelism adds. */
+
+/* Blocks (rank, local expert) a received-row count matrix may have. */
+#define MOE_EP_MAX_BLOCKS 16384
+
+/* Routing weight of every sorted position, so it can travel with its row:
+ *   row_w[dest_pos[t*K + j]] = topk_w[t, j]  (j < k),  1 for the shared slot
+ * (K = k + shared_expert).  topk_w [T,k] fp32, dest_pos [T*K] from moe_route
+ * (entries < 0, bad ids, are skipped), row_w [T*K] fp32. */
+MOE_API int moe_ep_row_weights(const float* topk_w, const int32_t* dest_pos, int32_t T,
+                               int32_t k, int32_t shared_expert, float* row_w,
+                               moe_stream_t stream);
+
+/* Local expert id of every received row.  counts [P, E_loc] int32 (device):
+ * counts[r, e] rows from rank r for local expert e, received rank-major then
+ * expert-minor; ids [n_rows] int32 gets e for each of them.  n_rows must equal
+ * the sum of counts: otherwise nothing is written and MOE_ERR_BAD_IDS is
+ * recorded in the status word.  P * E_loc <= MOE_EP_MAX_BLOCKS.  n_rows = 0 is
+ * a no-op. */
+MOE_API int moe_ep_segment_ids(const int32_t* counts, int32_t P, int32_t E_loc, int64_t n_rows,
+                               int32_t* ids, moe_stream_t stream);
+
+/* ------------------------------------------------------------------------ */
 /* Status                                                                    */
 /* ------------------------------------------------------------------------ */
 
