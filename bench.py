@@ -89,6 +89,9 @@ def parse_args(argv=None):
                     help="also compute the full weight gradients dW_gu, dW_dn each step")
     ap.add_argument("--route-only", action="store_true",
                     help="time only moe_route on the routing sweep points")
+    ap.add_argument("--rank-r-tokens", action="store_true",
+                    help="the LoRA-A products read the token rows (X, dY) instead of the "
+                         "permuted copies")
     ap.add_argument("--sweep", action="store_true",
                     help="time route, permute and combine at every routing-workload point "
                          "(with --route-only: routing alone)")
@@ -597,7 +600,8 @@ def run_ours(args):
     topw = torch.empty(cfg.T, cfg.k, dtype=torch.float32, device=dev)
     L.moe_router_topk(act["logits"], cfg.k, ids, topw)
     layer = MoELoRALayer(cfg.T, cfg.d, cfg.f, cfg.E, cfg.k, cfg.r, cfg.alpha, weights,
-                         shared_expert=cfg.shared, device=dev, full_grads=args.full_grads)
+                         shared_expert=cfg.shared, device=dev, full_grads=args.full_grads,
+                         rank_r_tokens=args.rank_r_tokens)
     X, dY = act["X"], act["dY"]
     stream = torch.cuda.current_stream()
 

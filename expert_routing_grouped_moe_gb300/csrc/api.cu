@@ -563,8 +563,8 @@ int moe_lora_grouped_mlp_fwd(const moe_dims* dims, const moe_bf16* Xp, const moe
   (void)counts;
   int rc = check_dims(dims);
   if (rc) return rc;
-  if ((Xp == nullptr) == (X == nullptr))
-    return fail(MOE_ERR_INVALID_ARG, "pass exactly one of Xp (permuted rows) and X (token rows)");
+  if (Xp == nullptr && X == nullptr)
+    return fail(MOE_ERR_INVALID_ARG, "pass Xp (permuted rows), X (token rows) or both");
   if (Xp) MOE_CHECK_PTR(Xp);
   if (X) MOE_CHECK_PTR(X);
   MOE_CHECK_PTR(W_gu); MOE_CHECK_PTR(A_gu); MOE_CHECK_PTR(B_gu);
@@ -587,7 +587,8 @@ int moe_lora_grouped_mlp_fwd(const moe_dims* dims, const moe_bf16* Xp, const moe
   const int64_t Nf = N * f, Nr = N * r;
   {  // xa_gu pair = s * Xp A_gu^T
     GemmParams p = base;
-    SLICE_ROWS(p, 0, Xp, X, d, MAP3(p.sl[0].b, A_gu, G, r, d, 64, 64), d);
+    // token rows gathered from X when given (L2-resident), else the permuted rows
+    SLICE_ROWS(p, 0, X ? nullptr : Xp, X, d, MAP3(p.sl[0].b, A_gu, G, r, d, 64, 64), d);
     p.nslices = 1; p.N = r; p.n_ntiles = (r + 63) / 64; p.out0 = xa_gu; p.ld0 = r; p.pair = Nr;
     if ((rc = run_gemm({128, false, false, Epi::kLoRAGrid}, p, RG, st->num_sms, s, "xa_gu")))
       return rc;
@@ -656,10 +657,10 @@ int moe_lora_grouped_mlp_bwd(const moe_dims* dims, const moe_bf16* dYp, const mo
   (void)counts;
   int rc = check_dims(dims);
   if (rc) return rc;
-  if ((dYp == nullptr) == (dY == nullptr))
-    return fail(MOE_ERR_INVALID_ARG, "pass exactly one of dYp (permuted rows) and dY (token rows)");
-  if ((Xp == nullptr) == (X == nullptr))
-    return fail(MOE_ERR_INVALID_ARG, "pass exactly one of Xp (permuted rows) and X (token rows)");
+  if (dYp == nullptr && dY == nullptr)
+    return fail(MOE_ERR_INVALID_ARG, "pass dYp (permuted rows), dY (token rows) or both");
+  if (Xp == nullptr && X == nullptr)
+    return fail(MOE_ERR_INVALID_ARG, "pass Xp (permuted rows), X (token rows) or both");
   if (dYp) MOE_CHECK_PTR(dYp);
   if (dY) MOE_CHECK_PTR(dY);
   if (Xp) MOE_CHECK_PTR(Xp);
@@ -759,7 +760,8 @@ int moe_lora_grouped_mlp_bwd(const moe_dims* dims, const moe_bf16* dYp, const mo
 
   {  // u = dYp B_dn -> pair us = s*u
     GemmParams p = base;
-    SLICE_ROWS(p, 0, dYp, dY, d, MAP3(p.sl[0].b, B_dn, G, d, r, 64, 64), d);
+    // token rows gathered from dY when given (L2-resident), else the permuted rows
+    SLICE_ROWS(p, 0, dY ? nullptr : dYp, dY, d, MAP3(p.sl[0].b, B_dn, G, d, r, 64, 64), d);
     p.nslices = 1; p.N = r; p.n_ntiles = (r + 63) / 64; p.ld0 = r; p.pair = Nr;
     p.out0 = w.us;
     if ((rc = run_gemm({128, true, false, Epi::kLoRAGrid}, p, RG, st->num_sms, s, "u"))) return rc;

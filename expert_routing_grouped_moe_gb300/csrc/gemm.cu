@@ -77,8 +77,12 @@ struct Cfg {
   // rows leave straight from registers; the ring takes the room instead)
   static constexpr uint32_t kStgBytes =
       kGrid ? 0u : (EPI == static_cast<int>(Epi::kDgradDn) ? 2 : 1) * kStgTileBytes;
+  // grid-mode LoRA products run two CTAs per SM (short kernels of ~1.7 waves
+  // at one CTA per SM): half the shared memory and registers each
+  static constexpr int kCtasPerSm = kGrid ? 2 : 1;
+  static constexpr uint32_t kSmemBudget = kGrid ? (kSmemMax / 2 - 1024) : kSmemMax;
   static constexpr uint32_t kRingFit =
-      (kSmemMax - kFixedSmem - kEpiWarps * kStgBytes) / kStageBytes * kStageBytes;
+      (kSmemBudget - kFixedSmem - kEpiWarps * kStgBytes) / kStageBytes * kStageBytes;
   static constexpr uint32_t kRingCap = kGrid ? kRingFit : kRingMax;
   // 4 / 4 / 6 stages for BN 256 / 192 (dgrad) / 128 (weight gradients); 7 in grid mode;
   // pairs: 6 stages of 32 KB (5 with the SwiGLU backward's two staging tiles)
@@ -740,7 +744,8 @@ __device__ __forceinline__ void epi_wgrad_full(const GemmParams& p, const TileIn
 }
 
 template <int BN, bool B_MN, bool WGRAD, int EPI, bool PAIR>
-__global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant__ GemmParams p) {
+__global__ void __launch_bounds__(kThreads, Cfg<BN, EPI, PAIR>::kCtasPerSm)
+    gemm_kernel(const __grid_constant__ GemmParams p) {
   using C = Cfg<BN, EPI, PAIR>;
   constexpr int S = C::kStages;
   constexpr bool GRID = EPI == static_cast<int>(Epi::kLoRAGrid);
@@ -1274,7 +1279,8 @@ cudaError_t launch_one(const GemmParams& p, int num_sms, cudaStream_t s) {
     const int pairs = tiles < max_pairs[dev] ? (tiles > 0 ? tiles : 1) : max_pairs[dev];
     return launch_pdl_cluster(kern, dim3(2 * pairs), dim3(kThreads), C::kSmemBytes, s, 2u, p);
   }
-  const int grid = tiles < num_sms ? (tiles > 0 ? tiles : 1) : num_sms;
+  const int slots = num_sms * C::kCtasPerSm;
+  const int grid = tiles < slots ? (tiles > 0 ? tiles : 1) : slots;
   return launch_pdl(kern, dim3(grid), dim3(kThreads), C::kSmemBytes, s, p);
 }
 

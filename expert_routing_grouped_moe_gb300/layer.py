@@ -27,13 +27,16 @@ LAUNCHES_BWD = 11
 
 class MoELoRALayer:
     def __init__(self, T, d, f, E, k, r, alpha, weights: dict, shared_expert=False,
-                 device="cuda", gather=False, full_grads=False):
+                 device="cuda", gather=False, full_grads=False, rank_r_tokens=False):
         """full_grads: the backward also returns dW_gu [G,2f,d] and dW_dn
         [G,d,f] (fp32 gradients of the expert weights, for full fine-tuning;
-        needs the permuted-row mode)."""
+        needs the permuted-row mode).  rank_r_tokens (permuted-row mode):
+        the LoRA-A products xa_gu and u read the token rows of X / dY (small
+        enough to stay in L2) instead of the permuted copies."""
         if full_grads and gather:
             raise ValueError("full weight gradients need the permuted-row mode (gather=False)")
         self.gather = bool(gather)
+        self.rank_r_tokens = bool(rank_r_tokens) and not self.gather
         self.full_grads = bool(full_grads)
         self.dims = L.make_dims(T, d, f, E, k, r, alpha / r, shared_expert)
         self.T, self.d, self.f, self.E, self.k, self.r = T, d, f, E, k, r
@@ -97,7 +100,8 @@ class MoELoRALayer:
         if not self.gather:
             L.moe_permute(X, self.K, self.dest_pos, self.Xp, stream)
         w = self.w
-        L.moe_lora_grouped_mlp_fwd(self.dims, self.Xp, None if self.Xp is not None else X,
+        X_tok = X if (self.Xp is None or self.rank_r_tokens) else None
+        L.moe_lora_grouped_mlp_fwd(self.dims, self.Xp, X_tok,
                                    self.counts, self.offsets, self.tile_off,
                                    self.sorted_src, topk_w, w["W_gu"], w["A_gu"], w["B_gu"],
                                    w["W_dn"], w["A_dn"], w["B_dn"], self.Yp, self.h, self.act,
@@ -113,7 +117,8 @@ class MoELoRALayer:
         if not self.gather:
             L.moe_permute(dY, self.K, self.dest_pos, self.dYp, stream)
         w, g = self.w, self.grads
-        L.moe_lora_grouped_mlp_bwd(self.dims, self.dYp, None if self.dYp is not None else dY,
+        dY_tok = dY if (self.dYp is None or self.rank_r_tokens) else None
+        L.moe_lora_grouped_mlp_bwd(self.dims, self.dYp, dY_tok,
                                    self.Xp, None if self.Xp is not None else self._X,
                                    self.counts, self.offsets,
                                    self.tile_off, self.sorted_src, self._topk_w, w["W_gu"],

@@ -40,9 +40,10 @@ def make_inputs(cfg, seed, ids=None, w=None):
     return wts, act, ids_np, w_np
 
 
-def run(cfg, wts, act, ids_np, w_np, gather=False, full=False):
+def run(cfg, wts, act, ids_np, w_np, gather=False, full=False, rank_r_tokens=False):
     layer = MoELoRALayer(cfg.T, cfg.d, cfg.f, cfg.E, cfg.k, cfg.r, cfg.alpha, wts,
-                         shared_expert=cfg.shared, device=DEV, gather=gather, full_grads=full)
+                         shared_expert=cfg.shared, device=DEV, gather=gather, full_grads=full,
+                         rank_r_tokens=rank_r_tokens)
     ids = torch.from_numpy(np.ascontiguousarray(ids_np, dtype=np.int32)).to(DEV)
     w = torch.from_numpy(np.ascontiguousarray(w_np, dtype=np.float32)).to(DEV)
     Y = layer.forward(act["X"], ids, w).clone()
@@ -66,13 +67,16 @@ def group_rows(ids_np, cfg):
     return out, T * K
 
 
-@pytest.mark.parametrize("gather", [True, False])
+@pytest.mark.parametrize("mode", ["gather", "permuted", "rank_r_tokens"])
 @pytest.mark.parametrize("name", list(SMALL))
-def test_layer_full_parity(name, gather):
-    """gather=True: GEMMs gather token rows from X / dY; False: permuted copies."""
+def test_layer_full_parity(name, mode):
+    """gather: GEMMs gather token rows from X / dY; permuted: permuted copies;
+    rank_r_tokens: permuted copies, the LoRA-A products gather token rows."""
     cfg = SMALL[name]
+    gather = mode == "gather"
     wts, act, ids_np, w_np = make_inputs(cfg, seed=7)
-    layer, Y, g = run(cfg, wts, act, ids_np, w_np, gather=gather)
+    layer, Y, g = run(cfg, wts, act, ids_np, w_np, gather=gather,
+                      rank_r_tokens=mode == "rank_r_tokens")
     P = oracle_params(wts, cfg)
     X, dY = to64(act["X"]), to64(act["dY"])
     s = cfg.scale

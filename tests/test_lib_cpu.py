@@ -89,11 +89,10 @@ def test_fwd_argument_errors_before_launch(lib):
     assert rc == _lib.MOE_ERR_INVALID_ARG
     assert b"k=9" in lib.moe_last_error()
     d = _dims()
-    # exactly one of Xp (permuted rows) and X (token rows)
-    for xp, x in ((None, None), (fake, fake)):
-        rc = lib.moe_lora_grouped_mlp_fwd(ctypes.byref(d), xp, x, *([fake] * 16), None)
-        assert rc == _lib.MOE_ERR_INVALID_ARG
-        assert b"exactly one of Xp" in lib.moe_last_error()
+    # at least one of Xp (permuted rows) and X (token rows)
+    rc = lib.moe_lora_grouped_mlp_fwd(ctypes.byref(d), None, None, *([fake] * 16), None)
+    assert rc == _lib.MOE_ERR_INVALID_ARG
+    assert b"pass Xp" in lib.moe_last_error()
     args = [None] + [fake] * 17
     args[14] = P((1 << 20) + 4)  # Yp misaligned
     rc = lib.moe_lora_grouped_mlp_fwd(ctypes.byref(d), *args, None)
