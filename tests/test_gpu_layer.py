@@ -208,7 +208,11 @@ def test_layer_full_size_sampled(name, gather):
     wts, act, ids_np, w_np = make_inputs(cfg, seed=1)
     layer, Y, g = run(cfg, wts, act, ids_np, w_np, gather=gather)
     rng = np.random.default_rng(3)
-    toks = sorted(rng.choice(cfg.T, size=4, replace=False).tolist() + [0, cfg.T - 1])
+    # 40 random tokens plus the first and the last, and the rows of the
+    # largest, the smallest non-empty, an empty, the shared and four random
+    # experts (every tile shape the full-size kernels meet: ragged tails,
+    # pair tiles with an idle half, experts spanning several tiles)
+    toks = sorted(set(rng.choice(cfg.T, size=40, replace=False).tolist() + [0, cfg.T - 1]))
     counts = np.bincount(ids_np.reshape(-1), minlength=cfg.E)
     sample_groups = [int(np.argmax(counts)), int(np.argmin(np.where(counts > 0, counts, 1 << 30)))]
     empties = np.nonzero(counts == 0)[0]
@@ -216,6 +220,8 @@ def test_layer_full_size_sampled(name, gather):
         sample_groups.append(int(empties[0]))
     if cfg.shared:
         sample_groups.append(cfg.E)
+    others = [e for e in np.nonzero(counts > 0)[0].tolist() if e not in sample_groups]
+    sample_groups += [int(e) for e in rng.choice(others, size=min(4, len(others)), replace=False)]
     need = set(sample_groups)
     for t in toks:
         need.update(int(e) for e in ids_np[t])
