@@ -73,9 +73,13 @@ __device__ __forceinline__ uint32_t pack2(float lo, float hi) {
 constexpr int kMaxSlots = 33;
 
 // One warp per token, 8 tokens per CTA.  Row of slot j = dest_pos[t*K + j].
-// Two column slots per lane and up to 8 slots' rows per step: 16 loads in
-// flight per lane, summed in fp32 in slot order.
-__global__ void __launch_bounds__(256) combine_kernel(
+// A lane handles CS column slots (16-byte vectors 32 apart) and loads the
+// rows of SB slots at a time, summed in fp32 in slot order: for K <= 2 two
+// slots x 4 columns at three CTAs per SM, for K <= 4 four slots x 4 columns,
+// else 8 slots x 2 columns (two CTAs per SM), so the loads in flight per SM
+// do not shrink with K.
+template <int SB, int CS, int MINB>
+__global__ void __launch_bounds__(256, MINB) combine_kernel(
     const uint4* __restrict__ rows, const int32_t* __restrict__ dest_pos, int T, int d8, int k,
     int shared, const float* __restrict__ weights, const float* __restrict__ row_scalars,
     float* __restrict__ slot_out, uint4* __restrict__ out) {
@@ -97,34 +101,34 @@ __global__ void __launch_bounds__(256) combine_kernel(
   }
   __syncwarp();
   uint4* orow = out + static_cast<int64_t>(t) * d8;
-  for (int v0 = lane; v0 < d8; v0 += 64) {
-    float a[2][8];
+  for (int v0 = lane; v0 < d8; v0 += 32 * CS) {
+    float a[CS][8];
 #pragma unroll
-    for (int i = 0; i < 2; ++i)
+    for (int i = 0; i < CS; ++i)
 #pragma unroll
       for (int e = 0; e < 8; ++e) a[i][e] = 0.f;
-    for (int j0 = 0; j0 < K; j0 += 8) {
-      uint4 x[8][2];
+    for (int j0 = 0; j0 < K; j0 += SB) {
+      uint4 x[SB][CS];
 #pragma unroll
-      for (int jj = 0; jj < 8; ++jj) {
+      for (int jj = 0; jj < SB; ++jj) {
         const int j = j0 + jj;
         const int pr = j < K ? s_row[warp][j] : -1;
 #pragma unroll
-        for (int i = 0; i < 2; ++i) {
+        for (int i = 0; i < CS; ++i) {
           const int v = v0 + i * 32;
           x[jj][i] = (pr >= 0 && v < d8) ? __ldg(rows + static_cast<int64_t>(pr) * d8 + v)
                                          : make_uint4(0, 0, 0, 0);
         }
       }
 #pragma unroll
-      for (int jj = 0; jj < 8; ++jj)
+      for (int jj = 0; jj < SB; ++jj)
         if (j0 + jj < K) {
 #pragma unroll
-          for (int i = 0; i < 2; ++i) acc_bf16x8(a[i], x[jj][i], s_c[warp][j0 + jj]);
+          for (int i = 0; i < CS; ++i) acc_bf16x8(a[i], x[jj][i], s_c[warp][j0 + jj]);
         }
     }
 #pragma unroll
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < CS; ++i) {
       const int v = v0 + i * 32;
       if (v < d8)
         orow[v] = make_uint4(pack2(a[i][0], a[i][1]), pack2(a[i][2], a[i][3]),
@@ -159,7 +163,11 @@ cudaError_t launch_combine(const uint16_t* rows, const int32_t* dest_pos, int T,
                            int shared, const float* weights, const float* row_scalars,
                            float* slot_out, uint16_t* out, cudaStream_t s) {
   if (T == 0) return cudaSuccess;
-  return launch_pdl(combine_kernel, dim3((T + 7) / 8), dim3(256), 0, s,
+  const int K = k + shared;
+  auto kern = K <= 2   ? combine_kernel<2, 4, 3>
+              : K <= 4 ? combine_kernel<4, 4, 2>
+                       : combine_kernel<8, 2, 2>;
+  return launch_pdl(kern, dim3((T + 7) / 8), dim3(256), 0, s,
                     reinterpret_cast<const uint4*>(rows), dest_pos, T, d / 8, k, shared, weights,
                     row_scalars, slot_out, reinterpret_cast<uint4*>(out));
 }
