@@ -33,7 +33,7 @@ EXPORTED = (
     "moe_mlp_bwd_workspace_size", "moe_lora_grouped_mlp_bwd", "moe_status",
     "moe_last_error", "moe_abi_version", "moe_kernel_name", "moe_probe_arm", "moe_probe_count",
     "moe_route_noalloc", "moe_selftest_wait_timeout", "moe_probe_read_stream",
-    "moe_route_kernel_count", "moe_ep_row_weights", "moe_ep_segment_ids",
+    "moe_route_kernel_count", "moe_ep_row_weights", "moe_ep_segment_ids", "moe_route_logits",
 )
 
 
@@ -98,6 +98,8 @@ def load(path: str = LIB_PATH):
             "moe_probe_read_stream": (ctypes.c_int, [_P, _SZ, _I, _P]),
             "moe_route_kernel_count": (_I, [_I, _I, _I]),
             "moe_ep_row_weights": (ctypes.c_int, [_P, _P, _I, _I, _I, _P, _P]),
+            "moe_route_logits": (ctypes.c_int, [_P, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P,
+                                                _P, _SZ, _P]),
             "moe_ep_segment_ids": (ctypes.c_int, [_P, _I, _I, ctypes.c_int64, _P, _P]),
         }
         for name, (res, args) in sig.items():
@@ -184,6 +186,18 @@ def moe_route(ids, E, shared_expert, counts, offsets, tile_off, sorted_src, dest
                             _i32(tile_off, "tile_off"), _i32(sorted_src, "sorted_src"),
                             _i32(dest_pos, "dest_pos"), _ptr(ws, name="ws"),
                             ws.numel() * ws.element_size(), _stream(stream)), "moe_route")
+
+
+def moe_route_logits(logits, k, shared_expert, ids, weights, counts, offsets, tile_off,
+                     sorted_src, dest_pos, ws, stream=None):
+    """moe_router_topk then moe_route in one call (ids, weights written)."""
+    T, E = logits.shape
+    _check(load().moe_route_logits(
+        _f32(logits, "logits"), T, E, int(k), 1 if shared_expert else 0, _i32(ids, "ids"),
+        _f32(weights, "weights"), _i32(counts, "counts"), _i32(offsets, "offsets"),
+        _i32(tile_off, "tile_off"), _i32(sorted_src, "sorted_src"), _i32(dest_pos, "dest_pos"),
+        _ptr(ws, name="ws"), ws.numel() * ws.element_size(), _stream(stream)),
+        "moe_route_logits")
 
 
 def moe_route_noalloc(ids, E, shared_expert, counts, offsets, tile_off, sorted_src, dest_pos,

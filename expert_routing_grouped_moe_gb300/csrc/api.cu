@@ -491,9 +491,12 @@ int moe_router_topk(const float* logits, int32_t T, int32_t E, int32_t k, int32_
   return ok();
 }
 
-int moe_route(const int32_t* ids, int32_t T, int32_t k, int32_t E, int32_t shared_expert,
-              int32_t* counts, int32_t* offsets, int32_t* tile_off, int32_t* sorted_src,
-              int32_t* dest_pos, void* ws, size_t ws_bytes, moe_stream_t stream) {
+namespace {
+// Host checks of moe_route's arguments (before anything is launched).
+int check_route_args(const int32_t* ids, int32_t T, int32_t k, int32_t E, int32_t shared_expert,
+                     const int32_t* counts, const int32_t* offsets, const int32_t* tile_off,
+                     const int32_t* sorted_src, const int32_t* dest_pos, const void* ws,
+                     size_t ws_bytes) {
   if (!ids || !counts || !offsets || !tile_off || !sorted_src || !dest_pos || !ws)
     return fail(MOE_ERR_INVALID_ARG, "NULL pointer");
   if (T <= 0 || k <= 0 || E <= 0 || (shared_expert != 0 && shared_expert != 1))
@@ -505,6 +508,29 @@ int moe_route(const int32_t* ids, int32_t T, int32_t k, int32_t E, int32_t share
   if (!aligned16(ws)) return fail(MOE_ERR_INVALID_ARG, "ws not 16-byte aligned");
   if (ws_bytes < moe_route_workspace_size(T, static_cast<int32_t>(K), static_cast<int32_t>(G)))
     return fail(MOE_ERR_WORKSPACE, "route workspace too small");
+  return MOE_OK;
+}
+}  // namespace
+
+int moe_route_logits(const float* logits, int32_t T, int32_t E, int32_t k,
+                     int32_t shared_expert, int32_t* ids, float* weights, int32_t* counts,
+                     int32_t* offsets, int32_t* tile_off, int32_t* sorted_src, int32_t* dest_pos,
+                     void* ws, size_t ws_bytes, moe_stream_t stream) {
+  if (logits == nullptr || weights == nullptr) return fail(MOE_ERR_INVALID_ARG, "NULL pointer");
+  int rc = check_route_args(ids, T, k, E, shared_expert, counts, offsets, tile_off, sorted_src,
+                            dest_pos, ws, ws_bytes);
+  if (rc) return rc;
+  if ((rc = moe_router_topk(logits, T, E, k, ids, weights, stream))) return rc;
+  return moe_route(ids, T, k, E, shared_expert, counts, offsets, tile_off, sorted_src, dest_pos,
+                   ws, ws_bytes, stream);
+}
+
+int moe_route(const int32_t* ids, int32_t T, int32_t k, int32_t E, int32_t shared_expert,
+              int32_t* counts, int32_t* offsets, int32_t* tile_off, int32_t* sorted_src,
+              int32_t* dest_pos, void* ws, size_t ws_bytes, moe_stream_t stream) {
+  int rc0 = check_route_args(ids, T, k, E, shared_expert, counts, offsets, tile_off, sorted_src,
+                             dest_pos, ws, ws_bytes);
+  if (rc0) return rc0;
   DevState* st = nullptr;
   int rc = device_state(&st);
   if (rc) return rc;

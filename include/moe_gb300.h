@@ -107,6 +107,18 @@ MOE_API int moe_router_topk(const float* logits, int32_t T, int32_t E, int32_t k
 /* Routing: article section "Optimisation 3", steps 1-5.                     */
 /* ------------------------------------------------------------------------ */
 
+/* The router and the routing pass in one call, from the logits: the top-k
+ * ids and renormalised weights of moe_router_topk (written to ids [T,k] and
+ * weights [T,k]), then the routing tables of moe_route from those ids, all
+ * enqueued on `stream` with no host round trip in between.  Same arguments,
+ * checks and results as the two calls in sequence; every check runs before
+ * anything is launched. */
+MOE_API int moe_route_logits(const float* logits, int32_t T, int32_t E, int32_t k,
+                             int32_t shared_expert, int32_t* ids, float* weights,
+                             int32_t* counts, int32_t* offsets, int32_t* tile_off,
+                             int32_t* sorted_src, int32_t* dest_pos, void* ws, size_t ws_bytes,
+                             moe_stream_t stream);
+
 /* Bytes of scratch moe_route needs for T tokens, K slots, G groups. */
 MOE_API size_t moe_route_workspace_size(int32_t T, int32_t K, int32_t G);
 

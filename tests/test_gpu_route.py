@@ -124,3 +124,29 @@ def test_route_bad_ids_reported():
     assert np.all(got["dest_pos"][bad] == -1)
     np.testing.assert_array_equal(got["sorted_src"][got["dest_pos"][~bad]],
                                   np.nonzero(~bad)[0])
+
+
+@pytest.mark.parametrize("name", ["tiny", "qwen3_30b_a3b", "skewed_shared"])
+def test_route_logits_equals_router_then_route(name):
+    """The one-call router + routing gives the two calls' results bit for bit,
+    and they are the oracle's."""
+    cfg = synth.CONFIGS[name]
+    logits = synth.layer_activations(cfg, seed=8, device="cpu")["logits"].to(DEV)
+    T, k, E, shared = cfg.T, cfg.k, cfg.E, cfg.shared
+    K, G = k + int(shared), E + int(shared)
+    mk = lambda n: torch.full((n,), -7, dtype=torch.int32, device=DEV)  # noqa: E731
+    ids = torch.empty(T, k, dtype=torch.int32, device=DEV)
+    w = torch.empty(T, k, dtype=torch.float32, device=DEV)
+    t = {n: mk(c) for n, c in (("counts", G), ("offsets", G + 1), ("tile_off", G + 1),
+                               ("sorted_src", T * K), ("dest_pos", T * K))}
+    ws = torch.empty(L.moe_route_workspace_size(T, K, G), dtype=torch.uint8, device=DEV)
+    L.moe_route_logits(logits, k, shared, ids, w, t["counts"], t["offsets"], t["tile_off"],
+                       t["sorted_src"], t["dest_pos"], ws)
+    assert L.moe_status() == L.MOE_OK
+    ref, _ = gpu_route(ids.clone(), E, shared)
+    for key in ref:
+        np.testing.assert_array_equal(t[key].cpu().numpy(), ref[key], err_msg=key)
+    ids_ref, w_ref = oracle.router_topk(logits.cpu().numpy(), k)
+    np.testing.assert_array_equal(ids.cpu().numpy(), ids_ref)
+    np.testing.assert_allclose(w.cpu().numpy(), w_ref, rtol=2e-6, atol=1e-7)
+    check_route(ids, E, shared)

@@ -179,3 +179,16 @@ def test_route_and_route_noalloc_accept_the_same_shapes(lib):
     T_ok = (1 << 31) - 256
     assert lib.moe_route(fake, T_ok, 1, 1, 0, *([fake] * 6), 4, None) == \
         _lib.MOE_ERR_WORKSPACE
+
+
+def test_route_logits_checks_before_launch(lib):
+    from expert_routing_grouped_moe_gb300 import _lib
+    P = ctypes.c_void_p
+    fake = P(1 << 20)
+    # NULL logits, k > E, too small a workspace: refused before anything runs
+    assert lib.moe_route_logits(None, 4, 8, 2, 0, *([fake] * 8), 1 << 20, None) == \
+        _lib.MOE_ERR_INVALID_ARG
+    assert lib.moe_route_logits(fake, 4, 8, 9, 0, *([fake] * 8), 1 << 20, None) == \
+        _lib.MOE_ERR_INVALID_ARG
+    assert lib.moe_route_logits(fake, 4, 8, 2, 0, *([fake] * 8), 4, None) == \
+        _lib.MOE_ERR_WORKSPACE
