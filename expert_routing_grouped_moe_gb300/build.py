@@ -66,7 +66,8 @@ def build(verbose: bool = False, force: bool = False, ptxas_info: bool = False) 
                 if verbose and out.strip():
                     print(out, file=sys.stderr)
     if force or jobs or _stale(LIB, objs):
-        out = _run([nvcc, *ARCH, "-shared", "-cudart", "static", "-o", LIB + ".tmp", *objs])
+        out = _run([nvcc, *ARCH, "-shared", "-cudart", "static", "-o", LIB + ".tmp", *objs,
+                    "-ldl"])
         os.replace(LIB + ".tmp", LIB)
         if verbose and out.strip():
             print(out, file=sys.stderr)

@@ -481,6 +481,7 @@ int moe_probe_read_stream(const void* src, size_t bytes, int32_t pattern, moe_st
 
 int moe_router_topk(const float* logits, int32_t T, int32_t E, int32_t k, int32_t* ids,
                     float* weights, moe_stream_t stream) {
+  NvtxScope nvtx("moe_router_topk");
   if (logits == nullptr || ids == nullptr || weights == nullptr)
     return fail(MOE_ERR_INVALID_ARG, "NULL pointer");
   if (T <= 0 || E <= 0 || k <= 0 || k > E) return fail(MOE_ERR_INVALID_ARG, "bad T/E/k");
@@ -516,6 +517,7 @@ int moe_route_logits(const float* logits, int32_t T, int32_t E, int32_t k,
                      int32_t shared_expert, int32_t* ids, float* weights, int32_t* counts,
                      int32_t* offsets, int32_t* tile_off, int32_t* sorted_src, int32_t* dest_pos,
                      void* ws, size_t ws_bytes, moe_stream_t stream) {
+  NvtxScope nvtx("moe_route_logits");
   if (logits == nullptr || weights == nullptr) return fail(MOE_ERR_INVALID_ARG, "NULL pointer");
   int rc = check_route_args(ids, T, k, E, shared_expert, counts, offsets, tile_off, sorted_src,
                             dest_pos, ws, ws_bytes);
@@ -528,6 +530,7 @@ int moe_route_logits(const float* logits, int32_t T, int32_t E, int32_t k,
 int moe_route(const int32_t* ids, int32_t T, int32_t k, int32_t E, int32_t shared_expert,
               int32_t* counts, int32_t* offsets, int32_t* tile_off, int32_t* sorted_src,
               int32_t* dest_pos, void* ws, size_t ws_bytes, moe_stream_t stream) {
+  NvtxScope nvtx("moe_route");
   int rc0 = check_route_args(ids, T, k, E, shared_expert, counts, offsets, tile_off, sorted_src,
                              dest_pos, ws, ws_bytes);
   if (rc0) return rc0;
@@ -544,6 +547,7 @@ int moe_route(const int32_t* ids, int32_t T, int32_t k, int32_t E, int32_t share
 
 int moe_permute(const moe_bf16* src, int32_t T, int32_t d, int32_t K, const int32_t* dest_pos,
                 moe_bf16* dst, moe_stream_t stream) {
+  NvtxScope nvtx("moe_permute");
   MOE_CHECK_PTR(src);
   MOE_CHECK_PTR(dst);
   if (!dest_pos) return fail(MOE_ERR_INVALID_ARG, "NULL pointer");
@@ -562,6 +566,7 @@ int moe_unpermute_combine(const moe_bf16* rows, const int32_t* dest_pos, int32_t
                           int32_t k, int32_t shared_expert, const float* weights,
                           const float* row_scalars, float* slot_out, moe_bf16* out,
                           moe_stream_t stream) {
+  NvtxScope nvtx("moe_unpermute_combine");
   MOE_CHECK_PTR(rows);
   MOE_CHECK_PTR(out);
   if (!dest_pos) return fail(MOE_ERR_INVALID_ARG, "NULL pointer");
@@ -586,6 +591,7 @@ int moe_lora_grouped_mlp_fwd(const moe_dims* dims, const moe_bf16* Xp, const moe
                              const moe_bf16* W_dn, const moe_bf16* A_dn, const moe_bf16* B_dn,
                              moe_bf16* Yp, float* h, moe_bf16* act, moe_bf16* xa_gu,
                              moe_bf16* xa_dn, moe_stream_t stream) {
+  NvtxScope nvtx("moe_lora_grouped_mlp_fwd");
   (void)counts;
   int rc = check_dims(dims);
   if (rc) return rc;
@@ -680,6 +686,7 @@ int moe_lora_grouped_mlp_bwd(const moe_dims* dims, const moe_bf16* dYp, const mo
                              float* dw_rows, float* dA_gu, float* dB_gu, float* dA_dn,
                              float* dB_dn, float* dW_gu, float* dW_dn, void* ws,
                              size_t ws_bytes, moe_stream_t stream) {
+  NvtxScope nvtx("moe_lora_grouped_mlp_bwd");
   (void)counts;
   int rc = check_dims(dims);
   if (rc) return rc;

@@ -92,6 +92,7 @@ extern "C" {
 
 int moe_ep_row_weights(const float* topk_w, const int32_t* dest_pos, int32_t T, int32_t k,
                        int32_t shared_expert, float* row_w, moe_stream_t stream) {
+  NvtxScope nvtx("moe_ep_row_weights");
   if (!topk_w || !dest_pos || !row_w) return record_error(MOE_ERR_INVALID_ARG, "NULL pointer");
   if (T <= 0 || k <= 0 || (shared_expert != 0 && shared_expert != 1))
     return record_error(MOE_ERR_INVALID_ARG, "bad T/k/shared_expert");
@@ -110,6 +111,7 @@ int moe_ep_row_weights(const float* topk_w, const int32_t* dest_pos, int32_t T, 
 
 int moe_ep_segment_ids(const int32_t* counts, int32_t P, int32_t E_loc, int64_t n_rows,
                        int32_t* ids, moe_stream_t stream) {
+  NvtxScope nvtx("moe_ep_segment_ids");
   if (!counts || (!ids && n_rows > 0)) return record_error(MOE_ERR_INVALID_ARG, "NULL pointer");
   if (P <= 0 || E_loc <= 0 || n_rows < 0)
     return record_error(MOE_ERR_INVALID_ARG, "bad P/E_loc/n_rows");

@@ -6,6 +6,7 @@
 #include <cstdint>
 #include <cuda.h>
 #include <cuda_runtime.h>
+#include <nvtx3/nvToolsExt.h>
 
 namespace moe {
 
@@ -81,10 +82,22 @@ inline bool routed_rows_fit(int64_t T, int64_t K, int64_t G) {
 // CUDA event on the launch stream before and after the launches in scope.
 int probe_begin(const char* name, cudaStream_t s);
 void probe_end(int token, cudaStream_t s);
+// NVTX range (host-side, shown by Nsight tools; a no-op without one) around
+// a C-ABI call or a kernel launch.
+struct NvtxScope {
+  explicit NvtxScope(const char* name) { nvtxRangePushA(name); }
+  ~NvtxScope() { nvtxRangePop(); }
+  NvtxScope(const NvtxScope&) = delete;
+  NvtxScope& operator=(const NvtxScope&) = delete;
+};
+// Kernel launches in scope are traced under `name`: an NVTX range, and the
+// timing probe's events when it is armed for that name.
 struct ProbeScope {
+  NvtxScope range;
   int token;
   cudaStream_t s;
-  ProbeScope(const char* name, cudaStream_t st) : token(probe_begin(name, st)), s(st) {}
+  ProbeScope(const char* name, cudaStream_t st)
+      : range(name), token(probe_begin(name, st)), s(st) {}
   ~ProbeScope() { probe_end(token, s); }
   ProbeScope(const ProbeScope&) = delete;
   ProbeScope& operator=(const ProbeScope&) = delete;

@@ -56,6 +56,7 @@ extern "C" {
 int moe_route_noalloc(const int32_t* ids, int32_t T, int32_t k, int32_t E, int32_t shared_expert,
                       int32_t* counts, int32_t* offsets, int32_t* tile_off, int32_t* sorted_src,
                       int32_t* dest_pos, moe_stream_t stream) {
+  NvtxScope nvtx("moe_route_noalloc");
   if (!ids || !counts || !offsets || !tile_off || !sorted_src || !dest_pos)
     return set_msg(MOE_ERR_INVALID_ARG, "moe_route_noalloc: NULL pointer");
   if (T <= 0 || k <= 0 || E <= 0 || (shared_expert != 0 && shared_expert != 1) || k > E)
