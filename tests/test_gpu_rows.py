@@ -109,9 +109,13 @@ def test_combine(T, E, k, dist, shared, d, weighted):
     np.testing.assert_array_equal(slot.cpu().numpy(), scal.cpu().numpy()[prow[:, :k]])
 
 
-@pytest.mark.parametrize("T,E,k,dist", [(1 << 18, 128, 8, "zipf"), (1 << 20, 128, 8, "uniform"),
-                                         (1 << 20, 8, 2, "zipf")])
+@pytest.mark.parametrize("T,E,k,dist",
+                         [p for p in synth.ROUTE_SWEEP if p[0] == 1 << 18]
+                         + [(1 << 20, 128, 8, "uniform"), (1 << 20, 8, 2, "zipf"),
+                            (1 << 20, 64, 4, "zipf")])
 def test_permute_combine_full_size_sampled(T, E, k, dist):
+    """Every (E, k, distribution) point of the routing workload at T = 256K, and
+    three at 1M: sampled tokens' combine and permuted rows against the oracle."""
     d = 2048
     ids = synth.topk_ids(T, E, k, dist, seed=8, device=DEV)
     X = synth.hidden_rows(T, d, seed=8, device=DEV)
