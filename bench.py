@@ -500,6 +500,19 @@ def routing_sweep(torch, L, synth, dev, peaks, points=DEFAULT_SWEEP_POINTS, d=20
             calls["combine"] = (lambda: L.moe_unpermute_combine(Xp, dst, k, False, Y, weights=w),
                                 2 * N * d + 2 * T * d + 8 * N + 4 * T * k)
         res = {"T": T, "E": E, "k": k, "dist": dist, "d": d}
+        # context: the same routing step written with PyTorch ops, as the pages
+        # do it (stable sort of the flattened ids, one bincount, offsets by a
+        # cumulative sum, the inverse permutation by a scatter)
+        flat = ids.view(-1)
+
+        def torch_route():
+            order = torch.argsort(flat, stable=True)
+            cnt = torch.bincount(flat, minlength=E)
+            offs = torch.cumsum(cnt, 0)
+            inv = torch.empty_like(order)
+            inv[order] = torch.arange(N, device=dev)
+            return offs, inv
+        calls_ctx = {"torch_ops_route": (torch_route, 4 * T * k + 8 * N + 12 * E)}
         tot_ms, tot_b = 0.0, 0
         for name, (fn, nbytes) in calls.items():
             fn()
@@ -522,6 +535,22 @@ def routing_sweep(torch, L, synth, dev, peaks, points=DEFAULT_SWEEP_POINTS, d=20
         if not route_only:
             gbs = tot_b / (tot_ms / 1e3) / 1e9
             res["pipeline"] = {"ms": tot_ms, "gbs": gbs, "frac_of_hbm": gbs / peaks["hbm_gbs"]}
+        for name, (fn, nbytes) in calls_ctx.items():
+            fn()
+            torch.cuda.synchronize()
+            total = 0.0
+            for _ in range(reps):
+                flush.fill_(1)
+                e0 = torch.cuda.Event(enable_timing=True)
+                e1 = torch.cuda.Event(enable_timing=True)
+                e0.record()
+                fn()
+                e1.record()
+                torch.cuda.synchronize()
+                total += e0.elapsed_time(e1)
+            res[name] = {"ms": total / reps,
+                         "note": "context, not this library: torch.argsort(stable) + bincount + "
+                                 "cumsum + inverse scatter on the same ids"}
         out.append(res)
         calls.clear()
         X = Xp = Y = w = None  # noqa: F841  (free this point's rows before the next)

@@ -1083,16 +1083,20 @@ __global__ void __launch_bounds__(kThreads, Cfg<BN, EPI, PAIR>::kCtasPerSm)
         }
         const uint32_t sa = smem_u32(ring + stage * C::kStageBytes);
         const uint32_t sb = sa + kAStageBytes;
+        int wg_nk16 = 4;  // weight gradients: K steps of 16 rows this block takes
         if (WGRAD) {
           const int b = kb % ti.nkb;
           const int tail = ti.nvalid - b * BK;
           if (tail < BK) {
-            // rows [tail, 64) of this block belong to the next group (or lie
-            // past the buffer): zero them in the A tile (2 chunks) and, for
-            // the LoRA gradients, in the B tile too; with zero A rows the
-            // wide B tile's extra rows (finite data) add nothing
+            // the group's last block: rows [tail, 64) belong to the next group
+            // (or lie past the buffer).  The MMAs stop after the K step that
+            // holds row tail - 1; the rows of that step past tail are zeroed
+            // in the A tile (2 chunks) and, for the LoRA gradients, in the B
+            // tile too (rows past the written total may hold garbage); with
+            // zero A rows the wide B tile's extra rows (finite data) add nothing
+            wg_nk16 = (tail + 15) / 16;
             constexpr int kPieces = EPI == static_cast<int>(Epi::kWgradFull) ? 16 : 32;
-            const int n = (BK - tail) * kPieces;
+            const int n = (wg_nk16 * 16 - tail) * kPieces;
             for (int i = lane; i < n; i += 32) {
               const int line = tail + i / kPieces;
               const int piece = i % kPieces;
@@ -1107,7 +1111,7 @@ __global__ void __launch_bounds__(kThreads, Cfg<BN, EPI, PAIR>::kCtasPerSm)
         if (lane == 0) {
           tc_fence_after();
           if (p.gather_any) fence_proxy_async_smem();  // LSU-copied A rows -> async proxy
-          int nk16 = 4;
+          int nk16 = WGRAD ? wg_nk16 : 4;
           if (!WGRAD) nk16 = min(4, (p.sl[cs].K - ckc + 15) / 16);
           // descriptors of the stage's first K step; each further K step of
           // 16 moves the start address field (bits 0-13, address >> 4) by
