@@ -880,11 +880,10 @@ __global__ void __launch_bounds__(kThreads, Cfg<BN, EPI, PAIR>::kCtasPerSm)
       if (!WGRAD && p.gather_any) lane_rows(ti.row0, ti.nvalid, 4, y);
       int cs = 0, ckc = 0;  // rows mode: slice and K offset of the next K block
       for (int kb = 0; kb < ti.nk; ++kb) {
-        int s = 0, kc = 0, kext = 0, row = 0;
+        int s = 0, kc = 0, row = 0;
         if (!WGRAD) {
           s = cs;
           kc = ckc;
-          kext = p.sl[s].K - kc;
           ckc += BK;
           if (ckc >= p.sl[cs].K) {
             ++cs;
@@ -896,7 +895,6 @@ __global__ void __launch_bounds__(kThreads, Cfg<BN, EPI, PAIR>::kCtasPerSm)
           row = ti.row0 + b * BK;
           if (p.sl[s].gather) lane_rows(row, ti.nvalid - b * BK, 2, y);
         }
-        (void)kext;
         const bool gat = p.sl[s].gather != 0;
         int w_ok = 1;
         uint64_t* fb = full_bar + stage;

@@ -222,7 +222,7 @@ class ExpertParallelLayer:
         Yp = Xp.new_empty(Xp.shape)
         comm.all_to_all(Yp, out_rows, send, recv)
         Y, _ = ops.combine(Yp, t["dest_pos"], k)
-        self._fw = dict(t=t, send=send, recv=recv, n_recv=n_recv, rows_shape=Xp.shape)
+        self._fw = dict(t=t, send=send, recv=recv, n_recv=n_recv)
         return Y
 
     def backward(self, dY):
