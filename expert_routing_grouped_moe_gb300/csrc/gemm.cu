@@ -66,7 +66,7 @@ __host__ __device__ constexpr uint32_t pow2_at_least(uint32_t v) {
   return p;
 }
 
-template <int BN, int EPI, bool PAIR = false>
+template <int BN, int EPI, bool PAIR = false, bool B_MN = false>
 struct Cfg {
   // a CTA of a pair stages half of B's BN columns
   static constexpr uint32_t kBStageBytes = (PAIR ? BN / 2 : BN) * BK * 2;
@@ -77,15 +77,18 @@ struct Cfg {
   // rows leave straight from registers; the ring takes the room instead)
   static constexpr uint32_t kStgBytes =
       kGrid ? 0u : (EPI == static_cast<int>(Epi::kDgradDn) ? 2 : 1) * kStgTileBytes;
-  // grid-mode LoRA products run two CTAs per SM (short kernels of ~1.7 waves
-  // at one CTA per SM): half the shared memory and registers each
-  static constexpr int kCtasPerSm = kGrid ? 2 : 1;
-  static constexpr uint32_t kSmemBudget = kGrid ? (kSmemMax / 2 - 1024) : kSmemMax;
+  // grid-mode LoRA products with K-major B (X·Aᵀ) run two CTAs per SM (short
+  // kernels of ~1.7 waves at one CTA per SM): half the shared memory and
+  // registers each.  With MN-major B (the dH·B products) one CTA with the
+  // full 7-stage ring measured faster.
+  static constexpr int kCtasPerSm = (kGrid && !B_MN) ? 2 : 1;
+  static constexpr uint32_t kSmemBudget = kCtasPerSm == 2 ? (kSmemMax / 2 - 1024) : kSmemMax;
   static constexpr uint32_t kRingFit =
       (kSmemBudget - kFixedSmem - kEpiWarps * kStgBytes) / kStageBytes * kStageBytes;
   static constexpr uint32_t kRingCap = kGrid ? kRingFit : kRingMax;
-  // 4 / 4 / 6 stages for BN 256 / 192 (dgrad) / 128 (weight gradients); 7 in grid mode;
-  // pairs: 6 stages of 32 KB (5 with the SwiGLU backward's two staging tiles)
+  // 4 / 4 / 6 stages for BN 256 / 192 (dgrad) / 128 (weight gradients); in grid
+  // mode 3 at two CTAs per SM, 7 at one; pairs: 6 stages of 32 KB (5 with the
+  // SwiGLU backward's two staging tiles)
   static constexpr int kStages = (kRingFit < kRingCap ? kRingFit : kRingCap) / kStageBytes;
   static constexpr uint32_t kTmemCols = pow2_at_least(2 * BN);  // power of two >= 32
   static constexpr size_t kSmemBytes =
@@ -744,9 +747,9 @@ __device__ __forceinline__ void epi_wgrad_full(const GemmParams& p, const TileIn
 }
 
 template <int BN, bool B_MN, bool WGRAD, int EPI, bool PAIR>
-__global__ void __launch_bounds__(kThreads, Cfg<BN, EPI, PAIR>::kCtasPerSm)
+__global__ void __launch_bounds__(kThreads, Cfg<BN, EPI, PAIR, B_MN>::kCtasPerSm)
     gemm_kernel(const __grid_constant__ GemmParams p) {
-  using C = Cfg<BN, EPI, PAIR>;
+  using C = Cfg<BN, EPI, PAIR, B_MN>;
   constexpr int S = C::kStages;
   constexpr bool GRID = EPI == static_cast<int>(Epi::kLoRAGrid);
   static_assert(!PAIR || (!WGRAD && !GRID), "CTA pairs serve the rows-mode tiles");
@@ -1244,7 +1247,7 @@ __global__ void wait_selftest_kernel(int* status, unsigned long long timeout_ns)
 
 template <int BN, bool B_MN, bool WGRAD, int EPI, bool PAIR = false>
 cudaError_t launch_one(const GemmParams& p, int num_sms, cudaStream_t s) {
-  using C = Cfg<BN, EPI, PAIR>;
+  using C = Cfg<BN, EPI, PAIR, B_MN>;
   static_assert(C::kSmemBytes <= 232448, "shared memory budget");
   auto kern = gemm_kernel<BN, B_MN, WGRAD, EPI, PAIR>;
   cudaError_t e =
