@@ -37,7 +37,7 @@ PEAKS_FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # sources the capture ran (kernel_sources_digest); a figure whose stamp no
 # longer matches the sources is stale and reported as null.
 NCU_TRAFFIC = {
-    ("gate_up", "qwen3_30b_a3b"): {"bytes": 999936256 + 273641728, "sources": "45305221d8fa"},
+    ("gate_up", "qwen3_30b_a3b"): {"bytes": 997253120 + 273805824, "sources": "cb76e7de276b"},
 }
 GEMM_SOURCES = ("csrc/gemm.cu", "csrc/ptx.cuh", "csrc/internal.h", "csrc/api.cu")
 
@@ -774,6 +774,11 @@ def run_ours(args):
         "routing_sweep": route_sweep,
         "roofline": roof,
         "kernels": kernels,
+        "kernels_note": ("ms = CUDA-event time per launch on the launching stream in a "
+                         "separate probe pass; the weight-gradient kernels (stream 'aux') "
+                         "run beside the main stream's dgrad chain, so their span includes "
+                         "time spent waiting for and sharing SMs, and their frac "
+                         "understates the kernel (serialised ncu times are in profiles/)"),
         "cpu_baseline": cpu,
         "e2e": {"value": world * cfg.T / (e2e_ms / 1e3), "unit": "tokens/s",
                 "ms_per_step": e2e_ms, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
