@@ -1,6 +1,7 @@
 // C ABI of the MoE-LoRA expert layer: argument checks, tensor-map encoding and
 // kernel launches.  No call here allocates device memory or synchronises,
 // except moe_status().  See include/moe_gb300.h for the contract of each call.
+#include <algorithm>
 #include <cstdarg>
 #include <cstdio>
 #include <cstdlib>
@@ -297,14 +298,35 @@ namespace {
 struct BwdWs {
   uint16_t *us, *vs, *dh;  // hi/lo pair buffers
   float* dwp;
+  // LoRA weight gradients with groups split into parts of wg_rows rows (0: no
+  // split): the parts' partial sums and the arrival counters
+  int wg_rows;
+  float* wg_part;
+  int* wg_cnt;
+  size_t wg_cnt_bytes;
   size_t bytes;
 };
 
 size_t align_up(size_t x) { return (x + 1023) & ~size_t(1023); }
 
+// Rows per part in the LoRA weight-gradient GEMMs, whose tiles otherwise sum
+// over all of a group's rows.  A shared expert sees every token, K times the
+// mean routed group (and a skewed router adds more large groups); their tiles
+// would be many times longer than the rest and run last on a few SMs.  So
+// with a shared expert the groups are summed in parts of at least 1.25 times
+// the mean group size and 1024 rows (evenly loaded groups stay whole), the
+// parts added in order.  0 (no split): no shared expert, or the part table
+// does not fit in shared memory.  (Without a shared expert the split kernel
+// measured a few us slower on balanced routing, where nothing splits.)
+int wgrad_rows_per_part(int64_t N, int64_t G, bool shared) {
+  if (!shared || G < 1 || G + 1 > kTileTabInts) return 0;
+  int64_t rows = std::max<int64_t>(1024, (5 * N + 4 * G - 1) / (4 * G));
+  rows = std::min<int64_t>((rows + 63) / 64 * 64, int64_t(1) << 30);
+  return static_cast<int>(rows);
+}
+
 BwdWs bwd_layout(const moe_dims* dm, void* base) {
   const int64_t K = dm->k + dm->shared_expert, G = dm->E + dm->shared_expert;
-  (void)G;
   const size_t P = static_cast<size_t>(dm->T) * static_cast<size_t>(K);  // routed rows N
   const size_t nr = align_up(2 * P * dm->r * 2);
   const size_t ndh = align_up(2 * P * 2 * static_cast<size_t>(dm->f) * 2);
@@ -317,6 +339,15 @@ BwdWs bwd_layout(const moe_dims* dm, void* base) {
   w.vs = reinterpret_cast<uint16_t*>(b + o); o += nr;
   w.dh = reinterpret_cast<uint16_t*>(b + o); o += ndh;
   w.dwp = reinterpret_cast<float*>(b + o); o += ndw;
+  w.wg_rows = wgrad_rows_per_part(static_cast<int64_t>(P), G, dm->shared_expert != 0);
+  if (w.wg_rows > 0) {
+    // parts over all groups <= G + N / wg_rows; M tiles <= max(d, 2f) / 128
+    const size_t parts = static_cast<size_t>(G) + (P + w.wg_rows - 1) / w.wg_rows;
+    const size_t mt = (static_cast<size_t>(std::max(dm->d, 2 * dm->f)) + 127) / 128;
+    w.wg_part = reinterpret_cast<float*>(b + o); o += align_up(parts * mt * 8192 * 4);
+    w.wg_cnt_bytes = static_cast<size_t>(G) * mt * 8 * 4;
+    w.wg_cnt = reinterpret_cast<int*>(b + o); o += align_up(w.wg_cnt_bytes);
+  }
   w.bytes = o;
   return w;
 }
@@ -770,7 +801,14 @@ int moe_lora_grouped_mlp_bwd(const moe_dims* dims, const moe_bf16* dYp, const mo
     MAP2(p.wb_lo, j.b + Nr, N, r, 64, 64);
     p.M = j.M; p.N = r; p.n_ntiles = (j.M + 127) / 128;
     p.fout = j.out; p.fstride = static_cast<int64_t>(j.M) * r; p.transpose_out = j.transpose;
-    return run_gemm({128, true, true, Epi::kWgrad}, p, R, st->num_sms, ss, j.name);
+    if (w.wg_rows > 0) {
+      p.wg_rows = w.wg_rows;
+      p.wg_part = w.wg_part;
+      p.wg_cnt = w.wg_cnt;
+      p.max_tiles = static_cast<int>((G + (N + w.wg_rows - 1) / w.wg_rows) * p.n_ntiles);
+    }
+    return run_gemm({128, true, true, w.wg_rows > 0 ? Epi::kWgradSplit : Epi::kWgrad}, p, R,
+                    st->num_sms, ss, j.name);
   };
   // full fine-tuning: per-group sum over the group's rows of A^T B with A a
   // hi/lo pair [2, N, M] (two K passes) and B one wide bf16 row matrix [N, Nb];
@@ -797,6 +835,10 @@ int moe_lora_grouped_mlp_bwd(const moe_dims* dims, const moe_bf16* dYp, const mo
     SLICE_ROWS(p, 0, dY ? nullptr : dYp, dY, d, MAP3(p.sl[0].b, B_dn, G, d, r, 64, 64), d);
     p.nslices = 1; p.N = r; p.n_ntiles = (r + 63) / 64; p.ld0 = r; p.pair = Nr;
     p.out0 = w.us;
+    if (w.wg_rows > 0) {  // zero the split weight-gradient counters for the kernels after it
+      p.zero = w.wg_cnt;
+      p.n_zero = static_cast<int64_t>(w.wg_cnt_bytes / 4);
+    }
     if ((rc = run_gemm({128, true, false, Epi::kLoRAGrid}, p, RG, st->num_sms, s, "u"))) return rc;
   }
   if ((rc = stream_dep(st->ev[0], s, aux))) return rc;

@@ -242,6 +242,8 @@ struct TileInfo {
   int row0;    // first permuted row: of the tile (rows mode) / of the group (wgrad)
   int nvalid;  // rows mode: rows of the group in this tile (<= 128); wgrad: group rows
   int nkb;     // wgrad: 64-row K blocks per slice
+  // wgrad with split groups: this tile's part of the group's rows, of nparts
+  int part, nparts;
   // grid mode: groups g .. g + nx - 1 of this pass own rows [rlo, rhi) of the
   // tile; rows from rmid on belong to group g + 1 (B block / accumulator slot 1)
   int nx, rlo, rmid, rhi;
@@ -311,7 +313,7 @@ __device__ __forceinline__ void unit_next(Unit& u, const GemmParams& p, const in
 
 // ROWS = false skips the row range (row0, nvalid) of a rows-mode tile, which
 // the MMA issuer does not need.
-template <bool WGRAD, bool ROWS = true>
+template <bool WGRAD, bool ROWS = true, bool SPLIT = false>
 __device__ __forceinline__ TileInfo tile_info(const GemmParams& p, int t, const int* tab) {
   TileInfo ti;
   if (!WGRAD) {
@@ -332,6 +334,26 @@ __device__ __forceinline__ TileInfo tile_info(const GemmParams& p, int t, const 
       ti.nvalid = min(BM, cnt - local * BM);
     }
     ti.nkb = 0;
+  } else if constexpr (SPLIT) {
+    // groups split into parts of wg_rows rows: tile t = (part index * M tiles
+    // + mt) * N tiles + nt, where the group's parts are numbered from tab[g]
+    // (tab = parts of the earlier groups, then offsets when both fit)
+    const int per_g = p.n_ntiles * p.n_btiles;
+    const int pidx = t / per_g;
+    const int rem = t - pidx * per_g;
+    ti.mt = rem / p.n_btiles;
+    ti.nt = rem - ti.mt * p.n_btiles;
+    // every group in one part (no group above wg_rows): part index = group
+    ti.g = tab[p.G] == p.G ? pidx : group_of_tile(nullptr, tab, p.G, pidx);
+    ti.part = pidx - tab[ti.g];
+    ti.nparts = tab[ti.g + 1] - tab[ti.g];
+    const int* otab = 2 * (p.G + 1) <= kTileTabInts ? tab + p.G + 1 : nullptr;
+    const int off = otab ? otab[ti.g] : __ldg(p.offsets + ti.g);
+    const int cnt = (otab ? otab[ti.g + 1] : __ldg(p.offsets + ti.g + 1)) - off;
+    ti.row0 = off + ti.part * p.wg_rows;
+    ti.nvalid = min(p.wg_rows, cnt - ti.part * p.wg_rows);
+    ti.nkb = (ti.nvalid + BK - 1) / BK;
+    ti.nk = ti.nkb * p.nslices;
   } else {
     // tile t = (group * M tiles + mt) * N tiles + nt; `tab` holds offsets here
     const int per_g = p.n_ntiles * p.n_btiles;
@@ -356,10 +378,18 @@ __device__ __forceinline__ TileInfo tile_info(const GemmParams& p, int t, const 
 // offsets follow at tab + G + 1 when both fit.
 constexpr int kPairM = 2 * BM;
 
-__device__ __forceinline__ void pair_tile_table(const GemmParams& p, int* tab, int* wsum) {
+// tab[g] = sum over groups g' < g of max(min_units, ceil(count[g'] / unit)),
+// g = 0..G, by all threads of the CTA (G + 1 <= 2 * blockDim.x); wsum holds
+// one int per warp.  The group offsets are read from `offs` (a shared-memory
+// copy, visible to every thread) or, when NULL, from global memory.
+__device__ __forceinline__ void group_units_table(const GemmParams& p, int* tab, int* wsum,
+                                                  int unit, int min_units,
+                                                  const int* offs = nullptr) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   auto tiles = [&](int g) {
-    return g < p.G ? (__ldg(p.offsets + g + 1) - __ldg(p.offsets + g) + kPairM - 1) / kPairM : 0;
+    if (g >= p.G) return 0;
+    const int c = offs ? offs[g + 1] - offs[g] : __ldg(p.offsets + g + 1) - __ldg(p.offsets + g);
+    return max(min_units, (c + unit - 1) / unit);
   };
   // thread i: groups 2i and 2i + 1 (G + 1 <= 2 * blockDim.x)
   const int g0 = 2 * static_cast<int>(threadIdx.x);
@@ -657,8 +687,9 @@ __device__ __forceinline__ void epi_lora_grid(const GemmParams& p, const TileInf
   }
 }
 
+template <bool SPLIT>
 __device__ __forceinline__ void epi_wgrad(const GemmParams& p, const TileInfo& ti, uint32_t tq,
-                                          int hf, int q, int lane, uint32_t stg) {
+                                          int hf, int q, int lane, uint32_t stg, const int* tab) {
   // columns [0,64) = A * B_hi, [64,128) = A * B_lo; this warp: n in hf*32 + [0,32)
   const int m0 = ti.mt * BM + q * 32;
   const int m = m0 + lane;
@@ -677,6 +708,40 @@ __device__ __forceinline__ void epi_wgrad(const GemmParams& p, const TileInfo& t
     }
 #pragma unroll
     for (int i = 0; i < 16; ++i) v[c0 + i] = vh[i] + vl[i];
+  }
+  if (SPLIT && ti.nparts > 1) {
+    // a group split into parts: this warp parks its part's 32 x 32 sums, and
+    // the warp that completes the set adds the parts in part order (the same
+    // sum whatever order they finish in) and stores the result
+    const int wi = hf * 4 + q;
+    auto slab = [&](int pidx) {
+      return p.wg_part +
+             ((static_cast<int64_t>(pidx) * p.n_ntiles + ti.mt) * p.n_btiles + ti.nt) * 8192 +
+             wi * 1024;
+    };
+    const int first = tab[ti.g];  // part index of the group's part 0
+    float* mine = slab(first + ti.part);
+#pragma unroll
+    for (int i = 0; i < 32; ++i) __stcg(mine + i * 32 + lane, v[i]);
+    __threadfence();
+    __syncwarp();
+    int last = 0;
+    if (lane == 0) {
+      int* c = p.wg_cnt +
+               ((static_cast<int64_t>(ti.g) * p.n_ntiles + ti.mt) * p.n_btiles + ti.nt) * 8 + wi;
+      last = atomicAdd(c, 1) == ti.nparts - 1;
+      if (last) *c = 0;  // every part has arrived: zero for the next launch
+    }
+    last = __shfl_sync(0xffffffffu, last, 0);
+    if (!last) return;
+    __threadfence();
+#pragma unroll
+    for (int i = 0; i < 32; ++i) v[i] = 0.f;
+    for (int k = 0; k < ti.nparts; ++k) {
+      const float* src = slab(first + k);
+#pragma unroll
+      for (int i = 0; i < 32; ++i) v[i] += __ldcg(src + i * 32 + lane);
+    }
   }
   if (p.transpose_out) {
     // fout[g][n][m]: consecutive lanes write consecutive m (128-byte lines)
@@ -752,6 +817,7 @@ __global__ void __launch_bounds__(kThreads, Cfg<BN, EPI, PAIR, B_MN>::kCtasPerSm
   using C = Cfg<BN, EPI, PAIR, B_MN>;
   constexpr int S = C::kStages;
   constexpr bool GRID = EPI == static_cast<int>(Epi::kLoRAGrid);
+  constexpr bool SPLIT = EPI == static_cast<int>(Epi::kWgradSplit);
   static_assert(!PAIR || (!WGRAD && !GRID), "CTA pairs serve the rows-mode tiles");
   extern __shared__ uint8_t smem_raw[];
   // 1024-byte aligned stage ring (128B swizzle atoms are 8 rows x 128 B); the
@@ -825,12 +891,28 @@ __global__ void __launch_bounds__(kThreads, Cfg<BN, EPI, PAIR, B_MN>::kCtasPerSm
   // everything above overlaps the previous kernel; from here on its outputs
   // (routing tables, permuted rows, intermediates) are read
   pdl_wait();
+  if constexpr (GRID) {
+    // side job: words a later launch expects at zero (the split weight-gradient
+    // counters), cleared by the whole grid
+    for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < p.n_zero;
+         i += static_cast<int64_t>(gridDim.x) * blockDim.x)
+      p.zero[i] = 0;
+  }
   if constexpr (PAIR) {
     // the host launches pairs only when the table fits (tab != nullptr)
-    pair_tile_table(p, tile_tab, scan_tmp);
+    group_units_table(p, tile_tab, scan_tmp, kPairM, 0);
     if (2 * (p.G + 1) <= kTileTabInts)
       for (int i = threadIdx.x; i <= p.G; i += blockDim.x)
         tile_tab[p.G + 1 + i] = __ldg(p.offsets + i);
+  } else if (SPLIT) {
+    // the host splits groups only when the table fits (tab != nullptr); the
+    // offsets, when they fit after it, are copied first and scanned from there
+    int* otab = 2 * (p.G + 1) <= kTileTabInts ? tile_tab + p.G + 1 : nullptr;
+    if (otab != nullptr) {
+      for (int i = threadIdx.x; i <= p.G; i += blockDim.x) otab[i] = __ldg(p.offsets + i);
+      __syncthreads();
+    }
+    group_units_table(p, tile_tab, scan_tmp, p.wg_rows, 1, otab);
   } else if (tab != nullptr) {
     const int32_t* src = (WGRAD || GRID) ? p.offsets : p.tile_off;
     for (int i = threadIdx.x; i <= p.G; i += blockDim.x) tile_tab[i] = __ldg(src + i);
@@ -843,7 +925,7 @@ __global__ void __launch_bounds__(kThreads, Cfg<BN, EPI, PAIR, B_MN>::kCtasPerSm
   const uint32_t tmem_base = *tmem_slot;
 
   const int num_tiles =
-      WGRAD  ? p.G * p.n_ntiles * p.n_btiles
+      WGRAD  ? (SPLIT ? tile_tab[p.G] : p.G) * p.n_ntiles * p.n_btiles
       : GRID ? min((__ldg(p.offsets + p.G) + BM - 1) / BM, p.max_tiles)
       : PAIR ? min(tile_tab[p.G] * p.n_ntiles, p.max_tiles)
              : min(__ldg(p.tile_off + p.G) * p.n_ntiles, p.max_tiles);
@@ -879,7 +961,7 @@ __global__ void __launch_bounds__(kThreads, Cfg<BN, EPI, PAIR, B_MN>::kCtasPerSm
          unit_next<GRID>(u, p, tab, num_tiles, unit_stride)) {
       const TileInfo ti = PAIR ? pair_tile_info(p, u.t, tab, crank)
                           : GRID ? grid_info(p, u.t, u.gt, u.ps, tab)
-                                 : tile_info<WGRAD>(p, u.t, tab);
+                                 : tile_info<WGRAD, true, SPLIT>(p, u.t, tab);
       if (!WGRAD && p.gather_any) lane_rows(ti.row0, ti.nvalid, 4, y);
       int cs = 0, ckc = 0;  // rows mode: slice and K offset of the next K block
       for (int kb = 0; kb < ti.nk; ++kb) {
@@ -1062,7 +1144,7 @@ __global__ void __launch_bounds__(kThreads, Cfg<BN, EPI, PAIR, B_MN>::kCtasPerSm
          unit_next<GRID>(u, p, tab, num_tiles, unit_stride), ++local) {
       const TileInfo ti = PAIR ? pair_tile_info<false>(p, u.t, tab, crank)
                           : GRID ? grid_info(p, u.t, u.gt, u.ps, tab)
-                                 : tile_info<WGRAD, WGRAD>(p, u.t, tab);
+                                 : tile_info<WGRAD, WGRAD, SPLIT>(p, u.t, tab);
       const uint32_t idesc = (GRID && ti.nx == 1) ? idesc_one : idesc_full;
       const int buf = local & 1;
       const uint32_t use = static_cast<uint32_t>(local >> 1);
@@ -1179,7 +1261,7 @@ __global__ void __launch_bounds__(kThreads, Cfg<BN, EPI, PAIR, B_MN>::kCtasPerSm
          unit_next<GRID>(u, p, tab, num_tiles, unit_stride), ++local) {
       const TileInfo ti = PAIR ? pair_tile_info(p, u.t, tab, crank)
                           : GRID ? grid_info(p, u.t, u.gt, u.ps, tab)
-                                 : tile_info<WGRAD>(p, u.t, tab);
+                                 : tile_info<WGRAD, true, SPLIT>(p, u.t, tab);
       const int buf = local & 1;
       const uint32_t use = static_cast<uint32_t>(local >> 1);
       if (!mbar_wait(tfull_bar + buf, use & 1u, abort_flag, kWaitTimeoutNs)) break;
@@ -1193,7 +1275,7 @@ __global__ void __launch_bounds__(kThreads, Cfg<BN, EPI, PAIR, B_MN>::kCtasPerSm
       if constexpr (EPI == static_cast<int>(Epi::kWgradFull)) {
         epi_wgrad_full<BN>(p, ti, tq, hf, q, lane, stg);
       } else if constexpr (WGRAD) {
-        epi_wgrad(p, ti, tq, hf, q, lane, stg);
+        epi_wgrad<SPLIT>(p, ti, tq, hf, q, lane, stg, tab);
       } else if constexpr (EPI == static_cast<int>(Epi::kSwiGLU)) {
         epi_swiglu<BN>(p, ti, tq, hf, row0, nrows, lane, stg);
       } else if constexpr (EPI == static_cast<int>(Epi::kStore)) {
@@ -1254,7 +1336,8 @@ cudaError_t launch_one(const GemmParams& p, int num_sms, cudaStream_t s) {
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            static_cast<int>(C::kSmemBytes));
   if (e != cudaSuccess) return e;
-  const int tiles = WGRAD ? p.G * p.n_ntiles * p.n_btiles : p.max_tiles;
+  constexpr bool kSplit = EPI == static_cast<int>(Epi::kWgradSplit);
+  const int tiles = (WGRAD && !kSplit) ? p.G * p.n_ntiles * p.n_btiles : p.max_tiles;
   if constexpr (PAIR) {
     // persistent pairs: as many clusters of two as can be resident at once
     // (one CTA per SM), looked up once per device
@@ -1301,11 +1384,19 @@ cudaError_t launch_gemm(const GemmShape& sh, const GemmParams& p, int num_sms, c
   constexpr int kSt = static_cast<int>(Epi::kStore);
   constexpr int kDd = static_cast<int>(Epi::kDgradDn);
   constexpr int kWg = static_cast<int>(Epi::kWgrad);
+  constexpr int kWgS = static_cast<int>(Epi::kWgradSplit);
   const int e = static_cast<int>(sh.epi);
   if (p.nslices < 1 || p.nslices > kMaxSlices) return cudaErrorInvalidValue;
   if (sh.wgrad) {
     if (p.n_btiles < 1) return cudaErrorInvalidValue;
     if (sh.BN == 128 && e == kWg) return launch_one<128, true, true, kWg>(p, num_sms, s);
+    if (sh.BN == 128 && e == kWgS) {
+      // the part table lives in shared memory; parts are whole 64-row K blocks
+      if (p.G + 1 > kTileTabInts || p.wg_rows < BK || p.wg_rows % BK != 0 || !p.wg_part ||
+          !p.wg_cnt)
+        return cudaErrorInvalidValue;
+      return launch_one<128, true, true, kWgS>(p, num_sms, s);
+    }
     if (sh.BN == 256 && e == static_cast<int>(Epi::kWgradFull))
       return launch_one<256, true, true, static_cast<int>(Epi::kWgradFull)>(p, num_sms, s);
     return cudaErrorInvalidValue;

@@ -158,6 +158,8 @@ enum class Epi : int {
   kWgradFull = 6,  // fp32 per-group full weight gradient: acc (B = one wide matrix)
   kLoRAGrid = 7,   // out0 = s*acc as a hi/lo pair (N <= 64), on the plain 128-row
                    // grid; up to two groups per pass, their B blocks stacked (BN = 128)
+  kWgradSplit = 8,  // kWgrad with groups summed in parts of wg_rows rows, the parts'
+                    // fp32 sums added in part order by the last to finish
 };
 
 constexpr int kMaxSlices = 4;
@@ -208,7 +210,13 @@ struct GemmParams {
   int64_t pair;       // element offset from the hi to the lo half of a pair buffer
   int64_t fstride;    // stride between dw partial slices, or group stride of fout
   int transpose_out;  // wgrad: write fout[g][n][m] instead of fout[g][m][n]
-  int max_tiles;      // upper bound of tiles (host-known), rows mode
+  int wg_rows;        // kWgradSplit: groups split into parts of wg_rows rows (a multiple
+                      //   of 64; the part table needs G + 1 <= kTileTabInts)
+  float* wg_part;     //   parts' sums: [part][M tile][N tile][8 warps][32 x 32] fp32
+  int* wg_cnt;        //   arrivals per [group][M tile][N tile][warp]; zero before the launch
+  int* zero;          // grid mode: n_zero words the kernel sets to 0 after its dependency
+  int64_t n_zero;     //   wait, for a later launch (the split weight-gradient counters)
+  int max_tiles;      // upper bound of tiles (host-known): rows mode, split wgrad
   int nrows;          // rows of the permuted buffers (N = T * K)
   int* status;
 };

@@ -272,7 +272,13 @@ MOE_API size_t moe_mlp_bwd_workspace_size(const moe_dims* dims);
  * (act and dh as hi/lo pairs, so the sums keep ~16-bit terms).  They need the
  * permuted rows (Xp and dYp non-NULL), else MOE_ERR_UNSUPPORTED.
  * Gradients are overwritten (not accumulated); groups with no rows get zeros.
- * ws: >= moe_mlp_bwd_workspace_size bytes of device scratch, 16-byte aligned.
+ * With a shared expert (which sees every token), the LoRA gradients of each
+ * group with more than max(1024, 1.25 x the mean group) rows are summed in
+ * parts of that many rows, and the parts' fp32 sums added in part order, so
+ * results stay bit-for-bit reproducible.
+ * ws: >= moe_mlp_bwd_workspace_size bytes of device scratch, 16-byte aligned
+ * (the dh, u and v intermediates, dw partials, and the parts' partial sums
+ * with their arrival counters, which the call zeroes on its own stream).
  * The weight-gradient GEMMs run on a second stream that the library
  * creates once per device (no device memory); it forks from `stream` after
  * their inputs exist and joins back before the call returns, so all results

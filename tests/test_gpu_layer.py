@@ -177,6 +177,13 @@ EDGE = {
                                       alpha=16),
                     lambda T, E, k, rng: np.stack([rng.choice(E, size=k, replace=False)
                                                    for _ in range(T)])),
+    # two groups far above the mean (90 % of the tokens on expert 3, and the
+    # shared expert): the LoRA weight gradients sum their rows in several
+    # parts (1024 rows each here, six per group) and add the parts in order
+    "split_groups": (synth.LayerConfig("split_groups", T=6000, d=64, f=48, E=15, k=1, r=8,
+                                       alpha=16, shared=True),
+                     lambda T, E, k, rng: np.where(rng.random((T, 1)) < 0.9, 3,
+                                                   rng.integers(0, E, size=(T, 1)))),
 }
 
 
@@ -251,9 +258,16 @@ def test_layer_full_size_sampled(name, gather):
                 assert_close_bf16(got, ref[n], "%s[g%d]" % (n, gi))
 
 
-def test_layer_deterministic_and_graph_capturable():
-    cfg = SMALL["ragged"]
-    wts, act, ids_np, w_np = make_inputs(cfg, seed=21)
+@pytest.mark.parametrize("name", ["ragged", "split_groups"])
+def test_layer_deterministic_and_graph_capturable(name):
+    if name in SMALL:
+        cfg = SMALL[name]
+        wts, act, ids_np, w_np = make_inputs(cfg, seed=21)
+    else:
+        cfg, mk = EDGE[name]
+        ids_np = mk(cfg.T, cfg.E, cfg.k, np.random.default_rng(5)).astype(np.int32)
+        w_np = synth.combine_weights(cfg.T, cfg.k, seed=9).numpy()
+        wts, act, ids_np, w_np = make_inputs(cfg, seed=21, ids=ids_np, w=w_np)
     layer, Y1, g1 = run(cfg, wts, act, ids_np, w_np)
     ids = torch.from_numpy(ids_np).to(DEV)
     w = torch.from_numpy(w_np).to(DEV)
