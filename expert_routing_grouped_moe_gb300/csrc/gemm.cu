@@ -563,15 +563,19 @@ __device__ __forceinline__ void epi_dgrad_dn(const GemmParams& p, const TileInfo
       up[4 * c] = __uint_as_float(y.x); up[4 * c + 1] = __uint_as_float(y.y);
       up[4 * c + 2] = __uint_as_float(y.z); up[4 * c + 3] = __uint_as_float(y.w);
     }
+    // Columns past f in a partial last chunk need no mask: this tile's
+    // accumulator is exactly 0 there (W_dn and A_dn columns TMA zero-fills) and
+    // the h the forward stored there is finite, so they add 0 to dot, and
+    // their dh is not stored.
     float dg[16], du[16];
 #pragma unroll
     for (int i = 0; i < 16; ++i) {
-      if (j0 + i >= f) gt[i] = up[i] = 0.f;  // columns past f of a partial chunk
       const float sg = sigmoidf_(gt[i]);
-      const float sl = gt[i] * sg;
+      const float sl = gt[i] * sg;  // silu(gate)
       dot = fmaf(sl * up[i], gr[i], dot);
       const float da = w * gr[i];
-      dg[i] = da * up[i] * sg * (1.f + gt[i] * (1.f - sg));
+      // d silu / d gate = sg (1 + gate (1 - sg)) = sg + silu (1 - sg)
+      dg[i] = (da * up[i]) * fmaf(sl, 1.f - sg, sg);
       du[i] = da * sl;
     }
     __syncwarp();
