@@ -113,6 +113,10 @@ CASES = {
     # a shared expert and rank 8
     "shared": synth.LayerConfig("shared", T=300, d=192, f=72, E=8, k=2, r=8, alpha=16,
                                 shared=True),
+    # a shared expert of 2500 rows: its LoRA weight gradients are summed in
+    # three parts of 1024 rows, through the workspace's partial sums
+    "split": synth.LayerConfig("split", T=2500, d=128, f=64, E=7, k=1, r=8, alpha=16,
+                               shared=True),
 }
 
 
