@@ -133,14 +133,18 @@ def test_full_weight_gradients_parity(name):
         assert np.all(g["dW_gu"][e].cpu().numpy() == 0) and np.all(g["dW_dn"][e].cpu().numpy() == 0)
 
 
-def test_full_weight_gradients_sampled_full_size():
-    """dW_gu / dW_dn at the Qwen3-shaped size: the largest and the smallest
-    expert, against the per-expert oracle."""
-    cfg = synth.CONFIGS["qwen3_30b_a3b"]
+@pytest.mark.parametrize("name", ["qwen3_30b_a3b", "gpt_oss_20b", "skewed_shared"])
+def test_full_weight_gradients_sampled_full_size(name):
+    """dW_gu / dW_dn at the full workload sizes (single-CTA and pair tiles,
+    d = f = 2880 against every tile width): the largest and the smallest
+    non-empty expert, and the shared expert, against the per-expert oracle."""
+    cfg = synth.CONFIGS[name]
     wts, act, ids_np, w_np = make_inputs(cfg, seed=1)
     layer, Y, g = run(cfg, wts, act, ids_np, w_np, full=True)
     counts = np.bincount(ids_np.reshape(-1), minlength=cfg.E)
-    groups = [int(np.argmax(counts)), int(np.argmin(counts))]
+    groups = [int(np.argmax(counts)), int(np.argmin(np.where(counts > 0, counts, 1 << 30)))]
+    if cfg.shared:
+        groups.append(cfg.E)
     P = oracle_params(wts, cfg, groups=groups)
     X, dY = to64(act["X"]), to64(act["dY"])
     for gi in groups:
